@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Throughput of the block-FP8 MoE layer (Drama 3 backbone shape) on GB300.
+
+One step = one pass of the whole layer (router, quantisation, schedule,
+routed experts, shared expert, combine) over one batch of synthetic rows.
+
+At N=1 the workload is the one-row decode step (T=1, H=2048, 256 experts
+top-8, I=Is=512, block-FP8 experts).  Weights are rotated over several
+independent layer instances (0.77 GiB each, far above the 129 MB L2) so no
+step finds its weights in L2.  The K timed steps run as CUDA graphs on one
+stream; CUDA events bracket them.  With torchrun (N>1) every rank runs an
+independent replica (rows are independent: weak scaling, no data-path
+collective); the slowest rank's time counts.
+
+Printed: one JSON line.  `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer rows/s"
+UNIT = "rows/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="decode_t1")
+    ap.add_argument("--instances", type=int, default=16)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---- algorithmic bytes --------------------------------------------------------
+
+def layer_bytes(s, T: int, U: int) -> int:
+    """Bytes the layer must move: touched experts' e4m3 weights and scales,
+    router, shared expert, gate vector, x and y."""
+    G = s.group
+    expert = 2 * s.inter * s.hidden + s.hidden * s.inter + \
+        4 * ((2 * s.inter // G) * (s.hidden // G) + (s.hidden // G) * (s.inter // G))
+    fixed = 4 * s.n_experts * s.hidden + 2 * (3 * s.shared_inter * s.hidden) + 2 * s.hidden
+    return U * expert + fixed + 2 * 2 * T * s.hidden
+
+
+def stage_bytes(s, T: int, U: int) -> dict:
+    G, H, I, Is, E, k = s.group, s.hidden, s.inter, s.shared_inter, s.n_experts, s.top_k
+    w13 = 2 * I * H + 4 * (2 * I // G) * (H // G)
+    w2 = H * I + 4 * (H // G) * (I // G)
+    return {
+        "router": 4 * E * H + 2 * T * H + 4 * T * E,
+        "quant_gamma": 2 * T * H + 2 * H + T * H + 4 * T * (H // G) + 4 * T,
+        "topk": 4 * T * E + 8 * T * k,
+        "schedule": 4 * T * k * 4,
+        "gateup": U * w13 + 2 * 2 * Is * H + T * H + 2 * T * H
+        + T * k * (I + 4 * (I // G)) + 2 * T * Is,
+        "down": U * w2 + 2 * H * Is + T * k * (I + 4 * (I // G)) + 2 * T * k * H + 2 * T * Is
+        + 2 * T * H,
+        "combine": 2 * T * k * H + 2 * T * H + 2 * T * H + 8 * T * k + 4 * T,
+    }
+
+
+def fp8_flops(s, T: int) -> int:
+    return 2 * T * s.top_k * (2 * s.inter * s.hidden + s.hidden * s.inter)
+
+
+# ---- clocks ------------------------------------------------------------------
+
+QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(device_index), "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def finish(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            p = [v.strip() for v in line.split(",")]
+            if len(p) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(p[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + p[0].split(".")[1]) if "." in p[0] else 0.0
+                rows.append((ts + frac, p))
+            except Exception:
+                continue
+        inside = [p for ts, p in rows if self.t0 is not None and self.t0 - 0.05 <= ts <= self.t1 + 0.05]
+        use = inside if inside else [p for _, p in rows]
+        sm = [float(p[2]) for p in use if p[2].replace(".", "").isdigit()]
+        mx = [float(p[3]) for p in use if p[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i in range(4) if p[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples_in_timed_region": len(inside),
+                "power_w_max": max((float(p[4]) for p in use
+                                    if p[4].replace(".", "").isdigit()), default=None)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def traffic_for(kernel: str, workload: str):
+    """dram bytes per launch from a committed ncu capture, if the kernel's
+    source has not changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}@{workload}")
+    if not e:
+        return None
+    src = os.path.join(ROOT, e["source"])
+    if not os.path.exists(src):
+        return None
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != e["sha256"]:
+            return None
+    return e["bytes_per_launch"]
+
+
+# ---- reference arm: the CPU oracle -----------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch  # noqa: F401
+    import oracle
+    import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    s = wl.shape
+    oracle.build()
+    x = W.make_x(s, max(wl.rows, 1), wl.seed, wl.x_kind)
+    wr = W.make_router(s, wl.seed, wl.x_kind)
+    idx = set()
+    xb = W.bf16_bits(x)
+    for r in range(xb.shape[0]):
+        idx |= set(oracle.router_row(xb[r], wr.numpy(), s.top_k)[1].tolist())
+    layer = W.to_numpy_layer(W.make_layer(s, wl.seed, wl.x_kind, experts=sorted(idx)))
+    steps = args.steps if args.steps is not None else 5
+    for _ in range(max(args.warmup, 1) if args.warmup else 0):
+        oracle.moe_rows(layer, xb[:1])
+        break
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.moe_rows(layer, xb)
+    dt = time.perf_counter() - t0
+    rows = steps * xb.shape[0]
+    value = rows / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": steps, "warmup": 1, "ms_per_step": 1e3 * dt / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "rows": wl.rows, "hidden": s.hidden,
+                   "experts": s.n_experts, "top_k": s.top_k, "inter": s.inter,
+                   "shared_inter": s.shared_inter},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{steps} full passes of the {wl.name} batch ({xb.shape[0]} rows)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---- our arm -----------------------------------------------------------------
+
+def cpu_baseline(layer_host, xb, budget_s: float):
+    import oracle
+    oracle.build()
+    rows = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        r = rows % xb.shape[0]
+        oracle.moe_rows(layer_host, xb[r:r + 1])
+        rows += 1
+    dt = time.perf_counter() - t0
+    return rows / dt, rows
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import block_fp8_mixture_router_gb300 as moe
+    import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from block_fp8_mixture_router_gb300.build import build
+    build()
+    moe.load_library()
+
+    wl = W.WORKLOADS[args.workload]
+    s = wl.shape
+    T = wl.rows
+    L = max(1, args.instances)
+    shape = moe.LayerShape(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, s.group)
+    nets, xs, ys, layers = [], [], [], []
+    for i in range(L):
+        layer = W.make_layer(s, wl.seed + 7919 * i + 104729 * rank, wl.x_kind, device=dev)
+        net = moe.MoELayer(shape, max_rows=max(T, 16), device=local)
+        net.load(layer)
+        nets.append(net)
+        xs.append(W.make_x(s, T, wl.seed + 7919 * i + 104729 * rank, wl.x_kind, device=dev))
+        ys.append(torch.empty_like(xs[-1]))
+        if i == 0:
+            layers.append(layer)
+        del layer
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    K = args.steps if args.steps is not None else 32000 // max(1, T) * 1
+    K = max(1, K)
+    Wm = max(3, args.warmup)
+
+    def step(i):
+        j = i % L
+        nets[j].forward(xs[j], ys[j], stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(Wm):
+            step(i)
+    stream.synchronize()
+
+    # graphs: one of L steps (one per instance) and one of the remainder
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                step(i)
+        return g
+
+    full, rem = divmod(K, L)
+    g_full = capture(L) if full else None
+    g_rem = capture(rem) if rem else None
+    with torch.cuda.stream(stream):
+        if g_full:
+            g_full.replay()
+        if g_rem:
+            g_rem.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark_start()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rem:
+            g_rem.replay()
+        e1.record(stream)
+    e1.synchronize()
+    if sampler:
+        sampler.mark_end()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    clocks = sampler.finish() if sampler else None
+    value = world * K * T / (ms / 1e3)
+
+    # per-kernel device times (events after every launch), same rotation
+    stage_ms = {}
+    P = min(64, max(8, L * 4))
+    for i in range(P):
+        j = i % L
+        for name, t in nets[j].profile(xs[j], ys[j], stream=stream):
+            stage_ms.setdefault(name, []).append(t)
+    stage_avg = {n: sum(v) / len(v) for n, v in stage_ms.items()}
+    launches_per_step = len(stage_avg)
+
+    # touched experts per instance
+    Us = []
+    for j in range(L):
+        idx, _ = nets[j].route(xs[j], stream=stream)
+        stream.synchronize()
+        Us.append(len(set(idx.cpu().numpy().ravel().tolist())))
+    U = sum(Us) / len(Us)
+    sb = stage_bytes(s, T, U)
+    hbm, bf16_tf, peak_kind = measured_peaks()
+    dom = max(stage_avg, key=stage_avg.get)
+    dom_gbs = sb[dom] / (stage_avg[dom] * 1e-3) / 1e9
+    lb = layer_bytes(s, T, U)
+    step_ms = ms / K
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": Wm, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": wl.name, "rows": T, "hidden": s.hidden, "experts": s.n_experts,
+                   "top_k": s.top_k, "inter": s.inter, "shared_inter": s.shared_inter,
+                   "activations": "bf16", "expert_weights": "e4m3, fp32 128x128 block scales",
+                   "layer_instances": L,
+                   "l2": f"weights rotate over {L} layer instances "
+                         f"({L * lb / 2**30:.1f} GiB touched per rotation) > 129 MB L2",
+                   "timing": "CUDA graphs of whole steps, CUDA events on the launch stream",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": hbm,
+                     "unit": "GB/s", "frac": dom_gbs / hbm, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": sb[dom],
+                     "avg_launch_us": stage_avg[dom] * 1e3,
+                     "traffic": traffic_for(dom, wl.name)},
+        "layer_roofline": {"bound": "hbm", "algorithmic_bytes_per_step": lb,
+                           "achieved": lb / (step_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                           "frac": lb / (step_ms * 1e-3) / 1e9 / hbm,
+                           "distinct_experts": U,
+                           "fp8_tflops": fp8_flops(s, T) / (step_ms * 1e-3) / 1e12},
+        "stages_us": {n: round(v * 1e3, 3) for n, v in stage_avg.items()},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clocks,
+    }
+
+    # end to end through the C ABI with host buffers (copies inside the timed region)
+    xh = [x.cpu().pin_memory() for x in xs]
+    yh = [torch.empty_like(v) for v in xh]
+    yh = [v.pin_memory() for v in yh]
+    Ke = min(K, 2000)
+    for i in range(3):
+        nets[i % L].forward_host(xh[i % L], yh[i % L], stream=stream)
+    t0 = time.perf_counter()
+    for i in range(Ke):
+        j = i % L
+        nets[j].forward_host(xh[j], yh[j], stream=stream)
+    et = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([et], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        et = float(t.item())
+    line["e2e"] = {"value": world * Ke * T / et, "unit": UNIT,
+                   "h2d_bytes_per_step": T * s.hidden * 2, "d2h_bytes_per_step": T * s.hidden * 2,
+                   "steps": Ke, "api": "moe_forward_host"}
+
+    if rank == 0 and world == 1:
+        host = W.to_numpy_layer(layers[0])
+        xb = W.bf16_bits(xs[0])
+        v, n = cpu_baseline(host, xb, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{n} single-row passes of layer instance 0 "
+                                          f"({wl.name}), {args.cpu_seconds:.0f} s budget"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for net in nets:
+        net.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

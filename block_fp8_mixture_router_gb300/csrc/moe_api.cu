@@ -1,0 +1,514 @@
+// C ABI of the block-FP8 MoE layer: context, weight loading, forward.
+//
+// Interface style follows the pages: refuse unsupported shapes when the
+// layer is opened (PR #939 section "What it adds": config.zig "checks every
+// number the kernels assume and refuses any other checkpoint shape"),
+// caller-owned buffers, an allocation cap that is checked before anything is
+// allocated (PR #925, allocation-limit commit), and named error values instead
+// of traps.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+#include <vector>
+
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+struct moe_ctx {
+  moe_config cfg;
+  int device = 0;
+  int sm_count = 0;
+  bool loaded = false;
+  int opt_path = 0;
+  int opt_pdl = 1;
+  cudaStream_t last_stream = nullptr;
+  std::vector<void*> allocs;
+  DevLayer L{};
+  DevWork w{};
+  bf16* stage_x = nullptr;
+  bf16* stage_y = nullptr;
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+bool config_supported(const moe_config* c) {
+  if (c->hidden <= 0 || c->hidden % kGroup) return false;
+  if (c->inter <= 0 || c->inter % kGroup) return false;
+  if (c->shared_inter <= 0 || c->shared_inter % kGroup) return false;
+  if (c->top_k < 1 || c->top_k > kMaxTopK) return false;
+  if (c->n_experts < c->top_k || c->n_experts > kMaxExperts) return false;
+  if (c->act_group != kGroup) return false;
+  if (c->max_rows < 1 || c->max_rows > 65536) return false;
+  if (c->hidden > 65536 || c->inter > 65536 || c->shared_inter > 65536) return false;
+  return true;
+}
+
+// Byte layout of everything a context allocates, in allocation order.
+struct Plan {
+  size_t sizes[32];
+  int n = 0;
+  size_t total = 0;
+  size_t add(size_t b) {
+    b = (b + 255) & ~(size_t)255;
+    sizes[n++] = b;
+    total += b;
+    return b;
+  }
+};
+
+Plan make_plan(const moe_config* c) {
+  Plan p;
+  const size_t H = c->hidden, E = c->n_experts, k = c->top_k, I = c->inter, Is = c->shared_inter;
+  const size_t T = c->max_rows, G = kGroup, W = (T + 31) / 32;
+  const size_t MC = (size_t)max_chunks((int)T, (int)k, (int)E);
+  // weights
+  p.add(E * 2 * I * H);                   // 0 w13
+  p.add(E * (2 * I / G) * (H / G) * 4);   // 1 s13
+  p.add(E * H * I);                       // 2 w2
+  p.add(E * (H / G) * (I / G) * 4);       // 3 s2
+  p.add(E * H * 4);                       // 4 router
+  p.add(2 * Is * H * 2);                  // 5 ws13
+  p.add(H * Is * 2);                      // 6 ws2
+  p.add(H * 2);                           // 7 gate
+  // workspace
+  p.add(T * E * 4);                       // 8 logits
+  p.add(T * k * 4);                       // 9 idx
+  p.add(T * k * 4);                       // 10 wts
+  p.add(T * H);                           // 11 xq
+  p.add(T * (H / G) * 4);                 // 12 sx
+  p.add(T * 4);                           // 13 gamma
+  p.add(E * W * 4);                       // 14 bitmap
+  p.add(E * W * 4);                       // 15 wprefix
+  p.add(E * 4);                           // 16 counts
+  p.add((E + 1) * 4);                     // 17 off
+  p.add(T * k * 4);                       // 18 pair_of_slot
+  p.add(T * k * 4);                       // 19 slot_of_pair
+  p.add(MC * 16);                         // 20 chunks
+  p.add(16);                              // 21 n_chunks
+  p.add(T * k * I * 4);                   // 22 hbuf
+  p.add(T * k * I);                       // 23 hq
+  p.add(T * k * (I / G) * 4);             // 24 sh
+  p.add(MC * (I / G) * 4);                // 25 gcount
+  p.add(T * Is * 2);                      // 26 hs
+  p.add(T * k * H * 2);                   // 27 dbuf
+  p.add(T * H * 2);                       // 28 ds
+  p.add(64);                              // 29 status + done counters
+  p.add(T * H * 2);                       // 30 stage_x
+  p.add(T * H * 2);                       // 31 stage_y
+  return p;
+}
+
+void free_all(moe_ctx* c) {
+  for (void* ptr : c->allocs) cudaFree(ptr);
+  c->allocs.clear();
+}
+
+int check_launch(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+KArgs make_args(moe_ctx* c, const void* x, void* y, int T) {
+  KArgs a;
+  a.d = Dims{T, c->cfg.hidden, c->cfg.n_experts, c->cfg.top_k, c->cfg.inter, c->cfg.shared_inter};
+  a.L = c->L;
+  a.w = c->w;
+  a.x = static_cast<const bf16*>(x);
+  a.y = static_cast<bf16*>(y);
+  return a;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const char* pa = static_cast<const char*>(a);
+  const char* pb = static_cast<const char*>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+int run_router_and_quant(moe_ctx* c, const KArgs& a, cudaStream_t s) {
+  (void)c;
+  if (launch_router(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_quant_gamma(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_topk(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+// Records an event after each launch when profiling (names/events non-null).
+struct StageRec {
+  cudaEvent_t* ev = nullptr;
+  const char** names = nullptr;
+  int cap = 0;
+  int n = 0;
+  bool mark(const char* name, cudaStream_t s) {
+    if (!ev) return true;
+    if (n >= cap) return true;
+    names[n] = name;
+    return cudaEventRecord(ev[++n], s) == cudaSuccess;
+  }
+};
+
+#define LAUNCH(expr, name)                                 \
+  do {                                                     \
+    if ((expr) != cudaSuccess) return MOE_ERR_CUDA;        \
+    if (rec && !rec->mark(name, s)) return MOE_ERR_CUDA;   \
+  } while (0)
+
+int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
+                StageRec* rec = nullptr) {
+  KArgs a = make_args(c, x, y, T);
+  const int grid = 2 * c->sm_count;
+  LAUNCH(launch_router(a, s), "router");
+  LAUNCH(launch_quant_gamma(a, s), "quant_gamma");
+  LAUNCH(launch_topk(a, s), "topk");
+  LAUNCH(launch_schedule(a, s), "schedule");
+  LAUNCH(launch_gateup(a, grid, s), "gateup");
+  LAUNCH(launch_down(a, grid, s), "down");
+  LAUNCH(launch_combine(a, s), "combine");
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_NOT_LOADED: return "weights not loaded";
+    case MOE_ERR_ALLOC_LIMIT: return "allocation would exceed the workspace cap";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int moe_required_bytes(const moe_config* cfg, size_t* bytes) {
+  if (!cfg || !bytes) return MOE_ERR_INVALID_ARG;
+  if (!config_supported(cfg)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  *bytes = make_plan(cfg).total;
+  return MOE_OK;
+}
+
+int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || device < 0) return MOE_ERR_INVALID_ARG;
+  if (!config_supported(cfg)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const Plan plan = make_plan(cfg);
+  if (cfg->workspace_cap_bytes && plan.total > cfg->workspace_cap_bytes) return MOE_ERR_ALLOC_LIMIT;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device >= ndev) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  DeviceGuard guard(device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  moe_ctx* c = new (std::nothrow) moe_ctx();
+  if (!c) return MOE_ERR_CUDA;
+  c->cfg = *cfg;
+  c->device = device;
+  if (cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+    delete c;
+    return MOE_ERR_CUDA;
+  }
+  void* ptrs[32];
+  for (int i = 0; i < plan.n; ++i) {
+    if (cudaMalloc(&ptrs[i], plan.sizes[i]) != cudaSuccess) {
+      cudaGetLastError();
+      free_all(c);
+      delete c;
+      return MOE_ERR_CUDA;
+    }
+    c->allocs.push_back(ptrs[i]);
+  }
+  c->L.w13 = (const uint8_t*)ptrs[0];
+  c->L.s13 = (const float*)ptrs[1];
+  c->L.w2 = (const uint8_t*)ptrs[2];
+  c->L.s2 = (const float*)ptrs[3];
+  c->L.wr = (const float*)ptrs[4];
+  c->L.ws13 = (const bf16*)ptrs[5];
+  c->L.ws2 = (const bf16*)ptrs[6];
+  c->L.gate = (const bf16*)ptrs[7];
+  DevWork& w = c->w;
+  w.logits = (float*)ptrs[8];
+  w.idx = (int*)ptrs[9];
+  w.wts = (float*)ptrs[10];
+  w.xq = (uint8_t*)ptrs[11];
+  w.sx = (float*)ptrs[12];
+  w.gamma = (float*)ptrs[13];
+  w.bitmap = (uint32_t*)ptrs[14];
+  w.wprefix = (int*)ptrs[15];
+  w.counts = (int*)ptrs[16];
+  w.off = (int*)ptrs[17];
+  w.pair_of_slot = (int*)ptrs[18];
+  w.slot_of_pair = (int*)ptrs[19];
+  w.chunks = (int4*)ptrs[20];
+  w.n_chunks = (int*)ptrs[21];
+  w.hbuf = (float*)ptrs[22];
+  w.hq = (uint8_t*)ptrs[23];
+  w.sh = (float*)ptrs[24];
+  w.gcount = (int*)ptrs[25];
+  w.hs = (bf16*)ptrs[26];
+  w.dbuf = (bf16*)ptrs[27];
+  w.ds = (bf16*)ptrs[28];
+  w.status = (int*)ptrs[29];
+  w.done = w.status + 4;
+  c->stage_x = (bf16*)ptrs[30];
+  c->stage_y = (bf16*)ptrs[31];
+  // counters start at zero and are reset by the kernels that use them
+  if (cudaMemset(w.gcount, 0, plan.sizes[25]) != cudaSuccess ||
+      cudaMemset(w.status, 0, plan.sizes[29]) != cudaSuccess ||
+      cudaMemset(w.n_chunks, 0, plan.sizes[21]) != cudaSuccess) {
+    free_all(c);
+    delete c;
+    return MOE_ERR_CUDA;
+  }
+  *out = c;
+  return MOE_OK;
+}
+
+int moe_load_weights(moe_ctx* c, const moe_weights* wt, int pointers_on_device, void* stream) {
+  if (!c || !wt) return MOE_ERR_INVALID_ARG;
+  if (!wt->w13 || !wt->s13 || !wt->w2 || !wt->s2 || !wt->router || !wt->ws13 || !wt->ws2 ||
+      !wt->shared_gate)
+    return MOE_ERR_INVALID_ARG;
+  if (pointers_on_device != 0 && pointers_on_device != 1) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  const Plan plan = make_plan(&c->cfg);
+  const size_t H = c->cfg.hidden, E = c->cfg.n_experts, I = c->cfg.inter,
+               Is = c->cfg.shared_inter, G = kGroup;
+  const size_t n13 = E * (2 * I / G) * (H / G), n2 = E * (H / G) * (I / G);
+  // scales must be finite and positive: check them on the host first
+  std::vector<float> s13(n13), s2(n2);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(s13.data(), wt->s13, n13 * 4, cudaMemcpyDefault, s) != cudaSuccess ||
+      cudaMemcpyAsync(s2.data(), wt->s2, n2 * 4, cudaMemcpyDefault, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  for (float v : s13)
+    if (!(v > 0.0f) || !isfinite(v)) return MOE_ERR_INVALID_ARG;
+  for (float v : s2)
+    if (!(v > 0.0f) || !isfinite(v)) return MOE_ERR_INVALID_ARG;
+  (void)plan;
+  struct Cp { void* dst; const void* src; size_t n; } cps[] = {
+      {(void*)c->L.w13, wt->w13, E * 2 * I * H},
+      {(void*)c->L.s13, wt->s13, n13 * 4},
+      {(void*)c->L.w2, wt->w2, E * H * I},
+      {(void*)c->L.s2, wt->s2, n2 * 4},
+      {(void*)c->L.wr, wt->router, E * H * 4},
+      {(void*)c->L.ws13, wt->ws13, 2 * Is * H * 2},
+      {(void*)c->L.ws2, wt->ws2, H * Is * 2},
+      {(void*)c->L.gate, wt->shared_gate, H * 2},
+  };
+  for (const Cp& cp : cps)
+    if (cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDefault, s) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+  if (cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  c->loaded = true;
+  return MOE_OK;
+}
+
+int moe_forward(moe_ctx* c, const void* x, void* y, int rows, void* stream) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (rows < 0) return MOE_ERR_INVALID_ARG;
+  if (rows > c->cfg.max_rows) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!c->loaded) return MOE_ERR_NOT_LOADED;
+  if (rows == 0) return MOE_OK;
+  if (!x || !y) return MOE_ERR_INVALID_ARG;
+  const size_t nb = (size_t)rows * c->cfg.hidden * 2;
+  if (overlaps(x, nb, y, nb)) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)x | (uintptr_t)y) & 15) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  c->last_stream = s;
+  return run_forward(c, x, y, rows, s);
+}
+
+int moe_forward_host(moe_ctx* c, const void* x_host, void* y_host, int rows, void* stream) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (rows < 0) return MOE_ERR_INVALID_ARG;
+  if (rows > c->cfg.max_rows) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!c->loaded) return MOE_ERR_NOT_LOADED;
+  if (rows == 0) return MOE_OK;
+  if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  c->last_stream = s;
+  const size_t nb = (size_t)rows * c->cfg.hidden * 2;
+  if (cudaMemcpyAsync(c->stage_x, x_host, nb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  int rc = run_forward(c, c->stage_x, c->stage_y, rows, s);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(y_host, c->stage_y, nb, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+int moe_route(moe_ctx* c, const void* x, int rows, int32_t* idx, float* w, void* stream) {
+  if (!c || rows < 0) return MOE_ERR_INVALID_ARG;
+  if (rows > c->cfg.max_rows) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!c->loaded) return MOE_ERR_NOT_LOADED;
+  if (rows == 0) return MOE_OK;
+  if (!x || !idx || !w) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  c->last_stream = s;
+  KArgs a = make_args(c, x, nullptr, rows);
+  int rc = run_router_and_quant(c, a, s);
+  if (rc) return rc;
+  const size_t n = (size_t)rows * c->cfg.top_k;
+  if (cudaMemcpyAsync(idx, c->w.idx, n * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(w, c->w.wts, n * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+int moe_quantize(moe_ctx* c, const void* x, int rows, uint8_t* codes, float* scales, void* stream) {
+  if (!c || rows < 0) return MOE_ERR_INVALID_ARG;
+  if (rows > c->cfg.max_rows) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!c->loaded) return MOE_ERR_NOT_LOADED;
+  if (rows == 0) return MOE_OK;
+  if (!x || !codes || !scales) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  c->last_stream = s;
+  KArgs a = make_args(c, x, nullptr, rows);
+  if (launch_quant_gamma(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+  const size_t H = c->cfg.hidden;
+  if (cudaMemcpyAsync(codes, c->w.xq, rows * H, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(scales, c->w.sx, rows * (H / kGroup) * 4, cudaMemcpyDeviceToDevice, s) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+int moe_expert_activations(moe_ctx* c, int rows, uint8_t* hq, float* sh, void* stream) {
+  if (!c || rows < 0) return MOE_ERR_INVALID_ARG;
+  if (rows > c->cfg.max_rows) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!c->loaded) return MOE_ERR_NOT_LOADED;
+  if (rows == 0) return MOE_OK;
+  if (!hq || !sh) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  KArgs a = make_args(c, nullptr, nullptr, rows);
+  return check_launch(launch_gather_hq(a, hq, sh, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_profile_forward(moe_ctx* c, const void* x, void* y, int rows, float* stage_ms,
+                        const char** stage_names, int capacity, int* n_stages, void* stream) {
+  if (!c || !stage_ms || !stage_names || !n_stages || capacity < 1) return MOE_ERR_INVALID_ARG;
+  *n_stages = 0;
+  if (rows < 0) return MOE_ERR_INVALID_ARG;
+  if (rows > c->cfg.max_rows) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!c->loaded) return MOE_ERR_NOT_LOADED;
+  if (rows == 0) return MOE_OK;
+  if (!x || !y) return MOE_ERR_INVALID_ARG;
+  const size_t nb = (size_t)rows * c->cfg.hidden * 2;
+  if (overlaps(x, nb, y, nb)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  c->last_stream = s;
+  const int kMaxStages = 16;
+  cudaEvent_t ev[kMaxStages + 1];
+  int made = 0;
+  int rc = MOE_OK;
+  for (; made <= kMaxStages; ++made)
+    if (cudaEventCreate(&ev[made]) != cudaSuccess) {
+      rc = MOE_ERR_CUDA;
+      break;
+    }
+  StageRec rec;
+  if (rc == MOE_OK) {
+    rec.ev = ev;
+    rec.names = stage_names;
+    rec.cap = capacity < kMaxStages ? capacity : kMaxStages;
+    if (cudaEventRecord(ev[0], s) != cudaSuccess) rc = MOE_ERR_CUDA;
+  }
+  if (rc == MOE_OK) rc = run_forward(c, x, y, rows, s, &rec);
+  if (rc == MOE_OK && cudaEventSynchronize(ev[rec.n]) != cudaSuccess) rc = MOE_ERR_CUDA;
+  if (rc == MOE_OK) {
+    for (int i = 0; i < rec.n; ++i)
+      if (cudaEventElapsedTime(&stage_ms[i], ev[i], ev[i + 1]) != cudaSuccess) rc = MOE_ERR_CUDA;
+    *n_stages = rec.n;
+  }
+  for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);
+  if (rc != MOE_OK) cudaGetLastError();
+  return rc;
+}
+
+int moe_set_option(moe_ctx* c, int option, int value) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  switch (option) {
+    case MOE_OPT_PATH:
+      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+      c->opt_path = value;
+      return MOE_OK;
+    case MOE_OPT_PDL:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      c->opt_pdl = value;
+      return MOE_OK;
+    default:
+      return MOE_ERR_INVALID_ARG;
+  }
+}
+
+int moe_last_device_status(moe_ctx* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  int flag = 0;
+  if (cudaStreamSynchronize(c->last_stream) != cudaSuccess ||
+      cudaMemcpy(&flag, c->w.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(c->w.status, 0, 4) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return flag ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+}
+
+void moe_destroy(moe_ctx* c) {
+  if (!c) return;
+  {
+    DeviceGuard guard(c->device);
+    cudaDeviceSynchronize();
+    free_all(c);
+  }
+  delete c;
+}
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// Internal declarations shared by the kernels and the C-ABI host code.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int kGroup = 128;       // activation group = weight block edge
+constexpr int kChunk = 16;        // tokens per expert chunk (two n8 MMA tiles)
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 16;
+constexpr int kDecodeRows = 16;   // rows at or below which the decode kernels run
+
+struct Dims {
+  int T, H, E, k, I, Is;
+};
+
+// Device copies of the weights (context-owned).
+struct DevLayer {
+  const uint8_t* w13;  // e4m3 [E][2I][H]
+  const float* s13;    // [E][2I/128][H/128]
+  const uint8_t* w2;   // e4m3 [E][H][I]
+  const float* s2;     // [E][H/128][I/128]
+  const float* wr;     // fp32 [E][H]
+  const bf16* ws13;    // [2Is][H]
+  const bf16* ws2;     // [H][Is]
+  const bf16* gate;    // [H]
+};
+
+// Workspace (context-owned, sized for max_rows).
+struct DevWork {
+  float* logits;        // [T][E]
+  int* idx;             // [T][k]
+  float* wts;           // [T][k]
+  uint8_t* xq;          // [T][H]
+  float* sx;            // [T][H/128]
+  float* gamma;         // [T]
+  uint32_t* bitmap;     // [E][ceil(T/32)]
+  int* wprefix;         // [E][ceil(T/32)]
+  int* counts;          // [E]
+  int* off;             // [E+1]
+  int* pair_of_slot;    // [T*k]  slot order = (expert, row)
+  int* slot_of_pair;    // [T*k]
+  int4* chunks;         // [max_chunks] {expert, first slot, tokens, 0}
+  int* n_chunks;        // [1]
+  float* hbuf;          // [T*k][I]  SwiGLU rows before re-quantisation
+  uint8_t* hq;          // [T*k][I]  by slot
+  float* sh;            // [T*k][I/128]
+  int* gcount;          // [max_chunks][I/128] arrival counters (self-resetting)
+  bf16* hs;             // [T][Is]
+  bf16* dbuf;           // [T*k][H] by slot
+  bf16* ds;             // [T][H]
+  int* status;          // [1] device status flag
+  int* done;            // [4] arrival counters of last-block patterns (self-resetting)
+};
+
+struct KArgs {
+  Dims d;
+  DevLayer L;
+  DevWork w;
+  const bf16* x;
+  bf16* y;
+};
+
+// Upper bound of sum_e ceil(count_e / kChunk) over experts with sum_e count_e = T*k.
+inline int max_chunks(int T, int k, int E) { return (T * k + kChunk - 1) / kChunk + E; }
+
+// Launchers (return cudaGetLastError()).
+cudaError_t launch_router(const KArgs& a, cudaStream_t s);
+cudaError_t launch_quant_gamma(const KArgs& a, cudaStream_t s);
+cudaError_t launch_topk(const KArgs& a, cudaStream_t s);
+cudaError_t launch_schedule(const KArgs& a, cudaStream_t s);
+cudaError_t launch_gateup(const KArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down(const KArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_combine(const KArgs& a, cudaStream_t s);
+cudaError_t launch_gather_hq(const KArgs& a, uint8_t* hq, float* sh, cudaStream_t s);
+
+}  // namespace moe

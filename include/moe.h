@@ -1,0 +1,170 @@
+/*
+ * block_fp8_moe: the block-FP8 mixture-of-experts layer of the Drama 3 backbone
+ * on one GB300 (sm_103a), as a C ABI.
+ *
+ * The layer (PR #925/#920/#927, commit "the Drama 3 text backbone"; PR #939
+ * "Fish Audio Drama 3 text to speech on one CUDA GPU", section "Precision"):
+ *
+ *   y[t] = sum_{j<k} w[t,j] * E_{idx[t,j]}(x[t]) + sigmoid(x[t] . g) * S(x[t])
+ *
+ *   - router: logits = x . Wr^T in fp32; the k largest (ties to the lower
+ *     expert index, as the tie seen in section "Fidelity against the PyTorch
+ *     oracle" of PR #939 requires a rule); w = softmax over the k selected
+ *     logits (= fp32 softmax renormalised over the selection);
+ *   - E_e: a SwiGLU expert with e4m3 weights and one fp32 scale per 128x128
+ *     block.  Its inputs are quantised dynamically per row and per 128 inputs
+ *     (scale = amax / 448, round to nearest even, saturating), its gate/up
+ *     outputs are rounded to bf16, SwiGLU is taken in fp32 and re-quantised
+ *     the same way for the down projection (commit "one SwiGLU launch for the
+ *     routed and shared experts": routed rows are stored as their FP8
+ *     quantisation), and its output is rounded to bf16;
+ *   - S: the shared SwiGLU expert with bf16 weights, outputs rounded to bf16;
+ *   - combine in fp32, routed terms in rank order then the shared term, one
+ *     rounding to bf16 (commit "MoE combine on 8-wide vectors": every sum
+ *     keeps its order).
+ *
+ * Conventions for every call:
+ *   - Return value: MOE_OK (0) or one of the negative MOE_ERR_* codes below;
+ *     no call aborts, traps or prints.
+ *   - Tensors are dense row-major with the innermost dimension last.  bf16
+ *     values are passed as their 16-bit patterns (uint16_t), e4m3 values as
+ *     their 8-bit codes (OCP E4M3).
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream.  Calls marked "asynchronous" only enqueue work on it.
+ *   - A context is used by one stream at a time; contexts are independent.
+ */
+#ifndef BLOCK_FP8_MOE_H
+#define BLOCK_FP8_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,       /* null pointer, negative size, aliasing, bad option */
+  MOE_ERR_UNSUPPORTED_SHAPE = -2, /* a config the kernels do not assume, or rows > max_rows */
+  MOE_ERR_NOT_LOADED = -3,        /* forward/route before moe_load_weights succeeded */
+  MOE_ERR_ALLOC_LIMIT = -4,       /* weights + workspace would exceed workspace_cap_bytes */
+  MOE_ERR_CUDA = -5,              /* a CUDA runtime call failed (no device, OOM, launch) */
+  MOE_ERR_DEVICE_TIMEOUT = -6     /* a bounded device-side wait gave up (see moe_last_device_status) */
+};
+
+typedef struct moe_ctx moe_ctx; /* opaque: owns the device weights and workspace */
+
+/* Layer shape.  Supported: hidden % 128 == 0, inter % 128 == 0,
+ * shared_inter % 128 == 0, 1 <= top_k <= 16, top_k <= n_experts <= 256,
+ * act_group == 128, 1 <= max_rows <= 65536.  The Drama 3 layer is
+ * hidden 2048, 256 experts, top-8, inter 512, shared_inter 512. */
+typedef struct {
+  int hidden;          /* H */
+  int n_experts;       /* E */
+  int top_k;           /* k */
+  int inter;           /* I: routed SwiGLU width */
+  int shared_inter;    /* Is: shared SwiGLU width */
+  int act_group;       /* activation quantisation group = weight block edge (128) */
+  int max_rows;        /* largest T one forward accepts; sizes the workspace */
+  size_t workspace_cap_bytes; /* 0 = no cap; else weights + workspace must fit */
+} moe_config;
+
+/* Weights of one layer, as a block-FP8 checkpoint stores them ("weights load
+ * as stored; nothing is requantized").  All pointers are read only during
+ * moe_load_weights and stay owned by the caller.
+ *   w13    e4m3 [E][2I][H]  rows 0..I-1 are the gate projection, I..2I-1 up
+ *   s13    fp32 [E][2I/128][H/128]  one scale per 128x128 block of w13
+ *   w2     e4m3 [E][H][I]   down projection
+ *   s2     fp32 [E][H/128][I/128]
+ *   router fp32 [E][H]
+ *   ws13   bf16 [2Is][H]    shared expert gate (rows 0..Is-1) and up
+ *   ws2    bf16 [H][Is]     shared expert down
+ *   shared_gate bf16 [H]    gate vector g of the shared expert */
+typedef struct {
+  const uint8_t* w13;
+  const float* s13;
+  const uint8_t* w2;
+  const float* s2;
+  const float* router;
+  const uint16_t* ws13;
+  const uint16_t* ws2;
+  const uint16_t* shared_gate;
+} moe_weights;
+
+/* Validate `cfg`, select `device`, allocate the weight buffers and the
+ * workspace for cfg->max_rows rows.  Refuses unsupported shapes
+ * (MOE_ERR_UNSUPPORTED_SHAPE) and sizes above the cap (MOE_ERR_ALLOC_LIMIT)
+ * before allocating anything.  On success *out owns everything; on failure
+ * *out is NULL and nothing is left allocated.  Synchronous. */
+int moe_create(const moe_config* cfg, int device, moe_ctx** out);
+
+/* Copy one layer's weights into the context (layout described in
+ * moe_weights).  pointers_on_device = 1: device pointers; 0: host pointers
+ * (pageable or pinned).  Checks the block scales are finite and positive;
+ * returns after the copies have completed (synchronous on `stream`). */
+int moe_load_weights(moe_ctx* ctx, const moe_weights* w, int pointers_on_device, void* stream);
+
+/* y = MoE(x).  x: bf16 [rows][H] on the device; y: bf16 [rows][H] on the
+ * device; x and y must not overlap.  0 <= rows <= max_rows; rows == 0 does
+ * nothing.  Asynchronous on `stream`: no allocation, no host synchronisation,
+ * expert counts stay on the device.  Results are bitwise identical from run
+ * to run for the same inputs.  Device-side faults of earlier work surface as
+ * MOE_ERR_CUDA on a later call. */
+int moe_forward(moe_ctx* ctx, const void* x, void* y, int rows, void* stream);
+
+/* The same layer with x and y in host memory: copies x to the device, runs
+ * moe_forward, copies y back and synchronises `stream` before returning.
+ * Pinned host buffers give the fastest copies. */
+int moe_forward_host(moe_ctx* ctx, const void* x_host, void* y_host, int rows, void* stream);
+
+/* Router only (same kernels as moe_forward): idx int32 [rows][k] in rank
+ * order and w fp32 [rows][k], both device pointers.  Asynchronous. */
+int moe_route(moe_ctx* ctx, const void* x, int rows, int32_t* idx, float* w, void* stream);
+
+/* Activation quantisation only (same kernel as moe_forward): codes e4m3
+ * [rows][H] and scales fp32 [rows][H/128], both device pointers.
+ * Asynchronous. */
+int moe_quantize(moe_ctx* ctx, const void* x, int rows, uint8_t* codes, float* scales,
+                 void* stream);
+
+/* Expert-side intermediates of the most recent moe_forward, for checking:
+ * hq e4m3 [rows][k][I] and sh fp32 [rows][k][I/128] (the re-quantised SwiGLU
+ * rows fed to each selected expert's down projection, in rank order), device
+ * pointers.  Asynchronous; call on the stream of that forward. */
+int moe_expert_activations(moe_ctx* ctx, int rows, uint8_t* hq, float* sh, void* stream);
+
+/* Options.  MOE_OPT_PATH: 0 = automatic (rows <= 16 decode kernels, else
+ * the grouped prompt kernels), 1 = always decode kernels (rows <= 16 only),
+ * 2 = always grouped prompt kernels.  MOE_OPT_PDL: 1 = chain the decode
+ * kernels with programmatic dependent launch (default), 0 = plain launches. */
+enum { MOE_OPT_PATH = 1, MOE_OPT_PDL = 2 };
+int moe_set_option(moe_ctx* ctx, int option, int value);
+
+/* One forward like moe_forward, timed per kernel: a CUDA event is recorded
+ * after every launch on `stream` and the call waits for them.  On return
+ * stage_ms[i] is the device time of the i-th launch and stage_names[i] a
+ * static name, for i < *n_stages (at most `capacity`).  Synchronous; for
+ * measurement only (the events add small gaps between launches). */
+int moe_profile_forward(moe_ctx* ctx, const void* x, void* y, int rows, float* stage_ms,
+                        const char** stage_names, int capacity, int* n_stages, void* stream);
+
+/* Bytes moe_create would allocate for `cfg` (weights + workspace + staging). */
+int moe_required_bytes(const moe_config* cfg, size_t* bytes);
+
+/* Device-side status of the context: MOE_OK, or MOE_ERR_DEVICE_TIMEOUT if a
+ * bounded wait in an earlier forward gave up.  Synchronises the context's
+ * last stream.  Reading clears the flag. */
+int moe_last_device_status(moe_ctx* ctx);
+
+/* Release everything the context owns.  NULL is accepted. */
+void moe_destroy(moe_ctx* ctx);
+
+/* Static text for a status code. */
+const char* moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BLOCK_FP8_MOE_H */

@@ -1,0 +1,62 @@
+"""The C-ABI library loads on a host without a GPU and exports every entry
+point include/moe.h declares; shape refusal needs no device."""
+import os
+import re
+
+import pytest
+
+import block_fp8_mixture_router_gb300 as moe
+from block_fp8_mixture_router_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return moe.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(moe.EXPORTED)
+
+
+def test_refusals_without_a_device(lib):
+    ok = moe.moe_config(2048, 256, 8, 512, 512, 128, 1024, 0)
+    rc, n = moe.moe_required_bytes(ok)
+    assert rc == moe.MOE_OK and n > 768 << 20
+    bad = [moe.moe_config(2000, 256, 8, 512, 512, 128, 16, 0),
+           moe.moe_config(2048, 256, 8, 500, 512, 128, 16, 0),
+           moe.moe_config(2048, 256, 8, 512, 100, 128, 16, 0),
+           moe.moe_config(2048, 257, 8, 512, 512, 128, 16, 0),
+           moe.moe_config(2048, 4, 8, 512, 512, 128, 16, 0),
+           moe.moe_config(2048, 256, 0, 512, 512, 128, 16, 0),
+           moe.moe_config(2048, 256, 17, 512, 512, 128, 16, 0),
+           moe.moe_config(2048, 256, 8, 512, 512, 2048, 16, 0),
+           moe.moe_config(2048, 256, 8, 512, 512, 128, 0, 0),
+           moe.moe_config(2048, 256, 8, 512, 512, 128, 65537, 0)]
+    for cfg in bad:
+        rc, h = moe.moe_create(cfg, 0)
+        assert rc == moe.MOE_ERR_UNSUPPORTED_SHAPE and not h.value
+        assert moe.moe_required_bytes(cfg)[0] == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    capped = moe.moe_config(2048, 256, 8, 512, 512, 128, 1024, 1 << 20)
+    rc, h = moe.moe_create(capped, 0)
+    assert rc == moe.MOE_ERR_ALLOC_LIMIT and not h.value
+    assert moe.moe_create(ok, -1)[0] == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_forward(None, None, None, 1, 0) == moe.MOE_ERR_INVALID_ARG
+    moe.moe_destroy(None)
+    assert moe.status_string(moe.MOE_ERR_DEVICE_TIMEOUT) == "device-side wait timed out"

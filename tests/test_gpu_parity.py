@@ -1,0 +1,194 @@
+"""CUDA path against the CPU oracle, through the C ABI (needs a GB300)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from parity import bits, check_output, check_topk
+
+pytestmark = pytest.mark.gpu
+
+m = pytest.importorskip("block_fp8_mixture_router_gb300")
+
+
+def _shape(s: W.MoEShape) -> "m.LayerShape":
+    return m.LayerShape(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, s.group)
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    m.load_library()
+    return torch.device("cuda", 0)
+
+
+class Case:
+    """A layer built on the GPU, loaded into a context, plus its host copy."""
+
+    def __init__(self, wl: W.Workload, max_rows: int, dev, layer_idx: int = 0):
+        self.wl = wl
+        self.shape = wl.shape
+        seed = W.layer_seed(wl, layer_idx)
+        self.layer = W.make_layer(wl.shape, seed, wl.x_kind, device=dev)
+        self.moe = m.MoELayer(_shape(wl.shape), max_rows=max_rows)
+        self.moe.load(self.layer)
+        self._host = None
+        self.seed = seed
+
+    @property
+    def host(self):
+        if self._host is None:
+            self._host = W.to_numpy_layer(self.layer)
+        return self._host
+
+    def x(self, rows, tag="x"):
+        return W.make_x(self.shape, rows, self.seed, self.wl.x_kind, device="cuda", tag=tag)
+
+
+def run_and_check(case: Case, x: torch.Tensor, sample_rows=None, path=m.PATH_AUTO):
+    case.moe.set_option(m.MOE_OPT_PATH, path)
+    y = case.moe.forward(x)
+    idx, w = case.moe.route(x)
+    codes, scales = case.moe.quantize(x)
+    torch.cuda.synchronize()
+    rows = np.arange(x.shape[0]) if sample_rows is None else np.asarray(sample_rows)
+    xb = bits(x)[rows]
+    ref = oracle.moe_rows(case.host, xb, trace=True)
+    near, differ = check_topk(idx.cpu().numpy()[rows], ref.trace["logits"], case.shape.top_k)
+    assert differ.sum() <= max(1, 0.02 * rows.size), f"{differ.sum()} rows routed differently"
+    exact = ~differ
+    assert np.array_equal(codes.cpu().numpy()[rows], ref.trace["xq"])
+    assert np.array_equal(scales.cpu().numpy()[rows], ref.trace["sx"])
+    wg = w.cpu().numpy()[rows]
+    assert np.allclose(wg[exact], ref.trace["w"][exact], rtol=2e-5, atol=1e-7)
+    rel, mx = check_output(bits(y)[rows], ref.y_ref, rows_mask=exact)
+    return y, ref, rel, mx
+
+
+# ---- the tiny layer (H=256, 16 experts top-4, I=Is=128) ----------------------
+
+@pytest.mark.parametrize("rows", [1, 4, 5, 16, 17, 40])
+def test_tiny_layer(dev, rows):
+    case = Case(W.WORKLOADS["tiny_t4"], 64, dev)
+    x = case.x(rows)
+    _, ref, rel, mx = run_and_check(case, x)
+    # intermediates: re-quantised SwiGLU codes mostly identical (not gated by the bar)
+    hq, sh = case.moe.expert_activations(rows)
+    same = np.mean(hq.cpu().numpy() == ref.trace["hq"])
+    assert same > 0.98, same
+
+
+def test_tiny_layer_paths_agree(dev):
+    case = Case(W.WORKLOADS["tiny_t4"], 64, dev)
+    x = case.x(4)
+    y_auto, *_ = run_and_check(case, x, path=m.PATH_AUTO)
+    y_prompt, *_ = run_and_check(case, x, path=m.PATH_PROMPT)
+    assert y_auto.shape == y_prompt.shape
+
+
+# ---- full-width layers --------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def full_case(dev):
+    return Case(W.WORKLOADS["decode_t1"], 1024, dev)
+
+
+def test_decode_t1(full_case):
+    x = full_case.x(1)
+    run_and_check(full_case, x)
+
+
+def test_decode_t1_many_rows_one_by_one(full_case):
+    x = full_case.x(8, tag="many")
+    for r in range(8):
+        run_and_check(full_case, x[r:r + 1].contiguous())
+
+
+def test_decode_t11(dev):
+    case = Case(W.WORKLOADS["decode_t11"], 64, dev)
+    x = case.x(11)
+    run_and_check(case, x)
+    idx, _ = case.moe.route(x)
+    distinct = len(set(idx.cpu().numpy().ravel().tolist()))
+    assert distinct < 11 * 8, "rows were meant to share experts"
+
+
+@pytest.mark.parametrize("rows", [2, 4, 16, 17, 64, 255])
+def test_ragged_rows(full_case, rows):
+    x = full_case.x(rows, tag=f"r{rows}")
+    sample = sorted(set([0, rows - 1] + list(range(0, rows, max(1, rows // 6)))))
+    run_and_check(full_case, x, sample_rows=sample)
+
+
+def test_prompt_t1024_sampled(dev):
+    wl = W.WORKLOADS["prompt_t1024"]
+    case = Case(wl, 1024, dev)
+    x = case.x(1024)
+    idx, _ = case.moe.route(x)
+    counts = np.bincount(idx.cpu().numpy().ravel(), minlength=256)
+    assert counts.max() > 100 and (counts == 0).sum() >= 1, counts
+    sample = sorted(set([0, 1, 511, 1022, 1023] + list(range(7, 1024, 97))))
+    run_and_check(case, x, sample_rows=sample)
+    # every row's codes and scales, bit-exact, against the oracle's quantiser
+    codes, scales = case.moe.quantize(x)
+    xb = bits(x)
+    xf = torch.from_numpy(xb.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
+    for r in range(0, 1024, 64):
+        c, s = oracle.quant_row(xf[r])
+        assert np.array_equal(codes[r].cpu().numpy(), c) and np.array_equal(scales[r].cpu().numpy(), s)
+
+
+def test_repeat_bitwise(full_case):
+    for rows in (1, 11, 300):
+        x = full_case.x(rows, tag=f"rep{rows}")
+        ys = [full_case.moe.forward(x).clone() for _ in range(5)]
+        torch.cuda.synchronize()
+        for y in ys[1:]:
+            assert torch.equal(y.view(torch.int16), ys[0].view(torch.int16))
+
+
+def test_forward_host_matches_device(full_case):
+    x = full_case.x(3, tag="host")
+    y_dev = full_case.moe.forward(x)
+    xh = x.cpu().pin_memory()
+    y_host = full_case.moe.forward_host(xh)
+    torch.cuda.synchronize()
+    assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
+
+
+# ---- boundary behaviour ------------------------------------------------------
+
+def test_errors(full_case, dev):
+    ctx = full_case.moe.ctx
+    x = full_case.x(2, tag="err")
+    y = torch.empty_like(x)
+    assert m.moe_forward(ctx, x, y, 0) == m.MOE_OK
+    assert m.moe_forward(ctx, x, y, -1) == m.MOE_ERR_INVALID_ARG
+    assert m.moe_forward(ctx, x, y, 1025) == m.MOE_ERR_UNSUPPORTED_SHAPE
+    assert m.moe_forward(ctx, x, x, 2) == m.MOE_ERR_INVALID_ARG
+    assert m.moe_forward(ctx, None, y, 2) == m.MOE_ERR_INVALID_ARG
+    fresh = m.MoELayer(_shape(W.TINY), max_rows=4)
+    xt = torch.zeros((1, 256), dtype=torch.bfloat16, device=dev)
+    assert m.moe_forward(fresh.ctx, xt, torch.empty_like(xt), 1) == m.MOE_ERR_NOT_LOADED
+    cfg = m.moe_config(2048, 256, 8, 512, 512, 128, 1024, 1 << 20)
+    rc, h = m.moe_create(cfg, 0)
+    assert rc == m.MOE_ERR_ALLOC_LIMIT and not h.value
+    for bad in (m.moe_config(2000, 256, 8, 512, 512, 128, 16, 0),
+                m.moe_config(2048, 256, 8, 500, 512, 128, 16, 0),
+                m.moe_config(2048, 300, 8, 512, 512, 128, 16, 0),
+                m.moe_config(2048, 4, 8, 512, 512, 128, 16, 0),
+                m.moe_config(2048, 256, 8, 512, 512, 64, 16, 0)):
+        rc, h = m.moe_create(bad, 0)
+        assert rc == m.MOE_ERR_UNSUPPORTED_SHAPE and not h.value
+    assert m.moe_last_device_status(ctx) == m.MOE_OK
+    fresh.close()
+
+
+def test_max_rows(dev):
+    case = Case(W.WORKLOADS["tiny_t4"], 1024, dev)
+    x = case.x(1024, tag="max")
+    run_and_check(case, x, sample_rows=[0, 333, 1023])
