@@ -67,15 +67,23 @@ def stage_bytes(s, T: int, U: int) -> dict:
     G, H, I, Is, E, k = s.group, s.hidden, s.inter, s.shared_inter, s.n_experts, s.top_k
     w13 = 2 * I * H + 4 * (2 * I // G) * (H // G)
     w2 = H * I + 4 * (H // G) * (I // G)
+    gateup = U * w13 + 2 * 2 * Is * H + T * H + 2 * T * H + T * k * (I + 4 * (I // G)) + 2 * T * Is
+    down = U * w2 + 2 * H * Is + T * k * (I + 4 * (I // G)) + 2 * T * Is
     return {
+        # decode path: one persistent kernel for the whole layer
+        "decode_layer": layer_bytes(s, T, U),
+        # decode path, chained variant (three kernels)
+        "route_decode": 4 * E * H + 2 * T * H + 4 * T * E + T * H + 4 * T * (H // G) + 2 * H
+        + 8 * T * k,
+        "gateup_decode": gateup,
+        "down_combine_decode": down + 8 * T * k + 4 * T + 2 * T * H,
+        # prompt path
         "router": 4 * E * H + 2 * T * H + 4 * T * E,
         "quant_gamma": 2 * T * H + 2 * H + T * H + 4 * T * (H // G) + 4 * T,
         "topk": 4 * T * E + 8 * T * k,
         "schedule": 4 * T * k * 4,
-        "gateup": U * w13 + 2 * 2 * Is * H + T * H + 2 * T * H
-        + T * k * (I + 4 * (I // G)) + 2 * T * Is,
-        "down": U * w2 + 2 * H * Is + T * k * (I + 4 * (I // G)) + 2 * T * k * H + 2 * T * Is
-        + 2 * T * H,
+        "gateup": gateup,
+        "down": down + 2 * T * k * H + 2 * T * H,
         "combine": 2 * T * k * H + 2 * T * H + 2 * T * H + 8 * T * k + 4 * T,
     }
 

@@ -1,0 +1,305 @@
+// Decode path (rows <= 16): router + top-k + schedule in one launch, and the
+// down projections fused with the combine.  With the gate/up kernel between
+// them the layer is three launches chained by programmatic dependent launch.
+//
+// Chaining and prefetch follow PR #927 "backbone chain launches with PDL"
+// (section "What this changes": kernels wait before touching their
+// predecessor's data; immutable weights may be fetched before the wait).  The
+// one-row layer is bound by reading weights, so every kernel starts the
+// weight traffic it can before it waits: the router kernel fetches its router
+// rows and asks L2 for the shared expert, the gate/up kernel asks L2 for the
+// selected experts' down weights, and the layer's HBM reads overlap the
+// launch and dependency latencies.
+//
+// Router and top-k: PR #939 "Fish Audio Drama 3 text to speech on one CUDA
+// GPU", sections "What it adds" (the router in drama3.cu) and "Fidelity
+// against the PyTorch oracle" (near-tied 8th/9th experts: ties go to the
+// lower index).  Combine: commit "MoE combine on 8-wide vectors" (every sum
+// keeps its order: routed terms in rank order, then the shared term).
+#include <math.h>
+
+#include "moe_rowops.cuh"
+
+namespace moe {
+
+namespace {
+
+// Block-wide exclusive prefix sum over 256 threads (one value each).
+__device__ int block_exscan256(int v, int* total, int* scratch /*[8]*/) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) scratch[warp] = inc;
+  __syncthreads();
+  int base = 0, all = 0;
+  for (int w = 0; w < 8; ++w) {
+    if (w < warp) base += scratch[w];
+    all += scratch[w];
+  }
+  __syncthreads();
+  *total = all;
+  return base + inc - v;
+}
+
+// The last router CTA: top-k per row, then the schedule in the layout the
+// expert kernels read (slots sorted by (expert, row); one chunk per selected
+// expert, since an expert holds at most 16 rows here).
+__device__ void decode_schedule(const KArgs& a) {
+  __shared__ int s_idx[kDecodeRows * kMaxTopK];
+  __shared__ uint32_t s_tok[kMaxExperts];
+  __shared__ int s_scan[8];
+  const int T = a.d.T, k = a.d.k, E = a.d.E;
+  const int warp = threadIdx.x >> 5;
+  for (int t = warp; t < T; t += 8)
+    topk_row(a.w.logits + (size_t)t * E, E, k, a.w.idx + (size_t)t * k, a.w.wts + (size_t)t * k);
+  for (int e = threadIdx.x; e < kMaxExperts; e += blockDim.x) s_tok[e] = 0u;
+  __threadfence_block();
+  __syncthreads();
+  for (int p = threadIdx.x; p < T * k; p += blockDim.x) {
+    const int e = a.w.idx[p];
+    s_idx[p] = e;
+    atomicOr(&s_tok[e], 1u << (p / k));
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const uint32_t mask = e < E ? s_tok[e] : 0u;
+  const int cnt = __popc(mask);
+  int n_slots, n_used;
+  const int slot0 = block_exscan256(cnt, &n_slots, s_scan);
+  const int u = block_exscan256(cnt > 0 ? 1 : 0, &n_used, s_scan);
+  if (cnt > 0) {
+    a.w.chunks[u] = make_int4(e, slot0, cnt, 0);
+    uint32_t m = mask;
+    for (int r = 0; m; ++r) {
+      const int t = __ffs(m) - 1;
+      m &= m - 1;
+      int j = 0;
+      while (s_idx[t * k + j] != e) ++j;
+      const int p = t * k + j, slot = slot0 + r;
+      a.w.pair_of_slot[slot] = p;
+      a.w.slot_of_pair[p] = slot;
+    }
+  }
+  if (e < E) a.w.counts[e] = cnt;
+  if (threadIdx.x == 0) *a.w.n_chunks = n_used;
+}
+
+}  // namespace
+
+// ---- D1: router logits, x quantisation, top-k, schedule ---------------------
+// CTAs [0, n_router): two experts each; warp w covers expert 2b + w/4 over the
+// K quarter w%4.  CTAs [n_router, n_router + T): one row's quantisation and
+// shared gate.  The last router CTA to finish builds the schedule.
+__global__ void __launch_bounds__(256) k_route_decode(KArgs a) {
+  __shared__ float red[8][kDecodeRows];
+  __shared__ int s_last;
+  const int T = a.d.T, H = a.d.H, E = a.d.E;
+  const int n_router = (E + 1) / 2;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  // immutable weights first: ask L2 for this CTA's share of the shared expert
+  if (threadIdx.x == 0) {
+    const size_t b13 = (size_t)2 * a.d.Is * H * 2, b2 = (size_t)H * a.d.Is * 2;
+    prefetch_l2_share(a.L.ws13, b13, blockIdx.x, gridDim.x);
+    prefetch_l2_share(a.L.ws2, b2, blockIdx.x, gridDim.x);
+  }
+  if (blockIdx.x >= n_router) {
+    pdl_wait();
+    pdl_trigger();
+    quant_row_and_gate(a, blockIdx.x - n_router);
+    return;
+  }
+
+  const int e = 2 * blockIdx.x + (warp >> 2);
+  const int quarter = H / 4;
+  const int k0 = (warp & 3) * quarter;
+  const bool valid = e < E;
+  const float* wrow = a.L.wr + (size_t)(valid ? e : 0) * H + k0;
+  // router rows do not depend on the previous kernel: load before waiting
+  constexpr int kMaxV = 8;  // float4 per lane, up to H = 4096
+  const int nv = (quarter + 127) / 128;
+  float4 wv[kMaxV];
+#pragma unroll
+  for (int i = 0; i < kMaxV; ++i) {
+    wv[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (i < nv && 128 * i + 4 * lane < quarter)
+      wv[i] = __ldg(reinterpret_cast<const float4*>(wrow + 128 * i + 4 * lane));
+  }
+  pdl_wait();
+  pdl_trigger();
+
+  float acc[kDecodeRows];
+#pragma unroll
+  for (int t = 0; t < kDecodeRows; ++t) acc[t] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kMaxV; ++i) {
+    if (i >= nv) break;
+    if (128 * i + 4 * lane >= quarter) continue;
+    const int kk = k0 + 128 * i + 4 * lane;
+#pragma unroll
+    for (int t = 0; t < kDecodeRows; ++t) {
+      if (t >= T) break;
+      const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(a.x + (size_t)t * H + kk));
+      const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+      const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+      float s = acc[t];
+      s = fmaf(__low2float(p0), wv[i].x, s);
+      s = fmaf(__high2float(p0), wv[i].y, s);
+      s = fmaf(__low2float(p1), wv[i].z, s);
+      s = fmaf(__high2float(p1), wv[i].w, s);
+      acc[t] = s;
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kDecodeRows; ++t) {
+    if (t >= T) break;
+    const float v = warp_sum(acc[t]);
+    if (lane == 0) red[warp][t] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < 2 * T) {
+    const int h = threadIdx.x / T, t = threadIdx.x % T;
+    const int ee = 2 * blockIdx.x + h;
+    if (ee < E) {
+      const float v = ((red[4 * h][t] + red[4 * h + 1][t]) + red[4 * h + 2][t]) + red[4 * h + 3][t];
+      a.w.logits[(size_t)t * E + ee] = v;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int old = atomicAdd(&a.w.done[0], 1);
+    s_last = old == n_router - 1;
+    if (s_last) a.w.done[0] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  decode_schedule(a);
+}
+
+cudaError_t launch_route_decode(const KArgs& a, bool pdl, cudaStream_t s) {
+  const int grid = (a.d.E + 1) / 2 + a.d.T;
+  return launch_pdl(k_route_decode, dim3(grid), dim3(256), 0, s, pdl, a);
+}
+
+// ---- D3: down projections + combine -----------------------------------------
+// One CTA per 16 output rows.  Work items: every selected expert (its rows'
+// 16 x I slice of the down weights against those rows' re-quantised SwiGLU
+// codes) and the shared expert's slice in two K halves.  Items go to warps
+// round-robin, each covering its full K, so no cross-warp reduction is needed.
+__global__ void __launch_bounds__(256) k_down_combine_decode(KArgs a) {
+  __shared__ float s_d[kDecodeRows * kMaxTopK][16];
+  __shared__ float s_ds[2][kDecodeRows][16];
+  const int T = a.d.T, H = a.d.H, I = a.d.I, Is = a.d.Is, k = a.d.k;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, q = lane & 3;
+  const int m0 = 16 * blockIdx.x;
+  const int nbi = I / kGroup;
+  pdl_wait();
+  pdl_trigger();
+  const int U = *a.w.n_chunks;
+  for (int it = warp; it < U + 2; it += 8) {
+    if (it < U) {
+      const int4 ch = a.w.chunks[it];
+      const int e = ch.x, s0 = ch.y, ntok = ch.z;
+      const uint8_t* W = a.L.w2 + (size_t)e * H * I;
+      const float* S = a.L.s2 + ((size_t)e * (H / kGroup) + m0 / kGroup) * nbi;
+      const uint8_t* r0 = W + (size_t)(m0 + g) * I;
+      const uint8_t* r1 = W + (size_t)(m0 + 8 + g) * I;
+      const uint8_t* hb[2];
+      bool bval[2];
+      const float* shc[2][2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int tb = 8 * nt + g;
+        bval[nt] = tb < ntok;
+        hb[nt] = a.w.hq + (size_t)(s0 + (bval[nt] ? tb : 0)) * I;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int tc = 8 * nt + 2 * q + c;
+          shc[nt][c] = tc < ntok ? a.w.sh + (size_t)(s0 + tc) * nbi : nullptr;
+        }
+      }
+      const int n_nt = ntok > 8 ? 2 : 1;
+      float acc[2][4] = {};
+      for (int b = 0; b < I / 64; ++b) {
+        const int kb = (b * 64) / kGroup;
+        const int off = b * 64 + 16 * q;
+        const uint4 a0 = ld_stream16(r0 + off), a1 = ld_stream16(r1 + off);
+        const float sw = __ldg(S + kb);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          if (nt >= n_nt) break;
+          const uint4 bx = bval[nt] ? ld_cg16(hb[nt] + off) : make_uint4(0u, 0u, 0u, 0u);
+          const float sa = shc[nt][0] ? __ldcg(shc[nt][0] + kb) : 0.0f;
+          const float sb = shc[nt][1] ? __ldcg(shc[nt][1] + kb) : 0.0f;
+          float p[4] = {};
+          mma_e4m3_k64(p, a0, a1, bx);
+          acc[nt][0] = fmaf(p[0], sw * sa, acc[nt][0]);
+          acc[nt][1] = fmaf(p[1], sw * sb, acc[nt][1]);
+          acc[nt][2] = fmaf(p[2], sw * sa, acc[nt][2]);
+          acc[nt][3] = fmaf(p[3], sw * sb, acc[nt][3]);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int tok = 8 * nt + 2 * q + (c & 1);
+          if (nt < n_nt && tok < ntok) s_d[s0 + tok][g + 8 * (c >> 1)] = bf16_round(acc[nt][c]);
+        }
+    } else {
+      const int half = it - U;
+      const int kh = Is / 2;
+      const bf16* r0 = a.L.ws2 + (size_t)(m0 + g) * Is + half * kh;
+      const bf16* r1 = a.L.ws2 + (size_t)(m0 + 8 + g) * Is + half * kh;
+      const bf16* hb[2];
+      bool bval[2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        bval[nt] = 8 * nt + g < T;
+        hb[nt] = a.w.hs + (size_t)(bval[nt] ? 8 * nt + g : 0) * Is + half * kh;
+      }
+      const int n_nt = T > 8 ? 2 : 1;
+      float acc[2][4] = {};
+      for (int b = 0; b < kh / 32; ++b) {
+        const int off = b * 32 + 8 * q;
+        const uint4 a0 = ld_stream16(r0 + off), a1 = ld_stream16(r1 + off);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          if (nt >= n_nt) break;
+          const uint4 bx = bval[nt] ? ld_cg16(hb[nt] + off) : make_uint4(0u, 0u, 0u, 0u);
+          mma_bf16_k32(acc[nt], a0, a1, bx);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int tok = 8 * nt + 2 * q + (c & 1);
+          if (nt < n_nt && tok < T) s_ds[half][tok][g + 8 * (c >> 1)] = acc[nt][c];
+        }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * 16; i += blockDim.x) {
+    const int t = i >> 4, r = i & 15;
+    float acc = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const int slot = __ldcg(a.w.slot_of_pair + t * k + j);
+      acc = fmaf(__ldcg(a.w.wts + t * k + j), s_d[slot][r], acc);
+    }
+    const float ds = bf16_round(s_ds[0][t][r] + s_ds[1][t][r]);
+    a.y[(size_t)t * H + m0 + r] = __float2bfloat16_rn(fmaf(__ldcg(a.w.gamma + t), ds, acc));
+  }
+}
+
+cudaError_t launch_down_combine_decode(const KArgs& a, bool pdl, cudaStream_t s) {
+  return launch_pdl(k_down_combine_decode, dim3(a.d.H / 16), dim3(256), 0, s, pdl, a);
+}
+
+}  // namespace moe

@@ -146,10 +146,7 @@ __device__ void gateup_routed(const KArgs& a, Smem& sm, int chunk_id, int mp) {
       float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
       m = warp_max(m);
       const float s = group_scale(m);
-      const uint32_t packed = (uint32_t)e4m3_code(__fdiv_rn(v.x, s)) |
-                              ((uint32_t)e4m3_code(__fdiv_rn(v.y, s)) << 8) |
-                              ((uint32_t)e4m3_code(__fdiv_rn(v.z, s)) << 16) |
-                              ((uint32_t)e4m3_code(__fdiv_rn(v.w, s)) << 24);
+      const uint32_t packed = quant4(v.x, v.y, v.z, v.w, s);
       *reinterpret_cast<uint32_t*>(a.w.hq + (size_t)slot * I + grp * kGroup + 4 * lane) = packed;
       if (lane == 0) a.w.sh[(size_t)slot * nbi + grp] = s;
     }
@@ -214,13 +211,53 @@ __device__ void gateup_shared(const KArgs& a, Smem& sm, int tchunk, int ms) {
 
 }  // namespace
 
+namespace {
+
+// L2 prefetch of the weight rows one gate/up unit reads (two contiguous runs).
+__device__ void prefetch_gateup_unit(const KArgs& a, int u, int n_routed, int total) {
+  if (u >= total) return;
+  const int H = a.d.H, I = a.d.I, Is = a.d.Is;
+  if (u < n_routed) {
+    const int mpp = I / 16;
+    const int e = a.w.chunks[u / mpp].x, n0 = 16 * (u % mpp);
+    const uint8_t* W = a.L.w13 + (size_t)e * 2 * I * H;
+    prefetch_l2(W + (size_t)n0 * H, 16u * H);
+    prefetch_l2(W + (size_t)(I + n0) * H, 16u * H);
+  } else {
+    const int ms = (u - n_routed) % (Is / 8);
+    prefetch_l2(a.L.ws13 + (size_t)(8 * ms) * H, 8u * H * 2);
+    prefetch_l2(a.L.ws13 + (size_t)(Is + 8 * ms) * H, 8u * H * 2);
+  }
+}
+
+}  // namespace
+
+// Down-projection weights of the selected experts are prefetched into L2 by
+// the decode gate/up kernel when they fit this budget (for the next kernel).
+constexpr size_t kDownPrefetchBudget = 48u << 20;
+
+template <bool kDecode>
 __global__ void __launch_bounds__(256) k_gateup(KArgs a) {
   __shared__ Smem sm;
+  if (kDecode) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const int n_routed = *a.w.n_chunks * (a.d.I / 16);
   const int n_tchunks = (a.d.T + kChunk - 1) / kChunk;
   const int ms_per = a.d.Is / 8;
   const int total = n_routed + n_tchunks * ms_per;
+  if (kDecode && threadIdx.x == 0) {
+    prefetch_gateup_unit(a, blockIdx.x, n_routed, total);
+    prefetch_gateup_unit(a, blockIdx.x + gridDim.x, n_routed, total);
+    const int U = *a.w.n_chunks;
+    const size_t per = (size_t)a.d.H * a.d.I;
+    if ((size_t)U * per <= kDownPrefetchBudget)
+      for (int c = 0; c < U; ++c)
+        prefetch_l2_share(a.L.w2 + (size_t)a.w.chunks[c].x * per, per, blockIdx.x, gridDim.x);
+  }
   for (int u = blockIdx.x; u < total; u += gridDim.x) {
+    if (kDecode && threadIdx.x == 0) prefetch_gateup_unit(a, u + 2 * gridDim.x, n_routed, total);
     if (u < n_routed) {
       gateup_routed(a, sm, u / (a.d.I / 16), u % (a.d.I / 16));
     } else {
@@ -231,8 +268,12 @@ __global__ void __launch_bounds__(256) k_gateup(KArgs a) {
 }
 
 cudaError_t launch_gateup(const KArgs& a, int grid, cudaStream_t s) {
-  k_gateup<<<grid, 256, 0, s>>>(a);
+  k_gateup<false><<<grid, 256, 0, s>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_gateup_decode(const KArgs& a, int grid, bool pdl, cudaStream_t s) {
+  return launch_pdl(k_gateup<true>, dim3(grid), dim3(256), 0, s, pdl, a);
 }
 
 // ---- down projections ------------------------------------------------------

@@ -9,7 +9,7 @@
 // (dynamic 1 x 128 FP8 activation quantization).
 #include <math.h>
 
-#include "moe_device.cuh"
+#include "moe_rowops.cuh"
 
 namespace moe {
 
@@ -63,107 +63,11 @@ cudaError_t launch_router(const KArgs& a, cudaStream_t s) {
 }
 
 // ---- activation quantisation (1 x 128 groups) and the shared gate ----------
-// One CTA per row.  Warp w quantises groups w, w+8, ...; each lane holds 4
-// consecutive values of the group.  The gate dot product x . g is reduced in a
-// fixed order (per-thread strided sums, then warps 0..7).
-__global__ void __launch_bounds__(256) k_quant_gamma(KArgs a) {
-  __shared__ float red[8];
-  const int H = a.d.H, t = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bf16* xr = a.x + (size_t)t * H;
-  const int ngroups = H / kGroup;
-  for (int gi = warp; gi < ngroups; gi += 8) {
-    const int base = gi * kGroup + 4 * lane;
-    uint2 raw = *reinterpret_cast<const uint2*>(xr + base);
-    __nv_bfloat162 p0 = *reinterpret_cast<__nv_bfloat162*>(&raw.x);
-    __nv_bfloat162 p1 = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
-    float v[4] = {__low2float(p0), __high2float(p0), __low2float(p1), __high2float(p1)};
-    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-    m = warp_max(m);
-    const float s = group_scale(m);
-    uint32_t packed = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) packed |= (uint32_t)e4m3_code(__fdiv_rn(v[i], s)) << (8 * i);
-    *reinterpret_cast<uint32_t*>(a.w.xq + (size_t)t * H + base) = packed;
-    if (lane == 0) a.w.sx[(size_t)t * ngroups + gi] = s;
-  }
-  float acc = 0.0f;
-  for (int i = threadIdx.x; i < H; i += 256)
-    acc = fmaf(__bfloat162float(xr[i]), __bfloat162float(a.L.gate[i]), acc);
-  acc = warp_sum(acc);
-  if (lane == 0) red[warp] = acc;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float v = 0.0f;
-    for (int w = 0; w < 8; ++w) v += red[w];
-    a.w.gamma[t] = __fdiv_rn(1.0f, 1.0f + expf(-v));
-  }
-}
+__global__ void __launch_bounds__(256) k_quant_gamma(KArgs a) { quant_row_and_gate(a, blockIdx.x); }
 
 cudaError_t launch_quant_gamma(const KArgs& a, cudaStream_t s) {
   k_quant_gamma<<<a.d.T, 256, 0, s>>>(a);
   return cudaGetLastError();
-}
-
-// ---- top-k + renormalised softmax ------------------------------------------
-// One warp per row; lane l holds experts l, l+32, ..., so within a lane the
-// index grows with the slot and a strict '>' keeps the lower index on ties.
-__device__ __forceinline__ void topk_row(const float* logits, int E, int k, int* idx_out,
-                                         float* w_out) {
-  const int lane = threadIdx.x & 31;
-  float v[8];
-  uint32_t taken = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    int e = lane + 32 * i;
-    v[i] = e < E ? logits[e] : -INFINITY;
-    if (e >= E) taken |= 1u << i;
-  }
-  float sel_v[kMaxTopK];
-  int sel_e[kMaxTopK];
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    if (j >= k) break;
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (!(taken >> i & 1u) && (be == 0x7fffffff || v[i] > bv)) {
-        bv = v[i];
-        be = lane + 32 * i;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    sel_v[j] = bv;
-    sel_e[j] = be;
-  }
-  // softmax over the selected logits (the largest is the first)
-  float den = 0.0f;
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j)
-    if (j < k) den += expf(sel_v[j] - sel_v[0]);
-  for (int j = lane; j < k; j += 32) {
-    float num = 0.0f;
-    int e = 0;
-    // registers are indexed statically: select by loop
-#pragma unroll
-    for (int jj = 0; jj < kMaxTopK; ++jj)
-      if (jj == j) {
-        num = expf(sel_v[jj] - sel_v[0]);
-        e = sel_e[jj];
-      }
-    idx_out[j] = e;
-    w_out[j] = __fdiv_rn(num, den);
-  }
 }
 
 __global__ void __launch_bounds__(256) k_topk(KArgs a) {

@@ -24,6 +24,8 @@ struct moe_ctx {
   bool loaded = false;
   int opt_path = 0;
   int opt_pdl = 1;
+  int dec_grid = 0;        // persistent decode kernel: CTAs (one per SM), 0 = unavailable
+  size_t dec_optin = 0;    // shared memory a CTA may use
   cudaStream_t last_stream = nullptr;
   std::vector<void*> allocs;
   DevLayer L{};
@@ -60,7 +62,7 @@ bool config_supported(const moe_config* c) {
 
 // Byte layout of everything a context allocates, in allocation order.
 struct Plan {
-  size_t sizes[32];
+  size_t sizes[40];
   int n = 0;
   size_t total = 0;
   size_t add(size_t b) {
@@ -107,9 +109,10 @@ Plan make_plan(const moe_config* c) {
   p.add(T * Is * 2);                      // 26 hs
   p.add(T * k * H * 2);                   // 27 dbuf
   p.add(T * H * 2);                       // 28 ds
-  p.add(64);                              // 29 status + done counters
+  p.add(64);                              // 29 status and barrier counters
   p.add(T * H * 2);                       // 30 stage_x
   p.add(T * H * 2);                       // 31 stage_y
+  p.add(kDecodeRows * E * 8);             // 32 tagged decode logits
   return p;
 }
 
@@ -136,8 +139,21 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return pa < pb + nb && pb < pa + na;
 }
 
+bool use_decode(const moe_ctx* c, int T);
+bool use_fused(const moe_ctx* c, int T);
+cudaError_t launch_fused(moe_ctx* c, const KArgs& a, cudaStream_t s);
+
+// Routing with the kernels the forward of T rows would use (the persistent
+// decode kernel routes inside the layer: run the layer into the staging
+// output and keep its published routing).
 int run_router_and_quant(moe_ctx* c, const KArgs& a, cudaStream_t s) {
-  (void)c;
+  if (use_decode(c, a.d.T) && use_fused(c, a.d.T)) {
+    KArgs b = a;
+    b.y = c->stage_y;
+    return launch_fused(c, b, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
+  if (use_decode(c, a.d.T))
+    return launch_route_decode(a, c->opt_pdl != 0, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   if (launch_router(a, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_quant_gamma(a, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_topk(a, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -164,10 +180,50 @@ struct StageRec {
     if (rec && !rec->mark(name, s)) return MOE_ERR_CUDA;   \
   } while (0)
 
+// The decode kernels serve rows <= kDecodeRows for hidden sizes up to 4096.
+bool use_decode(const moe_ctx* c, int T) {
+  if (c->opt_path == 2) return false;
+  return T <= kDecodeRows && c->cfg.hidden <= 4096;
+}
+
+// The persistent decode kernel unless the chained decode kernels are asked for.
+// Stages and shared memory of the persistent decode kernel for T rows: as
+// many stages as the per-CTA opt-in shared memory holds.
+int decode_plan(const moe_ctx* c, int T, size_t* smem) {
+  const int H = c->cfg.hidden, E = c->cfg.n_experts;
+  const int n = decode_layer_stages(T, H, E, c->dec_optin);
+  if (n < 2 || !decode_layer_fits(T, H, E, c->cfg.top_k, c->cfg.inter, c->cfg.shared_inter, n))
+    return 0;
+  *smem = decode_layer_smem(T, H, E, n);
+  return n;
+}
+
+bool use_fused(const moe_ctx* c, int T) {
+  size_t smem = 0;
+  return c->opt_path != 3 && c->dec_grid > 0 && decode_plan(c, T, &smem) >= 2;
+}
+
+cudaError_t launch_fused(moe_ctx* c, const KArgs& a, cudaStream_t s) {
+  size_t smem = 0;
+  const int n = decode_plan(c, a.d.T, &smem);
+  return launch_decode_layer(a, c->dec_grid, n, smem, c->opt_pdl != 0, s);
+}
+
 int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
                 StageRec* rec = nullptr) {
   KArgs a = make_args(c, x, y, T);
   const int grid = 2 * c->sm_count;
+  if (use_decode(c, T) && use_fused(c, T)) {
+    LAUNCH(launch_fused(c, a, s), "decode_layer");
+    return MOE_OK;
+  }
+  if (use_decode(c, T)) {
+    const bool pdl = c->opt_pdl != 0;
+    LAUNCH(launch_route_decode(a, pdl, s), "route_decode");
+    LAUNCH(launch_gateup_decode(a, grid, pdl, s), "gateup_decode");
+    LAUNCH(launch_down_combine_decode(a, pdl, s), "down_combine_decode");
+    return MOE_OK;
+  }
   LAUNCH(launch_router(a, s), "router");
   LAUNCH(launch_quant_gamma(a, s), "quant_gamma");
   LAUNCH(launch_topk(a, s), "topk");
@@ -224,7 +280,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     delete c;
     return MOE_ERR_CUDA;
   }
-  void* ptrs[32];
+  void* ptrs[40];
   for (int i = 0; i < plan.n; ++i) {
     if (cudaMalloc(&ptrs[i], plan.sizes[i]) != cudaSuccess) {
       cudaGetLastError();
@@ -265,16 +321,37 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   w.dbuf = (bf16*)ptrs[27];
   w.ds = (bf16*)ptrs[28];
   w.status = (int*)ptrs[29];
-  w.done = w.status + 4;
+  w.done = w.status + 1;
+  w.tlog = (unsigned long long*)ptrs[32];
   c->stage_x = (bf16*)ptrs[30];
   c->stage_y = (bf16*)ptrs[31];
   // counters start at zero and are reset by the kernels that use them
   if (cudaMemset(w.gcount, 0, plan.sizes[25]) != cudaSuccess ||
       cudaMemset(w.status, 0, plan.sizes[29]) != cudaSuccess ||
-      cudaMemset(w.n_chunks, 0, plan.sizes[21]) != cudaSuccess) {
+      cudaMemset(w.n_chunks, 0, plan.sizes[21]) != cudaSuccess ||
+      cudaMemset(w.tlog, 0, plan.sizes[32]) != cudaSuccess) {
     free_all(c);
     delete c;
     return MOE_ERR_CUDA;
+  }
+  // persistent decode kernel: one CTA per SM must fit at the largest row count
+  {
+    int optin = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) ==
+        cudaSuccess) {
+      const int H = cfg->hidden, E = cfg->n_experts;
+      const int nst = decode_layer_stages(kDecodeRows, H, E, (size_t)optin);
+      const size_t smem = decode_layer_smem(kDecodeRows, H, E, nst);
+      // launches size their shared memory per row count, up to the opt-in limit
+      if (nst >= 2 && setup_decode_layer((size_t)optin) == cudaSuccess &&
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel(), 256, smem) ==
+              cudaSuccess &&
+          per_sm >= 1 && 2 * c->sm_count >= E && cfg->hidden <= 2048) {
+        c->dec_grid = c->sm_count;
+        c->dec_optin = (size_t)optin;
+      }
+    }
+    cudaGetLastError();
   }
   *out = c;
   return MOE_OK;
@@ -475,7 +552,7 @@ int moe_set_option(moe_ctx* c, int option, int value) {
   if (!c) return MOE_ERR_INVALID_ARG;
   switch (option) {
     case MOE_OPT_PATH:
-      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+      if (value < 0 || value > 3) return MOE_ERR_INVALID_ARG;
       c->opt_path = value;
       return MOE_OK;
     case MOE_OPT_PDL:
@@ -497,6 +574,16 @@ int moe_last_device_status(moe_ctx* c) {
       cudaMemset(c->w.status, 0, 4) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
+  }
+  if (flag) {
+    // a bounded wait gave up: counters may be mid-count, start them afresh
+    const Plan plan = make_plan(&c->cfg);
+    if (cudaMemset(c->w.status, 0, plan.sizes[29]) != cudaSuccess ||
+        cudaMemset(c->w.gcount, 0, plan.sizes[25]) != cudaSuccess ||
+        cudaMemset(c->w.tlog, 0, plan.sizes[32]) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
   }
   return flag ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
 }

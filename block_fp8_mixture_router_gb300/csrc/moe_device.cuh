@@ -21,6 +21,34 @@ __device__ __forceinline__ uint4 ld_cg16(const void* p) {
   return __ldcg(reinterpret_cast<const uint4*>(p));
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+// Without the launch attribute both are no-ops, so the same kernel serves
+// plain and chained launches.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// Ask L2 to fetch [p, p + bytes) (16-byte aligned, multiple of 16); no wait.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Prefetch share `part` of `parts` equal shares of [p, p + bytes), in pieces.
+__device__ __forceinline__ void prefetch_l2_share(const void* p, size_t bytes, int part, int parts) {
+  const size_t per = ((bytes + parts - 1) / parts + 15) & ~(size_t)15;
+  size_t lo = per * part;
+  size_t hi = lo + per < bytes ? lo + per : bytes;
+  const char* c = static_cast<const char*>(p);
+  while (lo < hi) {
+    uint32_t n = (uint32_t)((hi - lo) < 65536 ? (hi - lo) : 65536);
+    n &= ~15u;
+    if (n == 0) break;
+    prefetch_l2(c + lo, n);
+    lo += n;
+  }
+}
+
 // ---- warp MMAs ------------------------------------------------------------
 // D(16x8, f32) += A(16x32, e4m3, row) * B(32x8, e4m3, col)
 __device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -70,12 +98,30 @@ __device__ __forceinline__ float bf16_round(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
 
-// e4m3 code of v: round to nearest even, saturating to +-448, NaN -> NaN code.
-__device__ __forceinline__ uint8_t e4m3_code(float v) {
-  return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+// e4m3 codes of four values, first value in the lowest byte: the hardware
+// conversion, round to nearest even, saturating to +-448, NaN to the NaN code.
+__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(lo) : "f"(v1), "f"(v0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(hi) : "f"(v3), "f"(v2));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-__device__ __forceinline__ float silu_f32(float z) { return __fdiv_rn(z, 1.0f + expf(-z)); }
+// Quantise four values of a group with scale s: codes of v/s (IEEE division).
+__device__ __forceinline__ uint32_t quant4(float v0, float v1, float v2, float v3, float s) {
+  return e4m3x4(__fdiv_rn(v0, s), __fdiv_rn(v1, s), __fdiv_rn(v2, s), __fdiv_rn(v3, s));
+}
+
+// silu(z) = z / (1 + e^-z) with the fast exponential and divide; the
+// exponent is clamped so the divisor stays finite (silu(z) is then ~0).
+__device__ __forceinline__ float silu_f32(float z) {
+  return __fdividef(z, 1.0f + __expf(fminf(-z, 80.0f)));
+}
+
+// Logistic sigmoid with the fast exponential and divide.
+__device__ __forceinline__ float sigmoid_f32(float v) {
+  return __fdividef(1.0f, 1.0f + __expf(fminf(-v, 80.0f)));
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

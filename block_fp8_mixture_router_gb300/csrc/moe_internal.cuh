@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -58,7 +60,8 @@ struct DevWork {
   bf16* dbuf;           // [T*k][H] by slot
   bf16* ds;             // [T][H]
   int* status;          // [1] device status flag
-  int* done;            // [4] arrival counters of last-block patterns (self-resetting)
+  int* done;            // [12] barrier counters (self-resetting) and the decode launch tag
+  unsigned long long* tlog;  // [kDecodeRows][E] decode logits as {launch tag, value} words
 };
 
 struct KArgs {
@@ -81,5 +84,40 @@ cudaError_t launch_gateup(const KArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_down(const KArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_combine(const KArgs& a, cudaStream_t s);
 cudaError_t launch_gather_hq(const KArgs& a, uint8_t* hq, float* sh, cudaStream_t s);
+
+// Decode path (rows <= kDecodeRows): three kernels chained with programmatic
+// dependent launch when `pdl` is set.
+cudaError_t launch_route_decode(const KArgs& a, bool pdl, cudaStream_t s);
+cudaError_t launch_gateup_decode(const KArgs& a, int grid, bool pdl, cudaStream_t s);
+cudaError_t launch_down_combine_decode(const KArgs& a, bool pdl, cudaStream_t s);
+
+// Decode path as one persistent kernel (one CTA per SM, grid barriers).
+size_t decode_layer_smem(int T, int H, int E, int n_stages);
+int decode_layer_stages(int T, int H, int E, size_t budget);
+bool decode_layer_fits(int T, int H, int E, int k, int I, int Is, int n_stages);
+cudaError_t setup_decode_layer(size_t max_smem);
+const void* decode_layer_kernel();
+cudaError_t launch_decode_layer(const KArgs& a, int grid, int n_stages, size_t smem, bool pdl,
+                                cudaStream_t s);
+
+// Launch `kernel` on `s`, allowing it to start before the previous kernel in
+// the stream completes when `pdl` is set (it must call griddepcontrol.wait
+// before reading that kernel's results).
+template <typename... KArgsT, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgsT...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 }  // namespace moe

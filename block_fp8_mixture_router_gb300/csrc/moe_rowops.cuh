@@ -1,0 +1,105 @@
+// Per-row device routines shared by the prompt and decode kernels: the
+// activation quantisation with the shared-expert gate, and the top-k.
+#pragma once
+
+#include <math.h>
+
+#include "moe_device.cuh"
+
+namespace moe {
+
+// ---- activation quantisation (1 x 128 groups) and the shared gate ----------
+// One 256-thread CTA per row.  Warp w quantises groups w, w+8, ...; each lane holds 4
+// consecutive values of the group.  The gate dot product x . g is reduced in a
+// fixed order (per-thread strided sums, then warps 0..7).
+__device__ __forceinline__ void quant_row_and_gate(const KArgs& a, int t) {
+  __shared__ float red[8];
+  const int H = a.d.H;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bf16* xr = a.x + (size_t)t * H;
+  const int ngroups = H / kGroup;
+  for (int gi = warp; gi < ngroups; gi += 8) {
+    const int base = gi * kGroup + 4 * lane;
+    uint2 raw = *reinterpret_cast<const uint2*>(xr + base);
+    __nv_bfloat162 p0 = *reinterpret_cast<__nv_bfloat162*>(&raw.x);
+    __nv_bfloat162 p1 = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
+    float v[4] = {__low2float(p0), __high2float(p0), __low2float(p1), __high2float(p1)};
+    float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+    m = warp_max(m);
+    const float s = group_scale(m);
+    const uint32_t packed = quant4(v[0], v[1], v[2], v[3], s);
+    *reinterpret_cast<uint32_t*>(a.w.xq + (size_t)t * H + base) = packed;
+    if (lane == 0) a.w.sx[(size_t)t * ngroups + gi] = s;
+  }
+  float acc = 0.0f;
+  for (int i = threadIdx.x; i < H; i += 256)
+    acc = fmaf(__bfloat162float(xr[i]), __bfloat162float(a.L.gate[i]), acc);
+  acc = warp_sum(acc);
+  if (lane == 0) red[warp] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float v = 0.0f;
+    for (int w = 0; w < 8; ++w) v += red[w];
+    a.w.gamma[t] = sigmoid_f32(v);
+  }
+}
+
+// ---- top-k + renormalised softmax ------------------------------------------
+// One warp per row.  Logits become order-preserving 32-bit keys (-0 folded
+// into +0 first, so equal values have equal keys).  Lane l holds experts
+// l, l+32, ...; each round every lane offers its largest remaining key (the
+// lowest expert among equal keys), and the warp takes the largest key and,
+// among the lanes offering it, the lowest expert: the k largest logits, ties
+// to the lower index, in rank order.  The softmax over the selected logits is
+// taken with one lane per rank (k <= 32).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// kCg: read the logits at L2 (they were written by other CTAs of the same
+// kernel).
+template <bool kCg = false>
+__device__ __forceinline__ void topk_row(const float* logits, int E, int k, int* idx_out,
+                                         float* w_out) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = e < E ? order_key(kCg ? __ldcg(logits + e) : logits[e]) : 0u;
+  }
+  uint32_t my_key = 0u, my_e = 0u;
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0u;
+    int bi = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const bool better = key[i] > bk;
+      bk = better ? key[i] : bk;
+      bi = better ? i : bi;
+    }
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t win =
+        __reduce_min_sync(0xffffffffu, bk == mx ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu);
+    const bool mine = (int)(win & 31u) == lane;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) key[i] = (mine & (i == (int)(win >> 5))) ? 0u : key[i];
+    my_key = lane == j ? mx : my_key;
+    my_e = lane == j ? win : my_e;
+  }
+  const float top = key_value(__shfl_sync(0xffffffffu, my_key, 0));
+  const float ex = lane < k ? __expf(key_value(my_key) - top) : 0.0f;
+  const float den = warp_sum(ex);
+  if (lane < k) {
+    idx_out[lane] = (int)my_e;
+    w_out[lane] = __fdividef(ex, den);
+  }
+}
+
+}  // namespace moe

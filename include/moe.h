@@ -134,10 +134,12 @@ int moe_quantize(moe_ctx* ctx, const void* x, int rows, uint8_t* codes, float* s
  * pointers.  Asynchronous; call on the stream of that forward. */
 int moe_expert_activations(moe_ctx* ctx, int rows, uint8_t* hq, float* sh, void* stream);
 
-/* Options.  MOE_OPT_PATH: 0 = automatic (rows <= 16 decode kernels, else
- * the grouped prompt kernels), 1 = always decode kernels (rows <= 16 only),
- * 2 = always grouped prompt kernels.  MOE_OPT_PDL: 1 = chain the decode
- * kernels with programmatic dependent launch (default), 0 = plain launches. */
+/* Options.  MOE_OPT_PATH: 0 = automatic (rows <= 16: the persistent decode
+ * kernel, else the grouped prompt kernels), 1 = the same as 0, 2 = always
+ * the grouped prompt kernels, 3 = rows <= 16 on three chained decode kernels
+ * instead of the persistent one.  MOE_OPT_PDL: 1 = launch with programmatic
+ * dependent launch so a layer's immutable weight reads overlap the previous
+ * kernel's tail (default), 0 = plain launches. */
 enum { MOE_OPT_PATH = 1, MOE_OPT_PDL = 2 };
 int moe_set_option(moe_ctx* ctx, int option, int value);
 

@@ -82,12 +82,20 @@ def test_tiny_layer(dev, rows):
     assert same > 0.98, same
 
 
-def test_tiny_layer_paths_agree(dev):
+@pytest.mark.parametrize("path", [m.PATH_AUTO, m.PATH_PROMPT, m.PATH_DECODE_CHAINED])
+@pytest.mark.parametrize("rows", [1, 4, 9, 16])
+def test_tiny_layer_every_path(dev, path, rows):
     case = Case(W.WORKLOADS["tiny_t4"], 64, dev)
-    x = case.x(4)
-    y_auto, *_ = run_and_check(case, x, path=m.PATH_AUTO)
-    y_prompt, *_ = run_and_check(case, x, path=m.PATH_PROMPT)
-    assert y_auto.shape == y_prompt.shape
+    run_and_check(case, case.x(rows, tag=f"p{rows}"), path=path)
+
+
+@pytest.mark.parametrize("path", [m.PATH_PROMPT, m.PATH_DECODE_CHAINED])
+def test_full_layer_other_paths(full_case, path):
+    x = full_case.x(11, tag="paths")
+    try:
+        run_and_check(full_case, x, path=path)
+    finally:
+        full_case.moe.set_option(m.MOE_OPT_PATH, m.PATH_AUTO)
 
 
 # ---- full-width layers --------------------------------------------------------
