@@ -34,7 +34,9 @@ PATH_AUTO, PATH_DECODE, PATH_PROMPT, PATH_DECODE_CHAINED = 0, 1, 2, 3
 EXPORTED = ("moe_create", "moe_load_weights", "moe_forward", "moe_forward_host", "moe_route",
             "moe_quantize", "moe_expert_activations", "moe_set_option", "moe_required_bytes",
             "moe_last_device_status", "moe_destroy", "moe_status_string",
-            "moe_profile_forward")
+            "moe_profile_forward", "moe_route_static")
+
+MOE_ROUTE_STATIC_MAX_LOGITS = 262144
 
 
 class moe_config(ctypes.Structure):
@@ -74,6 +76,7 @@ def load_library(path: str = LIB_PATH):
     L.moe_forward_host.argtypes = [vp, vp, vp, i, vp]
     L.moe_route.argtypes = [vp, vp, i, vp, vp, vp]
     L.moe_quantize.argtypes = [vp, vp, i, vp, vp, vp]
+    L.moe_route_static.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
     L.moe_expert_activations.argtypes = [vp, i, vp, vp, vp]
     L.moe_set_option.argtypes = [vp, i, i]
     L.moe_profile_forward.argtypes = [vp, vp, vp, i, vp, vp, i, ctypes.POINTER(ctypes.c_int), vp]
@@ -133,6 +136,14 @@ def moe_forward_host(ctx, x, y, rows: int, stream=None) -> int:
 
 def moe_route(ctx, x, rows: int, idx, w, stream=None) -> int:
     return load_library().moe_route(ctx, _ptr(x), rows, _ptr(idx), _ptr(w), _stream(stream))
+
+
+def moe_route_static(x, router, rows: int, hidden: int, n_experts: int, top_k: int, idx, w,
+                     stream=None) -> int:
+    """The router on the library's fixed scratch (allocates nothing); calls on
+    one device must not overlap."""
+    return load_library().moe_route_static(_ptr(x), _ptr(router), rows, hidden, n_experts,
+                                           top_k, _ptr(idx), _ptr(w), _stream(stream))
 
 
 def moe_quantize(ctx, x, rows: int, codes, scales, stream=None) -> int:

@@ -122,6 +122,38 @@ int moe_forward_host(moe_ctx* ctx, const void* x_host, void* y_host, int rows, v
  * order and w fp32 [rows][k], both device pointers.  Asynchronous. */
 int moe_route(moe_ctx* ctx, const void* x, int rows, int32_t* idx, float* w, void* stream);
 
+/* Router without a context, for callers that must not allocate device
+ * memory: a runtime that has already handed all of the device's memory to
+ * its own pool, or a latency-critical loop that cannot afford cudaMalloc's
+ * implicit synchronisation.  This call is a library convenience; the pages
+ * that define the layer have no counterpart to it.
+ *
+ * Computes what moe_route computes, with the two router kernels moe_route
+ * runs above 16 rows (fp32 logits x . router^T, the top_k largest with ties
+ * to the lower expert, softmax over the selection): x bf16 [rows][hidden],
+ * router fp32 [n_experts][hidden],
+ * idx int32 [rows][top_k] in rank order, w fp32 [rows][top_k]; all device
+ * pointers on the current device, owned by the caller.  Asynchronous on
+ * `stream`.
+ *
+ * The logits live in one scratch array per device inside this library
+ * (MOE_ROUTE_STATIC_MAX_LOGITS fp32 values, 1 MiB): rows * n_experts above
+ * that limit returns MOE_ERR_UNSUPPORTED_SHAPE (256 experts: up to 1024 rows
+ * per call) before anything is launched.  Nothing in the scratch has to start
+ * at zero: every logit a call reads was written by the same call.
+ *   - Nothing is allocated, by this library or by a library it calls.
+ *   - The first call on each device looks up the scratch's address once
+ *     (cudaGetSymbolAddress); make that first call before any stream capture
+ *     starts.
+ *   - All calls on one device share the scratch: two calls whose work can
+ *     overlap on the device (other streams, other host threads) race and give
+ *     wrong results.  Order them on one stream, or with events.
+ * Supported: hidden % 128 == 0, 1 <= top_k <= 16, top_k <= n_experts <= 256,
+ * device ordinals 0..63; rows == 0 does nothing. */
+#define MOE_ROUTE_STATIC_MAX_LOGITS 262144
+int moe_route_static(const void* x, const float* router, int rows, int hidden, int n_experts,
+                     int top_k, int32_t* idx, float* w, void* stream);
+
 /* Activation quantisation only (same kernel as moe_forward): codes e4m3
  * [rows][H] and scales fp32 [rows][H/128], both device pointers.
  * Asynchronous. */
