@@ -161,8 +161,8 @@ def measured_peaks():
 
 
 def traffic_for(kernel: str, workload: str):
-    """dram bytes per launch from a committed ncu capture, if the kernel's
-    source has not changed since."""
+    """DRAM bytes per launch from a committed ncu capture, or None once any of
+    the kernel's source files has changed since (sha256 over them in order)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -171,12 +171,15 @@ def traffic_for(kernel: str, workload: str):
     e = d.get(f"{kernel}@{workload}")
     if not e:
         return None
-    src = os.path.join(ROOT, e["source"])
-    if not os.path.exists(src):
-        return None
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != e["sha256"]:
+    h = hashlib.sha256()
+    for rel in e["sources"]:
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src):
             return None
+        with open(src, "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != e["sha256"]:
+        return None
     return e["bytes_per_launch"]
 
 
