@@ -85,6 +85,25 @@ def stage_bytes(s, T: int, U: int) -> dict:
         "gateup": gateup,
         "down": down + 2 * T * k * H + 2 * T * H,
         "combine": 2 * T * k * H + 2 * T * H + 2 * T * H + 8 * T * k + 4 * T,
+        # prompt path on tcgen05
+        "router_tc": 4 * E * H + 2 * T * H + 4 * T * E,
+        "quant_scatter": 2 * T * H + 2 * H + T * k * (H + 4 * (H // G)) + 4 * T + 4 * T * k,
+        "shared_gateup_tc": 2 * 2 * Is * H + 2 * T * H + 2 * T * Is,
+        "gateup_tc": U * w13 + T * k * (H + 4 * (H // G)) + T * k * (I + 4 * (I // G)),
+        "shared_down_tc": 2 * H * Is + 2 * T * Is + 2 * T * H,
+        "down_tc": U * w2 + T * k * (I + 4 * (I // G)) + 2 * T * k * H,
+    }
+
+
+def stage_flops(s, T: int) -> dict:
+    """Tensor-core flops of the GEMM stages, by the dtype their MMAs take."""
+    H, I, Is, E, k = s.hidden, s.inter, s.shared_inter, s.n_experts, s.top_k
+    return {
+        "gateup_tc": ("fp8", 2 * T * k * 2 * I * H),
+        "down_tc": ("fp8", 2 * T * k * H * I),
+        "shared_gateup_tc": ("bf16", 2 * T * 2 * Is * H),
+        "shared_down_tc": ("bf16", 2 * T * H * Is),
+        "router_tc": ("bf16", 3 * 2 * T * E * H),
     }
 
 
@@ -357,6 +376,22 @@ def run_ours(args):
     hbm, bf16_tf, peak_kind = measured_peaks()
     dom = max(stage_avg, key=stage_avg.get)
     dom_gbs = sb[dom] / (stage_avg[dom] * 1e-3) / 1e9
+    # the binding roof of the dominant kernel: bytes at HBM speed, or its
+    # tensor-core flops at the peak of its dtype (fp8 = 2 x the bf16 peak)
+    sf = stage_flops(s, T).get(dom)
+    roof = {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": hbm, "unit": "GB/s",
+            "frac": dom_gbs / hbm, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": sb[dom],
+            "avg_launch_us": stage_avg[dom] * 1e3, "traffic": traffic_for(dom, wl.name)}
+    if sf is not None:
+        tf_peak = bf16_tf * (2.0 if sf[0] == "fp8" else 1.0)
+        tf = sf[1] / (stage_avg[dom] * 1e-3) / 1e12
+        roof["tensor_tflops"] = tf
+        roof["tensor_peak"] = tf_peak
+        roof["tensor_dtype"] = sf[0]
+        if sf[1] / (tf_peak * 1e12) > sb[dom] / (hbm * 1e9):
+            roof.update({"bound": "tensor", "achieved": tf, "peak": tf_peak, "unit": "TFLOP/s",
+                         "frac": tf / tf_peak,
+                         "peak_kind": peak_kind + (" (bf16 x 2 for fp8)" if sf[0] == "fp8" else "")})
     lb = layer_bytes(s, T, U)
     step_ms = ms / K
 
@@ -372,11 +407,7 @@ def run_ours(args):
                          f"({L * lb / 2**30:.1f} GiB touched per rotation) > 129 MB L2",
                    "timing": "CUDA graphs of whole steps, CUDA events on the launch stream",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": hbm,
-                     "unit": "GB/s", "frac": dom_gbs / hbm, "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": sb[dom],
-                     "avg_launch_us": stage_avg[dom] * 1e3,
-                     "traffic": traffic_for(dom, wl.name)},
+        "roofline": roof,
         "layer_roofline": {"bound": "hbm", "algorithmic_bytes_per_step": lb,
                            "achieved": lb / (step_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
                            "frac": lb / (step_ms * 1e-3) / 1e9 / hbm,

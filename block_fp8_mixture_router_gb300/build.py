@@ -68,7 +68,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for _, log in results:
             print(log)
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcuda"]
+    cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")

@@ -1,0 +1,565 @@
+// Prompt path (rows > 16): the expert GEMMs on the fifth-generation tensor
+// cores (tcgen05.mma with TMEM accumulators, operands staged by TMA).
+//
+// Expert arithmetic: PR #939 "Fish Audio Drama 3 text to speech on one CUDA
+// GPU", section "Precision" (block-FP8 weights with one fp32 scale per
+// 128x128 block, e4m3 inputs per row and per 128 inputs, amax/448); the
+// commit "one SwiGLU launch for the routed and shared experts" (routed
+// SwiGLU rows stored as their FP8 quantisation, shared rows as bf16).
+//
+// Operands are swapped relative to the usual token-by-weight product: a tile
+// is 128 output features (M, the weight rows, always full) by up to 64
+// (block-FP8) or 128 (bf16) tokens (N, rounded up to 16), so experts that see few rows waste no tensor
+// work on padding rows, and one 128-feature tile is exactly one row of weight
+// scale blocks.  For every 128-deep K block the MMAs write a fresh partial
+// into one of two TMEM buffers; the epilogue warps read it back, multiply by
+// (weight block scale x activation scale of each token) and accumulate in
+// registers while the tensor cores fill the other buffer.  The bf16 shared
+// expert needs no per-block scaling and accumulates across K in TMEM.
+//
+// A gate tile and its up tile share the token operand and land in the same
+// TMEM lanes, so the thread that owns feature j holds both halves of SwiGLU
+// for it.  The tile's outputs are transposed through shared memory and
+// stored token-major with coalesced 128/256-byte rows.
+//
+// CTA roles (320 threads): warp 0 lane 0 issues TMA, warp 1 owns TMEM and
+// lane 0 issues the MMAs, warps 2-9 are the epilogue (warp w reads TMEM lanes
+// 32*(w%4).. and column half (w-2)/4 of the tile's tokens).  Every wait is bounded; a wait that
+// gives up sets the status flag and all roles leave their loops.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "moe_rowops.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kTcThreads = 320;
+constexpr int kTile = 128;        // output features per tile (M)
+constexpr int kKBytes = 128;      // bytes of K per stage (one 128B swizzle row)
+constexpr int kATileBytes = kTile * kKBytes;
+constexpr int kBBox = 16;         // token rows per TMA box
+constexpr int kBBoxBytes = kBBox * kKBytes;
+constexpr int kTmemCols = 512;
+
+template <int kKind>
+struct Cfg {
+  static constexpr bool kF8 = kKind == kTcRoutedGateUp || kKind == kTcRoutedDown;
+  static constexpr bool kPair = kKind == kTcRoutedGateUp || kKind == kTcSharedGateUp;
+  static constexpr bool kRouted = kF8;
+  static constexpr bool kRouter = kKind == kTcRouter;
+  // Tokens per tile (N).  The block-FP8 kinds keep their promoted
+  // accumulators in registers (gate and up: 2 x kN/2 per epilogue thread),
+  // which at 10 warps (3 on some SM sub-partitions, 168 registers each)
+  // leaves room for 64 tokens; the bf16 kinds accumulate in TMEM.
+  static constexpr int kN = kF8 ? 64 : 128;
+  static constexpr int kCols = kN / 2;  // columns per epilogue thread
+  // TMEM accumulator buffers (gate at +0, up at +kN) and their count
+  static constexpr int kAccCols = (kPair ? 2 : 1) * kN;
+  static constexpr int kNumBuf = (kTmemCols / kAccCols) < 4 ? (kTmemCols / kAccCols) : 4;
+  static constexpr int kStages = kPair ? (kF8 ? 4 : 3) : (kF8 ? 6 : 4);
+  static constexpr int kStageBytes = (kPair ? 2 : 1) * kATileBytes + kN * kKBytes;
+};
+
+struct Item {
+  int e, f, row0, n;
+};
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
+
+// Work item w: token tile w / n_f (routed: tiles of every expert in expert
+// order; otherwise: tiles of all rows), output tile w % n_f.
+template <bool kRouted, int kN>
+__device__ __forceinline__ Item decode_item(const TcGemm& g, const int* s_pre, const int* s_off,
+                                            const int* s_cnt, int w) {
+  Item it;
+  const int tile = w / g.n_f;
+  it.f = w - tile * g.n_f;
+  if constexpr (kRouted) {
+    int lo = 0, hi = g.E;  // largest e with s_pre[e] <= tile
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_pre[mid] <= tile) lo = mid; else hi = mid;
+    }
+    const int j = tile - s_pre[lo];
+    it.e = lo;
+    it.row0 = s_off[lo] + kN * j;
+    it.n = min(kN, s_cnt[lo] - kN * j);
+  } else {
+    it.e = 0;
+    it.row0 = kN * tile;
+    it.n = min(kN, g.T - it.row0);
+  }
+  return it;
+}
+
+// Activation scales of an item's tokens: rows row0..row0+n-1 of sb
+// [rows][n_k], copied as one 16-byte-aligned span.  Returns the span's byte
+// offset and length; the item's first scale sits `lead` bytes into it.
+__device__ __forceinline__ void scale_span(const TcGemm& g, const Item& it, uint32_t* off,
+                                           uint32_t* bytes, uint32_t* lead) {
+  const uint64_t b0 = (uint64_t)it.row0 * g.n_k * 4, b1 = (uint64_t)(it.row0 + it.n) * g.n_k * 4;
+  const uint64_t a0 = b0 & ~15ull, a1 = (b1 + 15) & ~15ull;
+  *off = (uint32_t)a0;
+  *bytes = (uint32_t)(a1 - a0);
+  *lead = (uint32_t)(b0 - a0);
+}
+
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
+          "r"(tc::smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+
+template <int kKind>
+__global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant__ TcGemm g) {
+  using C = Cfg<kKind>;
+  constexpr bool kF8 = C::kF8, kPair = C::kPair, kRouted = C::kRouted;
+  constexpr int S = C::kStages, kN = C::kN, kCols = C::kCols, NB = C::kNumBuf;
+  constexpr int kAcc = C::kAccCols;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* stages = base;
+  float* tbuf = reinterpret_cast<float*>(base + S * C::kStageBytes);  // [kN col][128 row]
+  uint8_t* sbs = reinterpret_cast<uint8_t*>(tbuf + kN * kTile);       // 2 x scale spans
+  const uint32_t sbs_slot = kF8 ? (uint32_t)((kN * g.n_k * 4 + 32 + 15) & ~15) : 0u;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sbs + 2 * sbs_slot);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = bars + 2 * S + NB;
+  uint64_t* sfull = bars + 2 * S + 2 * NB;
+  uint64_t* sempty = sfull + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sempty + 2);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int* s_pre = reinterpret_cast<int*>(s_tmem + 2);  // [E+1]
+  int* s_off = s_pre + kMaxExperts + 1;              // [E]
+  int* s_cnt = s_off + kMaxExperts;                  // [E]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < NB; ++i) {
+      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tempty[i], 8);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&sfull[i], 1);
+      tc::mbar_init(&sempty[i], 8);
+    }
+    *s_abort = 0;
+    tc::fence_barrier_init();
+    tc::tma_prefetch_map(&g.a);
+    tc::tma_prefetch_map(&g.b);
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc::tmem_alloc(s_tmem, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  int n_tiles;
+  if constexpr (kRouted) {
+    // token tiles per expert and their prefix (warp 0; E <= 256, 8 per lane)
+    for (int e = threadIdx.x; e < g.E; e += kTcThreads) {
+      s_cnt[e] = g.counts[e];
+      s_off[e] = g.off[e];
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int loc[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = 8 * lane + i;
+        loc[i] = e < g.E ? (s_cnt[e] + kN - 1) / kN : 0;
+        sum += loc[i];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int run = incl - sum;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = 8 * lane + i;
+        if (e < g.E) s_pre[e] = run;
+        run += loc[i];
+      }
+      if (lane == 31) s_pre[g.E] = incl;
+    }
+  }
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *s_tmem;
+  if constexpr (kRouted) n_tiles = s_pre[g.E];
+  else n_tiles = (g.T + kN - 1) / kN;
+  const int n_items = n_tiles * g.n_f;
+  const int n_k = g.n_k;
+  const int kx = kF8 ? kKBytes : kKBytes / 2;  // K elements per stage
+
+  if (warp == 0) {
+    // ---- TMA producer ----
+    if (lane == 0) {
+      uint32_t st = 0, ph = 0;
+      bool ok = true;
+      int n_issued = 0;  // stages issued so far (the last S are drained on abort)
+      for (int w = blockIdx.x, j = 0; w < n_items && ok; w += gridDim.x, ++j) {
+        const Item it = decode_item<kRouted, kN>(g, s_pre, s_off, s_cnt, w);
+        if constexpr (kF8) {
+          // this item's activation scales into scale slot j % 2
+          const int sl = j & 1;
+          if (!tc::wait_bounded(&sempty[sl], ((j >> 1) & 1) ^ 1u, s_abort, g.status)) break;
+          uint32_t off, bytes, lead;
+          scale_span(g, it, &off, &bytes, &lead);
+          tc::mbar_arrive_expect_tx(&sfull[sl], bytes);
+          bulk_copy_g2s(sbs + sl * sbs_slot, reinterpret_cast<const uint8_t*>(g.sb) + off, bytes,
+                        &sfull[sl]);
+        }
+        const int arow = it.e * g.a_rows_e + it.f * kTile;
+        const int nb = (it.n + kBBox - 1) / kBBox;
+        const uint32_t bytes = (kPair ? 2 : 1) * kATileBytes + nb * kBBoxBytes;
+        for (int kb = 0; kb < n_k; ++kb) {
+          if (!tc::wait_bounded(&empty[st], ph ^ 1u, s_abort, g.status)) { ok = false; break; }
+          uint8_t* sp = stages + st * C::kStageBytes;
+          const int bx = (kb % g.b_kwrap) * kx;
+          tc::mbar_arrive_expect_tx(&full[st], bytes);
+          tc::tma_load_2d(sp, &g.a, kb * kx, arow, &full[st]);
+          if constexpr (kPair) tc::tma_load_2d(sp + kATileBytes, &g.a, kb * kx, arow + g.up_rows, &full[st]);
+          uint8_t* bp = sp + (kPair ? 2 : 1) * kATileBytes;
+          for (int i = 0; i < nb; ++i)
+            tc::tma_load_2d(bp + i * kBBoxBytes, &g.b, bx, it.row0 + kBBox * i, &full[st]);
+          ++n_issued;
+          if (++st == (uint32_t)S) { st = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // let copies already in flight land before the CTA leaves (bounded)
+        const unsigned long long t0 = tc::global_ns();
+        for (int i = 1; i <= S && i <= n_issued; ++i) {
+          const int k = n_issued - i;  // stage k % S was filled in phase (k / S) & 1
+          while (!tc::mbar_try_wait(&full[k % S], (uint32_t)((k / S) & 1)) &&
+                 tc::global_ns() - t0 < tc::kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer ----
+    if (lane == 0) {
+      uint32_t st = 0, ph = 0, tb = 0, tph = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const Item it = decode_item<kRouted, kN>(g, s_pre, s_off, s_cnt, w);
+        const int n16 = (it.n + 15) & ~15;
+        const uint32_t idesc = kF8 ? tc::idesc_f8(kTile, n16) : tc::idesc_bf16(kTile, n16);
+        for (int kb = 0; kb < n_k; ++kb) {
+          if (kF8 || kb == 0) {
+            if (!tc::wait_bounded(&tempty[tb], tph ^ 1u, s_abort, g.status)) { ok = false; break; }
+            tc::fence_after_sync();
+          }
+          if (!tc::wait_bounded(&full[st], ph, s_abort, g.status)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t sa0 = tc::smem_u32(stages + st * C::kStageBytes);
+          const uint32_t sa1 = sa0 + kATileBytes;
+          const uint32_t sb = sa0 + (kPair ? 2 : 1) * kATileBytes;
+          const uint32_t d0 = tmem + tb * kAcc;
+#pragma unroll
+          for (int kk = 0; kk < kKBytes / 32; ++kk) {
+            const uint32_t acc = (kk > 0 || (!kF8 && kb > 0)) ? 1u : 0u;
+            const uint64_t bdesc = tc::sw128_desc(sb + 32 * kk);
+            tc::mma<kF8>(d0, tc::sw128_desc(sa0 + 32 * kk), bdesc, idesc, acc);
+            if constexpr (kPair) tc::mma<kF8>(d0 + kN, tc::sw128_desc(sa1 + 32 * kk), bdesc, idesc, acc);
+          }
+          tc::commit(&empty[st]);
+          if (++st == (uint32_t)S) { st = 0; ph ^= 1u; }
+          if (kF8 || kb == n_k - 1) {
+            tc::commit(&tfull[tb]);
+            if (++tb == (uint32_t)NB) { tb = 0; tph ^= 1u; }
+          }
+        }
+      }
+    }
+  } else {
+    // ---- epilogue ----
+    const int ew = warp - 2;
+    const int q = warp & 3;
+    const int c0 = kCols * (ew >> 2);
+    const int row = 32 * q + lane;
+    const uint32_t tl = (uint32_t)(32 * q) << 16;
+    uint32_t tb = 0, tph = 0;
+    // After a failed wait the warps still walk every item (all later waits
+    // give up at once), so each of them reaches every named barrier.
+    for (int w = blockIdx.x, j = 0; w < n_items; w += gridDim.x, ++j) {
+      const Item it = decode_item<kRouted, kN>(g, s_pre, s_off, s_cnt, w);
+      const int n16 = (it.n + 15) & ~15;
+      const float* sc_tok = nullptr;  // this item's scales, [token][n_k]
+      if constexpr (kF8) {
+        const int sl = j & 1;
+        tc::wait_bounded(&sfull[sl], (j >> 1) & 1, s_abort, g.status);
+        uint32_t off, bytes, lead;
+        scale_span(g, it, &off, &bytes, &lead);
+        sc_tok = reinterpret_cast<const float*>(sbs + sl * sbs_slot + lead);
+      }
+      float acc0[kCols], acc1[kCols];
+#pragma unroll
+      for (int i = 0; i < kCols; ++i) { acc0[i] = 0.0f; acc1[i] = 0.0f; }
+      const float* sa_g = g.sa + ((size_t)it.e * (g.a_rows_e / kTile) + it.f) * n_k;
+      const float* sa_u = sa_g + (size_t)(g.up_rows / kTile) * n_k;
+      for (int kb = (kF8 ? 0 : n_k - 1); kb < n_k; ++kb) {
+        float wg = 0.0f, wu = 0.0f;
+        if constexpr (kF8) {
+          wg = __ldg(sa_g + kb);
+          if constexpr (kPair) wu = __ldg(sa_u + kb);
+        }
+        tc::wait_bounded(&tfull[tb], tph, s_abort, g.status);
+        __syncwarp();  // lanes may leave the poll at different tries
+        tc::fence_after_sync();
+        const uint32_t ta0 = tmem + tl + tb * kAcc + c0;
+        if constexpr (!kF8) epi_sync();  // every warp is done reading tbuf
+#pragma unroll
+        for (int c4 = 0; c4 < kCols / 16; ++c4) {
+          if (c0 + 16 * c4 < n16) {
+            uint32_t va[16], vb[16];
+            if constexpr (kPair) tc::tmem_ld16x2(ta0 + 16 * c4, ta0 + kN + 16 * c4, va, vb);
+            else tc::tmem_ld16(ta0 + 16 * c4, va);
+            if constexpr (kF8) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float s = sc_tok[(c0 + 16 * c4 + i) * n_k + kb];
+                acc0[16 * c4 + i] = fmaf(__uint_as_float(va[i]), wg * s, acc0[16 * c4 + i]);
+                if constexpr (kPair)
+                  acc1[16 * c4 + i] = fmaf(__uint_as_float(vb[i]), wu * s, acc1[16 * c4 + i]);
+              }
+            } else {
+              // bf16: the whole K is in this accumulator
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                float v = __uint_as_float(va[i]);
+                if constexpr (kPair)
+                  v = bf16_round(silu_f32(bf16_round(v)) * bf16_round(__uint_as_float(vb[i])));
+                tbuf[(c0 + 16 * c4 + i) * kTile + row] = v;
+              }
+            }
+          }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&tempty[tb]);
+        if (++tb == (uint32_t)NB) { tb = 0; tph ^= 1u; }
+      }
+      if constexpr (kF8) {
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sempty[j & 1]);  // scale slot free
+        epi_sync();  // every warp is done reading tbuf
+#pragma unroll
+        for (int i = 0; i < kCols; ++i) {
+          float v = acc0[i];
+          if constexpr (kPair) v = silu_f32(bf16_round(acc0[i])) * bf16_round(acc1[i]);
+          tbuf[(c0 + i) * kTile + row] = v;
+        }
+      }
+      epi_sync();
+      // ---- store: one token column per warp, 128 features per column ----
+      for (int col = ew; col < it.n; col += 8) {
+        const float4 v = *reinterpret_cast<const float4*>(tbuf + col * kTile + 4 * lane);
+        const size_t r = (size_t)(it.row0 + col);
+        if constexpr (kKind == kTcRoutedGateUp) {
+          float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+          m = warp_max(m);
+          const float s = group_scale(m);
+          *reinterpret_cast<uint32_t*>(g.hq + r * g.ldo + it.f * kTile + 4 * lane) =
+              quant4(v.x, v.y, v.z, v.w, s);
+          if (lane == 0) g.sh[r * (g.ldo / kTile) + it.f] = s;
+        } else if constexpr (kKind == kTcRouter) {
+          const int e = it.f * kTile + 4 * lane;  // logits [row][E], fp32
+          float* o = g.outf + r * g.ldo + e;
+          if (e + 3 < g.ldo) {
+            *reinterpret_cast<float4*>(o) = v;
+          } else {
+            if (e < g.ldo) o[0] = v.x;
+            if (e + 1 < g.ldo) o[1] = v.y;
+            if (e + 2 < g.ldo) o[2] = v.z;
+          }
+        } else {
+          __nv_bfloat162 p0 = __floats2bfloat162_rn(v.x, v.y);
+          __nv_bfloat162 p1 = __floats2bfloat162_rn(v.z, v.w);
+          uint2 o;
+          o.x = *reinterpret_cast<uint32_t*>(&p0);
+          o.y = *reinterpret_cast<uint32_t*>(&p1);
+          *reinterpret_cast<uint2*>(g.out + r * g.ldo + it.f * kTile + 4 * lane) = o;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int kKind>
+size_t smem_bytes(int n_k) {
+  using C = Cfg<kKind>;
+  const size_t slot = C::kF8 ? (((size_t)C::kN * n_k * 4 + 32 + 15) & ~(size_t)15) : 0;
+  return 1024 + (size_t)C::kStages * C::kStageBytes + (size_t)C::kN * kTile * 4 + 2 * slot +
+         (2 * C::kStages + 2 * C::kNumBuf + 4) * 8 + 16 + (3 * kMaxExperts + 1) * 4;
+}
+
+const void* kernel_of(int kind) {
+  switch (kind) {
+    case kTcRoutedGateUp: return (const void*)k_tc_gemm<kTcRoutedGateUp>;
+    case kTcRoutedDown: return (const void*)k_tc_gemm<kTcRoutedDown>;
+    case kTcSharedGateUp: return (const void*)k_tc_gemm<kTcSharedGateUp>;
+    case kTcSharedDown: return (const void*)k_tc_gemm<kTcSharedDown>;
+    default: return (const void*)k_tc_gemm<kTcRouter>;
+  }
+}
+
+// ---- activation quantisation straight into (expert, row) slot order --------
+// One CTA per row: quantise x[t] in 1 x 128 groups (as quant_row_and_gate),
+// write the codes and scales to each of the row's k slots, and gamma[t].
+__global__ void __launch_bounds__(256) k_quant_scatter(KArgs a, uint8_t* xg, float* sxg) {
+  __shared__ int slots[kMaxTopK];
+  __shared__ float red[8];
+  const int t = blockIdx.x, H = a.d.H, k = a.d.k;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x < k) slots[threadIdx.x] = a.w.slot_of_pair[t * k + threadIdx.x];
+  __syncthreads();
+  const bf16* xr = a.x + (size_t)t * H;
+  const int ngroups = H / kGroup;
+  for (int gi = warp; gi < ngroups; gi += 8) {
+    const int base = gi * kGroup + 4 * lane;
+    const uint2 raw = *reinterpret_cast<const uint2*>(xr + base);
+    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+    const float v0 = __low2float(p0), v1 = __high2float(p0), v2 = __low2float(p1),
+                v3 = __high2float(p1);
+    float m = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+    m = warp_max(m);
+    const float s = group_scale(m);
+    const uint32_t packed = quant4(v0, v1, v2, v3, s);
+    for (int j = 0; j < k; ++j) {
+      *reinterpret_cast<uint32_t*>(xg + (size_t)slots[j] * H + base) = packed;
+      if (lane == 0) sxg[(size_t)slots[j] * ngroups + gi] = s;
+    }
+  }
+  float acc = 0.0f;
+  for (int i = threadIdx.x; i < H; i += 256)
+    acc = fmaf(__bfloat162float(xr[i]), __bfloat162float(a.L.gate[i]), acc);
+  acc = warp_sum(acc);
+  if (lane == 0) red[warp] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float v = 0.0f;
+    for (int w = 0; w < 8; ++w) v += red[w];
+    a.w.gamma[t] = sigmoid_f32(v);
+  }
+}
+
+// Router weights as three bf16 parts, w = hi + mid + lo exactly (each part
+// rounds the remainder of the previous ones; a float's 24 significant bits
+// fit in three 8-bit ones).  With bf16 x every product x * part is exact in
+// fp32, so the tensor-core GEMM over [hi | mid | lo] gives fp32 logits.
+// out [Epad][3H]; rows E..Epad-1 are zero.
+__global__ void k_split_router(const float* __restrict__ wr, bf16* __restrict__ out, int E,
+                               int Epad, int H) {
+  const size_t n = (size_t)Epad * H;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int e = (int)(i / H), c = (int)(i % H);
+    const float w = e < E ? wr[(size_t)e * H + c] : 0.0f;
+    const bf16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const bf16 mid = __float2bfloat16_rn(r1);
+    const bf16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    bf16* row = out + (size_t)e * 3 * H;
+    row[c] = hi;
+    row[H + c] = mid;
+    row[2 * H + c] = lo;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_split_router(const float* wr, bf16* out, int E, int Epad, int H,
+                                cudaStream_t s) {
+  k_split_router<<<1024, 256, 0, s>>>(wr, out, E, Epad, H);
+  return cudaGetLastError();
+}
+
+size_t tc_gemm_smem(int kind, int n_k) {
+  switch (kind) {
+    case kTcRoutedGateUp: return smem_bytes<kTcRoutedGateUp>(n_k);
+    case kTcRoutedDown: return smem_bytes<kTcRoutedDown>(n_k);
+    case kTcSharedGateUp: return smem_bytes<kTcSharedGateUp>(n_k);
+    case kTcSharedDown: return smem_bytes<kTcSharedDown>(n_k);
+    default: return smem_bytes<kTcRouter>(n_k);
+  }
+}
+
+cudaError_t setup_tc_gemm(int kind, size_t smem) {
+  return cudaFuncSetAttribute(kernel_of(kind), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem);
+}
+
+cudaError_t launch_tc_gemm(int kind, const TcGemm& g, int grid, size_t smem, cudaStream_t s) {
+  if (grid < 1) return cudaSuccess;
+  void* args[] = {const_cast<TcGemm*>(&g)};
+  return cudaLaunchKernel(kernel_of(kind), dim3(grid), dim3(kTcThreads), args, smem, s);
+}
+
+cudaError_t launch_quant_scatter(const KArgs& a, uint8_t* xg, float* sxg, cudaStream_t s) {
+  k_quant_scatter<<<a.d.T, 256, 0, s>>>(a, xg, sxg);
+  return cudaGetLastError();
+}
+
+// Tensor map of a row-major 2-D array [rows][cols] (element size `esize`),
+// box = 128 bytes of columns x box_rows rows, 128-byte swizzle.
+// The driver's encoder, looked up through the runtime so that the library
+// loads on hosts without a driver (it then simply has no tensor-core path).
+static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    cudaGetLastError();
+  }
+  return fn;
+}
+
+bool make_tc_map(CUtensorMap* m, bool bf16_elems, const void* ptr, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = encoder();
+  if (!encode) return false;
+  const uint64_t esize = bf16_elems ? 2 : 1;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * esize};
+  cuuint32_t box[2] = {(cuuint32_t)(kKBytes / esize), box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult r = encode(
+      m, bf16_elems ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+      const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace moe

@@ -10,6 +10,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 #include <vector>
 
@@ -32,6 +33,13 @@ struct moe_ctx {
   DevWork w{};
   bf16* stage_x = nullptr;
   bf16* stage_y = nullptr;
+  // prompt path on tcgen05: launch arguments with the fixed tensor maps
+  bool tc_ok = false;
+  TcGemm tc[5] = {};
+  size_t tc_smem[5] = {};
+  bf16* router3 = nullptr; // router as bf16 parts [Epad][3H] (hi | mid | lo)
+  uint8_t* xg = nullptr;   // e4m3 activations in slot order [max_rows*k][H]
+  float* sxg = nullptr;    // their scales [max_rows*k][H/128]
 };
 
 namespace {
@@ -62,7 +70,7 @@ bool config_supported(const moe_config* c) {
 
 // Byte layout of everything a context allocates, in allocation order.
 struct Plan {
-  size_t sizes[40];
+  size_t sizes[48];
   int n = 0;
   size_t total = 0;
   size_t add(size_t b) {
@@ -113,6 +121,9 @@ Plan make_plan(const moe_config* c) {
   p.add(T * H * 2);                       // 30 stage_x
   p.add(T * H * 2);                       // 31 stage_y
   p.add(kDecodeRows * E * 8);             // 32 tagged decode logits
+  p.add(T * k * H);                       // 33 xg (slot order)
+  p.add(T * k * (H / G) * 4);             // 34 sxg
+  p.add(((E + 127) / 128) * 128 * 3 * H * 2);  // 35 router3
   return p;
 }
 
@@ -141,6 +152,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 bool use_decode(const moe_ctx* c, int T);
 bool use_fused(const moe_ctx* c, int T);
+bool use_tc(const moe_ctx* c, int T);
 cudaError_t launch_fused(moe_ctx* c, const KArgs& a, cudaStream_t s);
 
 // Routing with the kernels the forward of T rows would use (the persistent
@@ -154,6 +166,16 @@ int run_router_and_quant(moe_ctx* c, const KArgs& a, cudaStream_t s) {
   }
   if (use_decode(c, a.d.T))
     return launch_route_decode(a, c->opt_pdl != 0, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  if (use_tc(c, a.d.T)) {
+    TcGemm rt = c->tc[kTcRouter];
+    if (!make_tc_map(&rt.b, true, a.x, (uint64_t)a.d.T, (uint64_t)a.d.H, 16)) return MOE_ERR_CUDA;
+    rt.T = a.d.T;
+    const int g_rt = std::min(c->sm_count, (a.d.T + 127) / 128 * rt.n_f);
+    if (launch_tc_gemm(kTcRouter, rt, g_rt, c->tc_smem[kTcRouter], s) != cudaSuccess ||
+        launch_topk(a, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
   if (launch_router(a, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_quant_gamma(a, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_topk(a, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -182,7 +204,7 @@ struct StageRec {
 
 // The decode kernels serve rows <= kDecodeRows for hidden sizes up to 4096.
 bool use_decode(const moe_ctx* c, int T) {
-  if (c->opt_path == 2) return false;
+  if (c->opt_path == 2 || c->opt_path == 4) return false;
   return T <= kDecodeRows && c->cfg.hidden <= 4096;
 }
 
@@ -209,6 +231,89 @@ cudaError_t launch_fused(moe_ctx* c, const KArgs& a, cudaStream_t s) {
   return launch_decode_layer(a, c->dec_grid, n, smem, c->opt_pdl != 0, s);
 }
 
+// Tensor maps and launch arguments of the four tcgen05 GEMMs.  The weight
+// and workspace addresses are fixed for the context's life; only the shared
+// expert's input map (x) is encoded per forward.  Leaves tc_ok false (the
+// grouped mma.sync kernels then serve every prompt) if any map or the shared
+// memory a CTA needs is not available.
+void setup_tc(moe_ctx* c) {
+  const moe_config& f = c->cfg;
+  const uint64_t H = f.hidden, E = f.n_experts, k = f.top_k, I = f.inter, Is = f.shared_inter;
+  const uint64_t R = (uint64_t)f.max_rows * k;
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  if (H / kGroup > 32 || I / kGroup > 32) return;  // activation scales staged per tile
+  TcGemm* g = c->tc;
+  const uint64_t Epad = (E + 127) / 128 * 128;
+  for (int i = 0; i < 5; ++i) {
+    g[i].E = (int)E;
+    g[i].status = c->w.status;
+    g[i].counts = c->w.counts;
+    g[i].off = c->w.off;
+  }
+  bool ok = true;
+  // routed gate/up: W13 [E*2I][H] x xg [slots][H]
+  ok &= make_tc_map(&g[kTcRoutedGateUp].a, false, c->L.w13, E * 2 * I, H, 128);
+  ok &= make_tc_map(&g[kTcRoutedGateUp].b, false, c->xg, R, H, 16);
+  g[kTcRoutedGateUp].n_k = (int)(H / kGroup);
+  g[kTcRoutedGateUp].n_f = (int)(I / kGroup);
+  g[kTcRoutedGateUp].a_rows_e = (int)(2 * I);
+  g[kTcRoutedGateUp].up_rows = (int)I;
+  g[kTcRoutedGateUp].ldo = (int)I;
+  g[kTcRoutedGateUp].sa = c->L.s13;
+  g[kTcRoutedGateUp].sb = c->sxg;
+  g[kTcRoutedGateUp].hq = c->w.hq;
+  g[kTcRoutedGateUp].sh = c->w.sh;
+  // routed down: W2 [E*H][I] x hq [slots][I]
+  ok &= make_tc_map(&g[kTcRoutedDown].a, false, c->L.w2, E * H, I, 128);
+  ok &= make_tc_map(&g[kTcRoutedDown].b, false, c->w.hq, R, I, 16);
+  g[kTcRoutedDown].n_k = (int)(I / kGroup);
+  g[kTcRoutedDown].n_f = (int)(H / kGroup);
+  g[kTcRoutedDown].a_rows_e = (int)H;
+  g[kTcRoutedDown].ldo = (int)H;
+  g[kTcRoutedDown].sa = c->L.s2;
+  g[kTcRoutedDown].sb = c->w.sh;
+  g[kTcRoutedDown].out = c->w.dbuf;
+  // shared gate/up: Ws13 [2Is][H] x x [rows][H] (x's map is set per forward)
+  ok &= make_tc_map(&g[kTcSharedGateUp].a, true, c->L.ws13, 2 * Is, H, 128);
+  g[kTcSharedGateUp].n_k = (int)(H / 64);
+  g[kTcSharedGateUp].n_f = (int)(Is / kGroup);
+  g[kTcSharedGateUp].up_rows = (int)Is;
+  g[kTcSharedGateUp].ldo = (int)Is;
+  g[kTcSharedGateUp].out = c->w.hs;
+  // shared down: Ws2 [H][Is] x hs [rows][Is]
+  ok &= make_tc_map(&g[kTcSharedDown].a, true, c->L.ws2, H, Is, 128);
+  ok &= make_tc_map(&g[kTcSharedDown].b, true, c->w.hs, (uint64_t)f.max_rows, Is, 16);
+  g[kTcSharedDown].n_k = (int)(Is / 64);
+  g[kTcSharedDown].n_f = (int)(H / kGroup);
+  g[kTcSharedDown].ldo = (int)H;
+  g[kTcSharedDown].out = c->w.ds;
+  // router: [hi | mid | lo] [Epad][3H] x x [rows][H] (x's map per forward)
+  ok &= make_tc_map(&g[kTcRouter].a, true, c->router3, Epad, 3 * H, 128);
+  g[kTcRouter].n_k = (int)(3 * H / 64);
+  g[kTcRouter].n_f = (int)(Epad / kGroup);
+  g[kTcRouter].ldo = (int)E;
+  g[kTcRouter].outf = c->w.logits;
+  for (int i = 0; i < 5; ++i) g[i].b_kwrap = g[i].n_k;
+  g[kTcRouter].b_kwrap = (int)(H / 64);
+  for (int i = 0; i < 5 && ok; ++i) {
+    c->tc_smem[i] = tc_gemm_smem(i, g[i].n_k);
+    ok &= c->tc_smem[i] <= (size_t)optin && setup_tc_gemm(i, c->tc_smem[i]) == cudaSuccess;
+  }
+  cudaGetLastError();
+  c->tc_ok = ok;
+}
+
+// Rows above the decode range run on the tcgen05 kernels unless the
+// warp-MMA kernels are asked for or the shape has no tcgen05 set-up.
+bool use_tc(const moe_ctx* c, int T) {
+  return !use_decode(c, T) && c->tc_ok && c->opt_path != 4;
+}
+
 int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
                 StageRec* rec = nullptr) {
   KArgs a = make_args(c, x, y, T);
@@ -222,6 +327,34 @@ int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
     LAUNCH(launch_route_decode(a, pdl, s), "route_decode");
     LAUNCH(launch_gateup_decode(a, grid, pdl, s), "gateup_decode");
     LAUNCH(launch_down_combine_decode(a, pdl, s), "down_combine_decode");
+    return MOE_OK;
+  }
+  if (use_tc(c, T)) {
+    TcGemm rt = c->tc[kTcRouter];
+    if (!make_tc_map(&rt.b, true, x, (uint64_t)T, (uint64_t)c->cfg.hidden, 16)) return MOE_ERR_CUDA;
+    TcGemm sgu = c->tc[kTcSharedGateUp];
+    sgu.b = rt.b;
+    TcGemm sdn = c->tc[kTcSharedDown];
+    rt.T = sgu.T = sdn.T = T;
+    const int tiles = (T + 127) / 128;
+    const int g_rt = std::min(c->sm_count, tiles * rt.n_f);
+    const int g_sgu = std::min(c->sm_count, tiles * sgu.n_f);
+    const int g_sdn = std::min(c->sm_count, tiles * sdn.n_f);
+    LAUNCH(launch_tc_gemm(kTcRouter, rt, g_rt, c->tc_smem[kTcRouter], s), "router_tc");
+    LAUNCH(launch_topk(a, s), "topk");
+    LAUNCH(launch_schedule(a, s), "schedule");
+    LAUNCH(launch_quant_scatter(a, c->xg, c->sxg, s), "quant_scatter");
+    LAUNCH(launch_tc_gemm(kTcSharedGateUp, sgu, g_sgu, c->tc_smem[kTcSharedGateUp], s),
+           "shared_gateup_tc");
+    LAUNCH(launch_tc_gemm(kTcRoutedGateUp, c->tc[kTcRoutedGateUp], c->sm_count,
+                          c->tc_smem[kTcRoutedGateUp], s),
+           "gateup_tc");
+    LAUNCH(launch_tc_gemm(kTcSharedDown, sdn, g_sdn, c->tc_smem[kTcSharedDown], s),
+           "shared_down_tc");
+    LAUNCH(launch_tc_gemm(kTcRoutedDown, c->tc[kTcRoutedDown], c->sm_count,
+                          c->tc_smem[kTcRoutedDown], s),
+           "down_tc");
+    LAUNCH(launch_combine(a, s), "combine");
     return MOE_OK;
   }
   LAUNCH(launch_router(a, s), "router");
@@ -280,7 +413,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     delete c;
     return MOE_ERR_CUDA;
   }
-  void* ptrs[40];
+  void* ptrs[48];
   for (int i = 0; i < plan.n; ++i) {
     if (cudaMalloc(&ptrs[i], plan.sizes[i]) != cudaSuccess) {
       cudaGetLastError();
@@ -325,6 +458,9 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   w.tlog = (unsigned long long*)ptrs[32];
   c->stage_x = (bf16*)ptrs[30];
   c->stage_y = (bf16*)ptrs[31];
+  c->xg = (uint8_t*)ptrs[33];
+  c->sxg = (float*)ptrs[34];
+  c->router3 = (bf16*)ptrs[35];
   // counters start at zero and are reset by the kernels that use them
   if (cudaMemset(w.gcount, 0, plan.sizes[25]) != cudaSuccess ||
       cudaMemset(w.status, 0, plan.sizes[29]) != cudaSuccess ||
@@ -353,6 +489,7 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     }
     cudaGetLastError();
   }
+  setup_tc(c);
   *out = c;
   return MOE_OK;
 }
@@ -398,7 +535,10 @@ int moe_load_weights(moe_ctx* c, const moe_weights* wt, int pointers_on_device, 
       cudaGetLastError();
       return MOE_ERR_CUDA;
     }
-  if (cudaStreamSynchronize(s) != cudaSuccess) {
+  // the router as exact bf16 parts for the tensor-core router
+  const int Epad = (int)((E + 127) / 128 * 128);
+  if (launch_split_router(c->L.wr, c->router3, (int)E, Epad, (int)H, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }
@@ -552,7 +692,7 @@ int moe_set_option(moe_ctx* c, int option, int value) {
   if (!c) return MOE_ERR_INVALID_ARG;
   switch (option) {
     case MOE_OPT_PATH:
-      if (value < 0 || value > 3) return MOE_ERR_INVALID_ARG;
+      if (value < 0 || value > 4) return MOE_ERR_INVALID_ARG;
       c->opt_path = value;
       return MOE_OK;
     case MOE_OPT_PDL:

@@ -1,6 +1,7 @@
 // Internal declarations shared by the kernels and the C-ABI host code.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -83,6 +84,41 @@ cudaError_t launch_schedule(const KArgs& a, cudaStream_t s);
 cudaError_t launch_gateup(const KArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_down(const KArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_combine(const KArgs& a, cudaStream_t s);
+
+// ---- prompt path on tcgen05 tensor cores (k_prompt_tc.cu) -------------------
+enum { kTcRoutedGateUp = 0, kTcRoutedDown = 1, kTcSharedGateUp = 2, kTcSharedDown = 3,
+       kTcRouter = 4 };
+
+// One grouped GEMM launch: out-features x tokens tiles of 128 x (<=128).
+struct TcGemm {
+  CUtensorMap a;       // weights [rows][K], 128-byte boxes of 128 rows
+  CUtensorMap b;       // tokens or slots [rows][K], 128-byte boxes of 16 rows
+  int n_k;             // K blocks of 128 bytes
+  int b_kwrap;         // K blocks after which the B operand's K coordinate wraps
+  int n_f;             // 128-row output tiles per token tile
+  int a_rows_e;        // weight rows per expert (routed)
+  int up_rows;         // rows from a gate tile to its up tile (gate/up kinds)
+  int E;               // experts (routed)
+  int T;               // rows (shared)
+  int ldo;             // row length of the output
+  const int* counts;   // [E] rows per expert (routed)
+  const int* off;      // [E] first slot per expert (routed)
+  const float* sa;     // weight block scales (routed)
+  const float* sb;     // activation scales [slot][n_k] (routed)
+  uint8_t* hq;         // routed gate/up: e4m3 SwiGLU rows [slot][ldo]
+  float* sh;           // routed gate/up: their scales [slot][ldo/128]
+  bf16* out;           // expert kinds: bf16 [row][ldo]
+  float* outf;         // router: fp32 logits [row][ldo]
+  int* status;         // device status flag (set when a wait gives up)
+};
+
+size_t tc_gemm_smem(int kind, int n_k);
+cudaError_t setup_tc_gemm(int kind, size_t smem);
+cudaError_t launch_tc_gemm(int kind, const TcGemm& g, int grid, size_t smem, cudaStream_t s);
+cudaError_t launch_quant_scatter(const KArgs& a, uint8_t* xg, float* sxg, cudaStream_t s);
+cudaError_t launch_split_router(const float* wr, bf16* out, int E, int Epad, int H, cudaStream_t s);
+bool make_tc_map(CUtensorMap* m, bool bf16_elems, const void* ptr, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows);
 cudaError_t launch_gather_hq(const KArgs& a, uint8_t* hq, float* sh, cudaStream_t s);
 
 // Decode path (rows <= kDecodeRows): three kernels chained with programmatic

@@ -128,10 +128,10 @@ int moe_route(moe_ctx* ctx, const void* x, int rows, int32_t* idx, float* w, voi
  * implicit synchronisation.  This call is a library convenience; the pages
  * that define the layer have no counterpart to it.
  *
- * Computes what moe_route computes, with the two router kernels moe_route
- * runs above 16 rows (fp32 logits x . router^T, the top_k largest with ties
- * to the lower expert, softmax over the selection): x bf16 [rows][hidden],
- * router fp32 [n_experts][hidden],
+ * Computes what moe_route computes, with the CUDA-core router kernels that
+ * moe_route runs when MOE_OPT_PATH is 4 (fp32 logits x . router^T, the top_k
+ * largest with ties to the lower expert, softmax over the selection): x bf16
+ * [rows][hidden], router fp32 [n_experts][hidden],
  * idx int32 [rows][top_k] in rank order, w fp32 [rows][top_k]; all device
  * pointers on the current device, owned by the caller.  Asynchronous on
  * `stream`.
@@ -167,9 +167,12 @@ int moe_quantize(moe_ctx* ctx, const void* x, int rows, uint8_t* codes, float* s
 int moe_expert_activations(moe_ctx* ctx, int rows, uint8_t* hq, float* sh, void* stream);
 
 /* Options.  MOE_OPT_PATH: 0 = automatic (rows <= 16: the persistent decode
- * kernel, else the grouped prompt kernels), 1 = the same as 0, 2 = always
- * the grouped prompt kernels, 3 = rows <= 16 on three chained decode kernels
- * instead of the persistent one.  MOE_OPT_PDL: 1 = launch with programmatic
+ * kernel, else the grouped prompt kernels on the tcgen05 tensor cores),
+ * 1 = the same as 0, 2 = always the grouped prompt kernels, 3 = rows <= 16 on
+ * three chained decode kernels instead of the persistent one, 4 = always the
+ * grouped prompt kernels with warp-level MMAs instead of tcgen05 (the path
+ * every forward takes when a context's shape leaves no room for the tcgen05
+ * kernels: hidden or inter above 4096).  MOE_OPT_PDL: 1 = launch with programmatic
  * dependent launch so a layer's immutable weight reads overlap the previous
  * kernel's tail (default), 0 = plain launches. */
 enum { MOE_OPT_PATH = 1, MOE_OPT_PDL = 2 };

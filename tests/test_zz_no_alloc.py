@@ -30,8 +30,9 @@ def _layer(name, dev, max_rows):
     moe = m.MoELayer(m.LayerShape(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter,
                                   s.group), max_rows=max_rows)
     moe.load(layer)
-    # moe_route on the router kernels moe_route_static also runs
-    moe.set_option(m.MOE_OPT_PATH, m.PATH_PROMPT)
+    # moe_route on the router kernels moe_route_static also runs (the
+    # CUDA-core router of the warp-MMA prompt path)
+    moe.set_option(m.MOE_OPT_PATH, m.PATH_PROMPT_MMA)
     return wl, seed, layer, moe
 
 
