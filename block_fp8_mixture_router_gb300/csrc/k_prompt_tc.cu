@@ -22,9 +22,9 @@
 // for it.  The tile's outputs are transposed through shared memory and
 // stored token-major with coalesced 128/256-byte rows.
 //
-// CTA roles (320 threads): warp 0 lane 0 issues TMA, warp 1 owns TMEM and
-// lane 0 issues the MMAs, warps 2-9 are the epilogue (warp w reads TMEM lanes
-// 32*(w%4).. and column half (w-2)/4 of the tile's tokens).  Every wait is bounded; a wait that
+// CTA roles (576 threads): warp 0 lane 0 issues TMA, warp 1 owns TMEM and
+// lane 0 issues the MMAs, warps 2-17 are the epilogue (warp w reads TMEM
+// lanes 32*(w%4).. and column quarter (w-2)/4 of the tile's tokens).  Every wait is bounded; a wait that
 // gives up sets the status flag and all roles leave their loops.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -36,7 +36,8 @@ namespace moe {
 
 namespace {
 
-constexpr int kTcThreads = 320;
+constexpr int kEpiWarps = 16;                    // 4 per TMEM lane quarter
+constexpr int kTcThreads = 64 + 32 * kEpiWarps;  // + the TMA and MMA warps
 constexpr int kTile = 128;        // output features per tile (M)
 constexpr int kKBytes = 128;      // bytes of K per stage (one 128B swizzle row)
 constexpr int kATileBytes = kTile * kKBytes;
@@ -47,15 +48,18 @@ constexpr int kTmemCols = 512;
 template <int kKind>
 struct Cfg {
   static constexpr bool kF8 = kKind == kTcRoutedGateUp || kKind == kTcRoutedDown;
-  static constexpr bool kPair = kKind == kTcRoutedGateUp || kKind == kTcSharedGateUp;
+  // gate/up kinds: a gate tile and its up tile; routed down: two adjacent
+  // output tiles.  Either way two A tiles share the token operand.
+  static constexpr bool kSwiGLU = kKind == kTcRoutedGateUp || kKind == kTcSharedGateUp;
+  static constexpr bool kPair = kSwiGLU || kKind == kTcRoutedDown;
   static constexpr bool kRouted = kF8;
   static constexpr bool kRouter = kKind == kTcRouter;
   // Tokens per tile (N).  The block-FP8 kinds keep their promoted
-  // accumulators in registers (gate and up: 2 x kN/2 per epilogue thread),
-  // which at 10 warps (3 on some SM sub-partitions, 168 registers each)
-  // leaves room for 64 tokens; the bf16 kinds accumulate in TMEM.
+  // accumulators in registers (gate and up: 2 x kN/4 per epilogue thread,
+  // within the ~100 registers a thread has at 18 warps per CTA); the bf16
+  // kinds accumulate in TMEM.
   static constexpr int kN = kF8 ? 64 : 128;
-  static constexpr int kCols = kN / 2;  // columns per epilogue thread
+  static constexpr int kCols = kN / (kEpiWarps / 4);  // token columns per epilogue thread
   // TMEM accumulator buffers (gate at +0, up at +kN) and their count
   static constexpr int kAccCols = (kPair ? 2 : 1) * kN;
   static constexpr int kNumBuf = (kTmemCols / kAccCols) < 4 ? (kTmemCols / kAccCols) : 4;
@@ -65,18 +69,27 @@ struct Cfg {
 
 struct Item {
   int e, f, row0, n;
+  int kb0, kb1;  // K blocks of this item (a K split of the router, else all)
+  int ks;        // its K split (router), else 0
 };
 
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
+// Named barrier of the epilogue warps only.
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync 1, %0;\n" ::"n"(32 * kEpiWarps) : "memory");
+}
 
-// Work item w: token tile w / n_f (routed: tiles of every expert in expert
-// order; otherwise: tiles of all rows), output tile w % n_f.
+// Work item w = (token tile * n_f + output tile) * ksplit + K split; token
+// tiles of every expert in expert order (routed) or of all rows.
 template <bool kRouted, int kN>
 __device__ __forceinline__ Item decode_item(const TcGemm& g, const int* s_pre, const int* s_off,
                                             const int* s_cnt, int w) {
   Item it;
-  const int tile = w / g.n_f;
-  it.f = w - tile * g.n_f;
+  const int wf = w / g.ksplit;
+  it.ks = w - wf * g.ksplit;
+  it.kb0 = (int)((long long)it.ks * g.n_k / g.ksplit);
+  it.kb1 = (int)((long long)(it.ks + 1) * g.n_k / g.ksplit);
+  const int tile = wf / g.n_f;
+  it.f = wf - tile * g.n_f;
   if constexpr (kRouted) {
     int lo = 0, hi = g.E;  // largest e with s_pre[e] <= tile
     while (hi - lo > 1) {
@@ -95,16 +108,35 @@ __device__ __forceinline__ Item decode_item(const TcGemm& g, const int* s_pre, c
   return it;
 }
 
-// Activation scales of an item's tokens: rows row0..row0+n-1 of sb
-// [rows][n_k], copied as one 16-byte-aligned span.  Returns the span's byte
-// offset and length; the item's first scale sits `lead` bytes into it.
-__device__ __forceinline__ void scale_span(const TcGemm& g, const Item& it, uint32_t* off,
-                                           uint32_t* bytes, uint32_t* lead) {
-  const uint64_t b0 = (uint64_t)it.row0 * g.n_k * 4, b1 = (uint64_t)(it.row0 + it.n) * g.n_k * 4;
+// Byte range [b0, b1) of an array widened to 16-byte boundaries for one bulk
+// copy: the copy starts at *off, is *bytes long, and byte b0 sits *lead bytes
+// into it.
+struct Span {
+  uint64_t off;
+  uint32_t bytes, lead;
+};
+
+__device__ __forceinline__ Span span16(uint64_t b0, uint64_t b1) {
   const uint64_t a0 = b0 & ~15ull, a1 = (b1 + 15) & ~15ull;
-  *off = (uint32_t)a0;
-  *bytes = (uint32_t)(a1 - a0);
-  *lead = (uint32_t)(b0 - a0);
+  return Span{a0, (uint32_t)(a1 - a0), (uint32_t)(b0 - a0)};
+}
+
+// The scales an item needs, as three spans copied into one scale slot:
+// [0] the activation scales of its tokens (rows row0..row0+n-1 of sb
+// [rows][n_k]), [1] and [2] the weight block scales of its two A tiles (n_k
+// each).  Slot layout: span 0 at 0, span 1 at kSpanA, span 2 at kSpanA + kSpanW.
+struct ItemScales {
+  Span s[3];
+};
+
+__device__ __forceinline__ ItemScales item_scales(const TcGemm& g, const Item& it) {
+  ItemScales r;
+  r.s[0] = span16((uint64_t)it.row0 * g.n_k * 4, (uint64_t)(it.row0 + it.n) * g.n_k * 4);
+  const uint64_t w0 = ((uint64_t)it.e * (g.a_rows_e / 128) + (uint64_t)it.f * (g.f_rows / 128)) * g.n_k * 4;
+  const uint64_t w1 = w0 + (uint64_t)(g.up_rows / 128) * g.n_k * 4;
+  r.s[1] = span16(w0, w0 + (uint64_t)g.n_k * 4);
+  r.s[2] = span16(w1, w1 + (uint64_t)g.n_k * 4);
+  return r;
 }
 
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
@@ -128,7 +160,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
   uint8_t* stages = base;
   float* tbuf = reinterpret_cast<float*>(base + S * C::kStageBytes);  // [kN col][128 row]
   uint8_t* sbs = reinterpret_cast<uint8_t*>(tbuf + kN * kTile);       // 2 x scale spans
-  const uint32_t sbs_slot = kF8 ? (uint32_t)((kN * g.n_k * 4 + 32 + 15) & ~15) : 0u;
+  const uint32_t span_a = (uint32_t)((kN * g.n_k * 4 + 32 + 15) & ~15);
+  const uint32_t span_w = (uint32_t)((g.n_k * 4 + 32 + 15) & ~15);
+  const uint32_t sbs_slot = kF8 ? span_a + 2 * span_w : 0u;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sbs + 2 * sbs_slot);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
@@ -150,11 +184,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
     }
     for (int i = 0; i < NB; ++i) {
       tc::mbar_init(&tfull[i], 1);
-      tc::mbar_init(&tempty[i], 8);
+      tc::mbar_init(&tempty[i], kEpiWarps);
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&sfull[i], 1);
-      tc::mbar_init(&sempty[i], 8);
+      tc::mbar_init(&sempty[i], kEpiWarps);
     }
     *s_abort = 0;
     tc::fence_barrier_init();
@@ -203,7 +237,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
   const uint32_t tmem = *s_tmem;
   if constexpr (kRouted) n_tiles = s_pre[g.E];
   else n_tiles = (g.T + kN - 1) / kN;
-  const int n_items = n_tiles * g.n_f;
+  const int n_items = n_tiles * g.n_f * g.ksplit;
   const int n_k = g.n_k;
   const int kx = kF8 ? kKBytes : kKBytes / 2;  // K elements per stage
 
@@ -218,17 +252,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
         if constexpr (kF8) {
           // this item's activation scales into scale slot j % 2
           const int sl = j & 1;
-          if (!tc::wait_bounded(&sempty[sl], ((j >> 1) & 1) ^ 1u, s_abort, g.status)) break;
-          uint32_t off, bytes, lead;
-          scale_span(g, it, &off, &bytes, &lead);
-          tc::mbar_arrive_expect_tx(&sfull[sl], bytes);
-          bulk_copy_g2s(sbs + sl * sbs_slot, reinterpret_cast<const uint8_t*>(g.sb) + off, bytes,
+          if (!tc::wait_bounded(&sempty[sl], ((j >> 1) & 1) ^ 1u, s_abort, g.status)) {
+            ok = false;
+            break;
+          }
+          const ItemScales sc = item_scales(g, it);
+          uint8_t* slot = sbs + sl * sbs_slot;
+          tc::mbar_arrive_expect_tx(&sfull[sl], sc.s[0].bytes + sc.s[1].bytes + sc.s[2].bytes);
+          bulk_copy_g2s(slot, reinterpret_cast<const uint8_t*>(g.sb) + sc.s[0].off, sc.s[0].bytes,
                         &sfull[sl]);
+          bulk_copy_g2s(slot + span_a, reinterpret_cast<const uint8_t*>(g.sa) + sc.s[1].off,
+                        sc.s[1].bytes, &sfull[sl]);
+          bulk_copy_g2s(slot + span_a + span_w, reinterpret_cast<const uint8_t*>(g.sa) + sc.s[2].off,
+                        sc.s[2].bytes, &sfull[sl]);
         }
-        const int arow = it.e * g.a_rows_e + it.f * kTile;
+        const int arow = it.e * g.a_rows_e + it.f * g.f_rows;
         const int nb = (it.n + kBBox - 1) / kBBox;
         const uint32_t bytes = (kPair ? 2 : 1) * kATileBytes + nb * kBBoxBytes;
-        for (int kb = 0; kb < n_k; ++kb) {
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
           if (!tc::wait_bounded(&empty[st], ph ^ 1u, s_abort, g.status)) { ok = false; break; }
           uint8_t* sp = stages + st * C::kStageBytes;
           const int bx = (kb % g.b_kwrap) * kx;
@@ -262,8 +303,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
         const Item it = decode_item<kRouted, kN>(g, s_pre, s_off, s_cnt, w);
         const int n16 = (it.n + 15) & ~15;
         const uint32_t idesc = kF8 ? tc::idesc_f8(kTile, n16) : tc::idesc_bf16(kTile, n16);
-        for (int kb = 0; kb < n_k; ++kb) {
-          if (kF8 || kb == 0) {
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
+          if (kF8 || kb == it.kb0) {
             if (!tc::wait_bounded(&tempty[tb], tph ^ 1u, s_abort, g.status)) { ok = false; break; }
             tc::fence_after_sync();
           }
@@ -275,14 +316,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
           const uint32_t d0 = tmem + tb * kAcc;
 #pragma unroll
           for (int kk = 0; kk < kKBytes / 32; ++kk) {
-            const uint32_t acc = (kk > 0 || (!kF8 && kb > 0)) ? 1u : 0u;
+            const uint32_t acc = (kk > 0 || (!kF8 && kb > it.kb0)) ? 1u : 0u;
             const uint64_t bdesc = tc::sw128_desc(sb + 32 * kk);
             tc::mma<kF8>(d0, tc::sw128_desc(sa0 + 32 * kk), bdesc, idesc, acc);
             if constexpr (kPair) tc::mma<kF8>(d0 + kN, tc::sw128_desc(sa1 + 32 * kk), bdesc, idesc, acc);
           }
           tc::commit(&empty[st]);
           if (++st == (uint32_t)S) { st = 0; ph ^= 1u; }
-          if (kF8 || kb == n_k - 1) {
+          if (kF8 || kb == it.kb1 - 1) {
             tc::commit(&tfull[tb]);
             if (++tb == (uint32_t)NB) { tb = 0; tph ^= 1u; }
           }
@@ -293,7 +334,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
     // ---- epilogue ----
     const int ew = warp - 2;
     const int q = warp & 3;
-    const int c0 = kCols * (ew >> 2);
+    const int c0 = kCols * (ew >> 2);  // this warp's first token column
     const int row = 32 * q + lane;
     const uint32_t tl = (uint32_t)(32 * q) << 16;
     uint32_t tb = 0, tph = 0;
@@ -302,46 +343,51 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
     for (int w = blockIdx.x, j = 0; w < n_items; w += gridDim.x, ++j) {
       const Item it = decode_item<kRouted, kN>(g, s_pre, s_off, s_cnt, w);
       const int n16 = (it.n + 15) & ~15;
-      const float* sc_tok = nullptr;  // this item's scales, [token][n_k]
+      // this item's scales in the slot: [token][n_k], and n_k per A tile
+      const float* sc_tok = nullptr;
+      const float* s_wg = nullptr;
+      const float* s_wu = nullptr;
       if constexpr (kF8) {
         const int sl = j & 1;
         tc::wait_bounded(&sfull[sl], (j >> 1) & 1, s_abort, g.status);
-        uint32_t off, bytes, lead;
-        scale_span(g, it, &off, &bytes, &lead);
-        sc_tok = reinterpret_cast<const float*>(sbs + sl * sbs_slot + lead);
+        const ItemScales sc = item_scales(g, it);
+        const uint8_t* slot = sbs + sl * sbs_slot;
+        sc_tok = reinterpret_cast<const float*>(slot + sc.s[0].lead);
+        s_wg = reinterpret_cast<const float*>(slot + span_a + sc.s[1].lead);
+        s_wu = reinterpret_cast<const float*>(slot + span_a + span_w + sc.s[2].lead);
       }
       float acc0[kCols], acc1[kCols];
 #pragma unroll
       for (int i = 0; i < kCols; ++i) { acc0[i] = 0.0f; acc1[i] = 0.0f; }
-      const float* sa_g = g.sa + ((size_t)it.e * (g.a_rows_e / kTile) + it.f) * n_k;
-      const float* sa_u = sa_g + (size_t)(g.up_rows / kTile) * n_k;
-      for (int kb = (kF8 ? 0 : n_k - 1); kb < n_k; ++kb) {
-        float wg = 0.0f, wu = 0.0f;
-        if constexpr (kF8) {
-          wg = __ldg(sa_g + kb);
-          if constexpr (kPair) wu = __ldg(sa_u + kb);
-        }
+      for (int kb = (kF8 ? it.kb0 : it.kb1 - 1); kb < it.kb1; ++kb) {
         tc::wait_bounded(&tfull[tb], tph, s_abort, g.status);
         __syncwarp();  // lanes may leave the poll at different tries
         tc::fence_after_sync();
         const uint32_t ta0 = tmem + tl + tb * kAcc + c0;
-        if constexpr (!kF8) epi_sync();  // every warp is done reading tbuf
-#pragma unroll
-        for (int c4 = 0; c4 < kCols / 16; ++c4) {
-          if (c0 + 16 * c4 < n16) {
+        if constexpr (kF8) {
+          // block-FP8: partial x (weight block scale x token scale), all
+          // kCols columns of both tiles under one TMEM wait
+          static_assert(kCols == 16, "one x16 load per tile");
+          const float wg = s_wg[kb], wu = s_wu[kb];
+          if (c0 < n16) {
             uint32_t va[16], vb[16];
-            if constexpr (kPair) tc::tmem_ld16x2(ta0 + 16 * c4, ta0 + kN + 16 * c4, va, vb);
-            else tc::tmem_ld16(ta0 + 16 * c4, va);
-            if constexpr (kF8) {
+            tc::tmem_ld16x2(ta0, ta0 + kN, va, vb);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float s = sc_tok[(c0 + 16 * c4 + i) * n_k + kb];
-                acc0[16 * c4 + i] = fmaf(__uint_as_float(va[i]), wg * s, acc0[16 * c4 + i]);
-                if constexpr (kPair)
-                  acc1[16 * c4 + i] = fmaf(__uint_as_float(vb[i]), wu * s, acc1[16 * c4 + i]);
-              }
-            } else {
-              // bf16: the whole K is in this accumulator
+            for (int i = 0; i < 16; ++i) {
+              const float s = sc_tok[(c0 + i) * n_k + kb];
+              acc0[i] = fmaf(__uint_as_float(va[i]), wg * s, acc0[i]);
+              acc1[i] = fmaf(__uint_as_float(vb[i]), wu * s, acc1[i]);
+            }
+          }
+        } else {
+          // bf16: the whole K is in this accumulator
+          epi_sync();  // every warp is done reading tbuf
+#pragma unroll
+          for (int c4 = 0; c4 < kCols / 16; ++c4) {
+            if (c0 + 16 * c4 < n16) {
+              uint32_t va[16], vb[16];
+              if constexpr (kPair) tc::tmem_ld16x2(ta0 + 16 * c4, ta0 + kN + 16 * c4, va, vb);
+              else tc::tmem_ld16(ta0 + 16 * c4, va);
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
                 float v = __uint_as_float(va[i]);
@@ -360,43 +406,80 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
       if constexpr (kF8) {
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sempty[j & 1]);  // scale slot free
-        epi_sync();  // every warp is done reading tbuf
-#pragma unroll
-        for (int i = 0; i < kCols; ++i) {
-          float v = acc0[i];
-          if constexpr (kPair) v = silu_f32(bf16_round(acc0[i])) * bf16_round(acc1[i]);
-          tbuf[(c0 + i) * kTile + row] = v;
-        }
       }
-      epi_sync();
-      // ---- store: one token column per warp, 128 features per column ----
-      for (int col = ew; col < it.n; col += 8) {
-        const float4 v = *reinterpret_cast<const float4*>(tbuf + col * kTile + 4 * lane);
-        const size_t r = (size_t)(it.row0 + col);
-        if constexpr (kKind == kTcRoutedGateUp) {
-          float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-          m = warp_max(m);
-          const float s = group_scale(m);
-          *reinterpret_cast<uint32_t*>(g.hq + r * g.ldo + it.f * kTile + 4 * lane) =
-              quant4(v.x, v.y, v.z, v.w, s);
-          if (lane == 0) g.sh[r * (g.ldo / kTile) + it.f] = s;
-        } else if constexpr (kKind == kTcRouter) {
-          const int e = it.f * kTile + 4 * lane;  // logits [row][E], fp32
-          float* o = g.outf + r * g.ldo + e;
-          if (e + 3 < g.ldo) {
-            *reinterpret_cast<float4*>(o) = v;
-          } else {
-            if (e < g.ldo) o[0] = v.x;
-            if (e + 1 < g.ldo) o[1] = v.y;
-            if (e + 2 < g.ldo) o[2] = v.z;
+      // output tiles of this item: one for SwiGLU and the bf16 kinds, two for
+      // the routed down pair; each goes through tbuf
+      constexpr int kOut = (kF8 && !C::kSwiGLU) ? 2 : 1;
+#pragma unroll
+      for (int ot = 0; ot < kOut; ++ot) {
+        if constexpr (kF8) {
+          epi_sync();  // every warp is done reading tbuf
+#pragma unroll
+          for (int i = 0; i < kCols; ++i) {
+            float v;
+            if constexpr (C::kSwiGLU) v = silu_f32(bf16_round(acc0[i])) * bf16_round(acc1[i]);
+            else v = ot == 0 ? acc0[i] : acc1[i];
+            tbuf[(c0 + i) * kTile + row] = v;
           }
-        } else {
-          __nv_bfloat162 p0 = __floats2bfloat162_rn(v.x, v.y);
-          __nv_bfloat162 p1 = __floats2bfloat162_rn(v.z, v.w);
-          uint2 o;
-          o.x = *reinterpret_cast<uint32_t*>(&p0);
-          o.y = *reinterpret_cast<uint32_t*>(&p1);
-          *reinterpret_cast<uint2*>(g.out + r * g.ldo + it.f * kTile + 4 * lane) = o;
+        }
+        epi_sync();
+        // ---- store: token columns ew, ew+8, ... (128 features each), four
+        // columns at a time so their reductions and divisions overlap ----
+        const int fcol = it.f * g.f_rows + ot * kTile;  // first output feature
+        for (int c0s = ew; c0s < it.n; c0s += 4 * kEpiWarps) {
+          float4 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int col = c0s + kEpiWarps * u;
+            v[u] = col < it.n ? *reinterpret_cast<const float4*>(tbuf + col * kTile + 4 * lane)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          if constexpr (kKind == kTcRoutedGateUp) {
+            float m[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              m[u] = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+              for (int u = 0; u < 4; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], o));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int col = c0s + kEpiWarps * u;
+              if (col < it.n) {
+                const size_t r = (size_t)(it.row0 + col);
+                const float sq = group_scale(m[u]);
+                *reinterpret_cast<uint32_t*>(g.hq + r * g.ldo + fcol + 4 * lane) =
+                    quant4(v[u].x, v[u].y, v[u].z, v[u].w, sq);
+                if (lane == 0) g.sh[r * (g.ldo / kTile) + fcol / kTile] = sq;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int col = c0s + kEpiWarps * u;
+              if (col >= it.n) continue;
+              const size_t r = (size_t)(it.row0 + col);
+              if constexpr (kKind == kTcRouter) {
+                const int e = fcol + 4 * lane;  // logits [row][E], fp32
+                float* o = g.outf + ((size_t)it.ks * g.T + r) * g.ldo + e;
+                if (e + 3 < g.ldo) {
+                  *reinterpret_cast<float4*>(o) = v[u];
+                } else {
+                  if (e < g.ldo) o[0] = v[u].x;
+                  if (e + 1 < g.ldo) o[1] = v[u].y;
+                  if (e + 2 < g.ldo) o[2] = v[u].z;
+                }
+              } else {
+                __nv_bfloat162 p0 = __floats2bfloat162_rn(v[u].x, v[u].y);
+                __nv_bfloat162 p1 = __floats2bfloat162_rn(v[u].z, v[u].w);
+                uint2 o;
+                o.x = *reinterpret_cast<uint32_t*>(&p0);
+                o.y = *reinterpret_cast<uint32_t*>(&p1);
+                *reinterpret_cast<uint2*>(g.out + r * g.ldo + fcol + 4 * lane) = o;
+              }
+            }
+          }
         }
       }
     }
@@ -412,7 +495,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
 template <int kKind>
 size_t smem_bytes(int n_k) {
   using C = Cfg<kKind>;
-  const size_t slot = C::kF8 ? (((size_t)C::kN * n_k * 4 + 32 + 15) & ~(size_t)15) : 0;
+  const size_t slot = C::kF8 ? (((size_t)C::kN * n_k * 4 + 32 + 15) & ~(size_t)15) +
+                                   2 * (((size_t)n_k * 4 + 32 + 15) & ~(size_t)15)
+                             : 0;
   return 1024 + (size_t)C::kStages * C::kStageBytes + (size_t)C::kN * kTile * 4 + 2 * slot +
          (2 * C::kStages + 2 * C::kNumBuf + 4) * 8 + 16 + (3 * kMaxExperts + 1) * 4;
 }

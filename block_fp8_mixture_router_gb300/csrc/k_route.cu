@@ -82,67 +82,176 @@ cudaError_t launch_topk(const KArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// One warp per row: logits[t][e] = sum over splits s = 0..ks-1, in that
+// order, of part[s][t][e]; then the top-k of the row.
+__global__ void __launch_bounds__(256) k_topk_splits(KArgs a, const float* __restrict__ part,
+                                                     int ks) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= a.d.T) return;
+  const int E = a.d.E, lane = threadIdx.x & 31;
+  float* row = a.w.logits + (size_t)t * E;
+  const size_t stride = (size_t)a.d.T * E;
+  const float* pr = part + (size_t)t * E;
+  // lane holds experts lane + 32 i; each split's loads are issued together
+  float acc[kMaxExperts / 32];
+#pragma unroll
+  for (int i = 0; i < kMaxExperts / 32; ++i) {
+    const int e = lane + 32 * i;
+    acc[i] = e < E ? __ldg(pr + e) : 0.0f;
+  }
+#pragma unroll 4
+  for (int sp = 1; sp < ks; ++sp) {
+    float v[kMaxExperts / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? __ldg(pr + sp * stride + e) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) acc[i] += v[i];
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxExperts / 32; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) row[e] = acc[i];
+  }
+  __syncwarp();
+  topk_row(row, E, a.d.k, a.w.idx + (size_t)t * a.d.k, a.w.wts + (size_t)t * a.d.k);
+}
+
+cudaError_t launch_topk_splits(const KArgs& a, const float* part, int ks, cudaStream_t s) {
+  k_topk_splits<<<(a.d.T + 7) / 8, 256, 0, s>>>(a, part, ks);
+  return cudaGetLastError();
+}
+
 // ---- schedule: stable slots sorted by (expert, row), and expert chunks ----
 // A pair p = t*k + j routes row t to expert e = idx[p].  Rows pick distinct
 // experts, so an expert's slots in row order are its rank among the rows
-// that chose it: bit t of bitmap[e] marks row t, and a running popcount over
-// the bitmap words gives every rank.  One CTA; no ordering depends on timing.
-__global__ void __launch_bounds__(1024) k_schedule(KArgs a) {
-  __shared__ int s_cnt[kMaxExperts];
+// that chose it.  Two kernels, each one CTA per block of 256 rows:
+//   count:  a bitmap of the block's rows per expert gives every pair its rank
+//           within the block and each expert's count in the block;
+//   finish: slot = (rows of all experts before e) + (rows of e in earlier
+//           blocks) + (rank in the block).  Block 0 also writes the per-expert
+//           counts, offsets and the chunk list of the warp-MMA kernels.
+// Nothing depends on timing: every sum has a fixed order.
+constexpr int kSchedRows = 256;  // rows per block (8 bitmap words)
+
+__global__ void __launch_bounds__(256) k_sched_count(KArgs a, int* __restrict__ rank,
+                                                     int* __restrict__ blk_cnt) {
+  __shared__ uint32_t bm[kMaxExperts][kSchedRows / 32];
+  const int T = a.d.T, k = a.d.k, E = a.d.E, b = blockIdx.x, tid = threadIdx.x;
+  const int t0 = b * kSchedRows, nt = min(kSchedRows, T - t0);
+  for (int i = tid; i < E * (kSchedRows / 32); i += 256) (&bm[0][0])[i] = 0u;
+  __syncthreads();
+  const int p0 = t0 * k, np = nt * k;
+  for (int i = tid; i < np; i += 256) {
+    const int tl = i / k, e = __ldg(a.w.idx + p0 + i);
+    atomicOr(&bm[e][tl >> 5], 1u << (tl & 31));
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += 256) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < kSchedRows / 32; ++w) c += __popc(bm[e][w]);
+    blk_cnt[(size_t)b * E + e] = c;
+  }
+  for (int i = tid; i < np; i += 256) {
+    const int tl = i / k, e = __ldg(a.w.idx + p0 + i);
+    int r = __popc(bm[e][tl >> 5] & ((1u << (tl & 31)) - 1u));
+    for (int w = 0; w < (tl >> 5); ++w) r += __popc(bm[e][w]);
+    rank[p0 + i] = r;
+  }
+}
+
+__global__ void __launch_bounds__(256) k_sched_finish(KArgs a, const int* __restrict__ rank,
+                                                      const int* __restrict__ blk_cnt, int nb) {
+  __shared__ int s_pre[kMaxExperts];   // rows of e in earlier blocks
   __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_tot[kMaxExperts];
   __shared__ int s_ch[kMaxExperts + 1];
-  const int T = a.d.T, k = a.d.k, E = a.d.E, W = (T + 31) / 32;
-  const int tid = threadIdx.x;
-  uint32_t* bm = a.w.bitmap;
-  for (int i = tid; i < E * W; i += blockDim.x) bm[i] = 0u;
-  __syncthreads();
-  for (int p = tid; p < T * k; p += blockDim.x) {
-    int t = p / k, e = a.w.idx[p];
-    atomicOr(&bm[(size_t)e * W + (t >> 5)], 1u << (t & 31));
+  __shared__ int s_wsum[2][8];
+  const int T = a.d.T, k = a.d.k, E = a.d.E, b = blockIdx.x, tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  int tot = 0, chs = 0;
+  if (tid < E) {
+    int pre = 0, rest = 0;
+    for (int bb = 0; bb < b; ++bb) pre += __ldg(blk_cnt + (size_t)bb * E + tid);
+    for (int bb = b; bb < nb; ++bb) rest += __ldg(blk_cnt + (size_t)bb * E + tid);
+    s_pre[tid] = pre;
+    tot = pre + rest;
+    s_tot[tid] = tot;
+    chs = (tot + kChunk - 1) / kChunk;
   }
-  __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int w = 0; w < W; ++w) {
-      a.w.wprefix[(size_t)e * W + w] = run;
-      run += __popc(__ldcg(&bm[(size_t)e * W + w]));
+  // exclusive scans over experts (thread e holds expert e): warps, then warp sums
+  int ic = tot, ich = chs;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, ic, o);
+    const int vh = __shfl_up_sync(0xffffffffu, ich, o);
+    if (lane >= o) {
+      ic += v;
+      ich += vh;
     }
-    s_cnt[e] = run;
+  }
+  if (lane == 31) {
+    s_wsum[0][warp] = ic;
+    s_wsum[1][warp] = ich;
   }
   __syncthreads();
+  int wo = 0, wch = 0;
+  for (int w = 0; w < warp; ++w) {
+    wo += s_wsum[0][w];
+    wch += s_wsum[1][w];
+  }
+  if (tid < E) {
+    s_off[tid] = wo + ic - tot;
+    s_ch[tid] = wch + ich - chs;
+  }
   if (tid == 0) {
     int o = 0, c = 0;
-    for (int e = 0; e < E; ++e) {
-      s_off[e] = o;
-      s_ch[e] = c;
-      o += s_cnt[e];
-      c += (s_cnt[e] + kChunk - 1) / kChunk;
+    for (int w = 0; w < 8; ++w) {
+      o += s_wsum[0][w];
+      c += s_wsum[1][w];
     }
     s_off[E] = o;
     s_ch[E] = c;
-    *a.w.n_chunks = c;
   }
   __syncthreads();
-  for (int p = tid; p < T * k; p += blockDim.x) {
-    int t = p / k, e = a.w.idx[p];
-    size_t wi = (size_t)e * W + (t >> 5);
-    uint32_t below = __ldcg(&bm[wi]) & ((1u << (t & 31)) - 1u);
-    int slot = s_off[e] + a.w.wprefix[wi] + __popc(below);
+  const int p0 = b * kSchedRows * k, np = min(kSchedRows, T - b * kSchedRows) * k;
+  for (int i = tid; i < np; i += 256) {
+    const int p = p0 + i, e = __ldg(a.w.idx + p);
+    const int slot = s_off[e] + s_pre[e] + rank[p];
     a.w.pair_of_slot[slot] = p;
     a.w.slot_of_pair[p] = slot;
   }
-  for (int e = tid; e < E; e += blockDim.x) {
-    a.w.counts[e] = s_cnt[e];
-    a.w.off[e] = s_off[e];
-    int n = s_cnt[e];
-    for (int c = 0; c * kChunk < n; ++c)
-      a.w.chunks[s_ch[e] + c] = make_int4(e, s_off[e] + c * kChunk, min(kChunk, n - c * kChunk), 0);
+  if (b == 0) {
+    for (int e = tid; e < E; e += 256) {
+      a.w.counts[e] = s_tot[e];
+      a.w.off[e] = s_off[e];
+    }
+    if (tid == 0) {
+      a.w.off[E] = s_off[E];
+      *a.w.n_chunks = s_ch[E];
+    }
+    // expert chunks of <= kChunk rows (the warp-MMA expert kernels' work list)
+    for (int e = warp; e < E; e += 8) {
+      const int n = s_tot[e];
+      for (int c = lane; c * kChunk < n; c += 32)
+        a.w.chunks[s_ch[e] + c] =
+            make_int4(e, s_off[e] + c * kChunk, min(kChunk, n - c * kChunk), 0);
+    }
   }
-  if (tid == 0) a.w.off[E] = s_off[E];
 }
 
+cudaError_t setup_schedule() { return cudaSuccess; }
+
 cudaError_t launch_schedule(const KArgs& a, cudaStream_t s) {
-  k_schedule<<<1, 1024, 0, s>>>(a);
+  const int nb = (a.d.T + kSchedRows - 1) / kSchedRows;
+  int* rank = a.w.sched_rank;
+  int* blk = a.w.sched_blk;
+  k_sched_count<<<nb, 256, 0, s>>>(a, rank, blk);
+  if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
+  k_sched_finish<<<nb, 256, 0, s>>>(a, rank, blk, nb);
   return cudaGetLastError();
 }
 

@@ -38,6 +38,8 @@ struct moe_ctx {
   TcGemm tc[5] = {};
   size_t tc_smem[5] = {};
   bf16* router3 = nullptr; // router as bf16 parts [Epad][3H] (hi | mid | lo)
+  float* logits_part = nullptr;  // router K-split partial logits [splits][rows][E]
+  int part_rows = 0;             // splits x rows the partial buffer holds
   uint8_t* xg = nullptr;   // e4m3 activations in slot order [max_rows*k][H]
   float* sxg = nullptr;    // their scales [max_rows*k][H/128]
 };
@@ -80,6 +82,22 @@ struct Plan {
     return b;
   }
 };
+
+// Rows (splits x rows) of the router's partial-logit buffer: up to 16 splits
+// while splits x rows stays within 16384.
+size_t router_part_rows(const moe_config* c) {
+  return std::min<size_t>(16384, 16 * (size_t)c->max_rows);
+}
+
+// K splits of the tensor-core router for T rows: enough items to give every
+// SM one, within the partial buffer.
+int router_splits(int sm, int T, int n_f, int n_k, int part_rows) {
+  const int base = (T + 127) / 128 * n_f;
+  int ks = (sm + base - 1) / base;
+  ks = std::min(ks, std::min(16, n_k));
+  while (ks > 1 && (size_t)ks * T > (size_t)part_rows) --ks;
+  return std::max(ks, 1);
+}
 
 Plan make_plan(const moe_config* c) {
   Plan p;
@@ -124,6 +142,9 @@ Plan make_plan(const moe_config* c) {
   p.add(T * k * H);                       // 33 xg (slot order)
   p.add(T * k * (H / G) * 4);             // 34 sxg
   p.add(((E + 127) / 128) * 128 * 3 * H * 2);  // 35 router3
+  p.add(router_part_rows(c) * E * 4);     // 36 router partial logits
+  p.add(T * k * 4);                       // 37 schedule: rank in block
+  p.add(((T + 255) / 256) * E * 4);       // 38 schedule: rows per expert per block
   return p;
 }
 
@@ -153,6 +174,9 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 bool use_decode(const moe_ctx* c, int T);
 bool use_fused(const moe_ctx* c, int T);
 bool use_tc(const moe_ctx* c, int T);
+bool router_args(const moe_ctx* c, const void* x, int T, TcGemm* rt, int* grid);
+cudaError_t launch_topk_after_router(const KArgs& a, const moe_ctx* c, const TcGemm& rt,
+                                     cudaStream_t s);
 cudaError_t launch_fused(moe_ctx* c, const KArgs& a, cudaStream_t s);
 
 // Routing with the kernels the forward of T rows would use (the persistent
@@ -167,12 +191,11 @@ int run_router_and_quant(moe_ctx* c, const KArgs& a, cudaStream_t s) {
   if (use_decode(c, a.d.T))
     return launch_route_decode(a, c->opt_pdl != 0, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   if (use_tc(c, a.d.T)) {
-    TcGemm rt = c->tc[kTcRouter];
-    if (!make_tc_map(&rt.b, true, a.x, (uint64_t)a.d.T, (uint64_t)a.d.H, 16)) return MOE_ERR_CUDA;
-    rt.T = a.d.T;
-    const int g_rt = std::min(c->sm_count, (a.d.T + 127) / 128 * rt.n_f);
+    TcGemm rt;
+    int g_rt = 0;
+    if (!router_args(c, a.x, a.d.T, &rt, &g_rt)) return MOE_ERR_CUDA;
     if (launch_tc_gemm(kTcRouter, rt, g_rt, c->tc_smem[kTcRouter], s) != cudaSuccess ||
-        launch_topk(a, s) != cudaSuccess)
+        launch_topk_after_router(a, c, rt, s) != cudaSuccess)
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
@@ -247,6 +270,7 @@ void setup_tc(moe_ctx* c) {
     return;
   }
   if (H / kGroup > 32 || I / kGroup > 32) return;  // activation scales staged per tile
+  if (H % (2 * kGroup)) return;                     // down items: two output tiles
   TcGemm* g = c->tc;
   const uint64_t Epad = (E + 127) / 128 * 128;
   for (int i = 0; i < 5; ++i) {
@@ -272,7 +296,9 @@ void setup_tc(moe_ctx* c) {
   ok &= make_tc_map(&g[kTcRoutedDown].a, false, c->L.w2, E * H, I, 128);
   ok &= make_tc_map(&g[kTcRoutedDown].b, false, c->w.hq, R, I, 16);
   g[kTcRoutedDown].n_k = (int)(I / kGroup);
-  g[kTcRoutedDown].n_f = (int)(H / kGroup);
+  g[kTcRoutedDown].n_f = (int)(H / (2 * kGroup));  // two adjacent output tiles per item
+  g[kTcRoutedDown].f_rows = 2 * kGroup;
+  g[kTcRoutedDown].up_rows = kGroup;
   g[kTcRoutedDown].a_rows_e = (int)H;
   g[kTcRoutedDown].ldo = (int)H;
   g[kTcRoutedDown].sa = c->L.s2;
@@ -298,7 +324,11 @@ void setup_tc(moe_ctx* c) {
   g[kTcRouter].n_f = (int)(Epad / kGroup);
   g[kTcRouter].ldo = (int)E;
   g[kTcRouter].outf = c->w.logits;
-  for (int i = 0; i < 5; ++i) g[i].b_kwrap = g[i].n_k;
+  for (int i = 0; i < 5; ++i) {
+    g[i].b_kwrap = g[i].n_k;
+    g[i].ksplit = 1;
+    if (i != kTcRoutedDown) g[i].f_rows = kGroup;
+  }
   g[kTcRouter].b_kwrap = (int)(H / 64);
   for (int i = 0; i < 5 && ok; ++i) {
     c->tc_smem[i] = tc_gemm_smem(i, g[i].n_k);
@@ -312,6 +342,23 @@ void setup_tc(moe_ctx* c) {
 // warp-MMA kernels are asked for or the shape has no tcgen05 set-up.
 bool use_tc(const moe_ctx* c, int T) {
   return !use_decode(c, T) && c->tc_ok && c->opt_path != 4;
+}
+
+// Router launch arguments for T rows of x: the input's tensor map and the K
+// splits.  Returns false if the map cannot be encoded.
+bool router_args(const moe_ctx* c, const void* x, int T, TcGemm* rt, int* grid) {
+  *rt = c->tc[kTcRouter];
+  if (!make_tc_map(&rt->b, true, x, (uint64_t)T, (uint64_t)c->cfg.hidden, 16)) return false;
+  rt->T = T;
+  rt->ksplit = router_splits(c->sm_count, T, rt->n_f, rt->n_k, c->part_rows);
+  rt->outf = rt->ksplit > 1 ? c->logits_part : c->w.logits;
+  *grid = std::min(c->sm_count, (T + 127) / 128 * rt->n_f * rt->ksplit);
+  return true;
+}
+
+cudaError_t launch_topk_after_router(const KArgs& a, const moe_ctx* c, const TcGemm& rt,
+                                     cudaStream_t s) {
+  return rt.ksplit > 1 ? launch_topk_splits(a, c->logits_part, rt.ksplit, s) : launch_topk(a, s);
 }
 
 int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
@@ -330,18 +377,18 @@ int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
     return MOE_OK;
   }
   if (use_tc(c, T)) {
-    TcGemm rt = c->tc[kTcRouter];
-    if (!make_tc_map(&rt.b, true, x, (uint64_t)T, (uint64_t)c->cfg.hidden, 16)) return MOE_ERR_CUDA;
+    TcGemm rt;
+    int g_rt = 0;
+    if (!router_args(c, x, T, &rt, &g_rt)) return MOE_ERR_CUDA;
     TcGemm sgu = c->tc[kTcSharedGateUp];
     sgu.b = rt.b;
     TcGemm sdn = c->tc[kTcSharedDown];
-    rt.T = sgu.T = sdn.T = T;
+    sgu.T = sdn.T = T;
     const int tiles = (T + 127) / 128;
-    const int g_rt = std::min(c->sm_count, tiles * rt.n_f);
     const int g_sgu = std::min(c->sm_count, tiles * sgu.n_f);
     const int g_sdn = std::min(c->sm_count, tiles * sdn.n_f);
     LAUNCH(launch_tc_gemm(kTcRouter, rt, g_rt, c->tc_smem[kTcRouter], s), "router_tc");
-    LAUNCH(launch_topk(a, s), "topk");
+    LAUNCH(launch_topk_after_router(a, c, rt, s), "topk");
     LAUNCH(launch_schedule(a, s), "schedule");
     LAUNCH(launch_quant_scatter(a, c->xg, c->sxg, s), "quant_scatter");
     LAUNCH(launch_tc_gemm(kTcSharedGateUp, sgu, g_sgu, c->tc_smem[kTcSharedGateUp], s),
@@ -461,6 +508,10 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   c->xg = (uint8_t*)ptrs[33];
   c->sxg = (float*)ptrs[34];
   c->router3 = (bf16*)ptrs[35];
+  c->logits_part = (float*)ptrs[36];
+  w.sched_rank = (int*)ptrs[37];
+  w.sched_blk = (int*)ptrs[38];
+  c->part_rows = (int)router_part_rows(cfg);
   // counters start at zero and are reset by the kernels that use them
   if (cudaMemset(w.gcount, 0, plan.sizes[25]) != cudaSuccess ||
       cudaMemset(w.status, 0, plan.sizes[29]) != cudaSuccess ||
@@ -488,6 +539,12 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
       }
     }
     cudaGetLastError();
+  }
+  if (setup_schedule() != cudaSuccess) {
+    cudaGetLastError();
+    free_all(c);
+    delete c;
+    return MOE_ERR_CUDA;
   }
   setup_tc(c);
   *out = c;

@@ -63,6 +63,8 @@ struct DevWork {
   int* status;          // [1] device status flag
   int* done;            // [12] barrier counters (self-resetting) and the decode launch tag
   unsigned long long* tlog;  // [kDecodeRows][E] decode logits as {launch tag, value} words
+  int* sched_rank;      // [T*k] rank of each pair among its expert's rows in its 256-row block
+  int* sched_blk;       // [ceil(T/256)][E] rows per expert in each 256-row block
 };
 
 struct KArgs {
@@ -80,7 +82,11 @@ inline int max_chunks(int T, int k, int E) { return (T * k + kChunk - 1) / kChun
 cudaError_t launch_router(const KArgs& a, cudaStream_t s);
 cudaError_t launch_quant_gamma(const KArgs& a, cudaStream_t s);
 cudaError_t launch_topk(const KArgs& a, cudaStream_t s);
+// top-k of logits given as `ks` partial sums part[ks][T][E], summed in split
+// order into the workspace logits first
+cudaError_t launch_topk_splits(const KArgs& a, const float* part, int ks, cudaStream_t s);
 cudaError_t launch_schedule(const KArgs& a, cudaStream_t s);
+cudaError_t setup_schedule();
 cudaError_t launch_gateup(const KArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_down(const KArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_combine(const KArgs& a, cudaStream_t s);
@@ -95,9 +101,11 @@ struct TcGemm {
   CUtensorMap b;       // tokens or slots [rows][K], 128-byte boxes of 16 rows
   int n_k;             // K blocks of 128 bytes
   int b_kwrap;         // K blocks after which the B operand's K coordinate wraps
+  int ksplit;          // K splits per output tile (router; partial sums), else 1
   int n_f;             // 128-row output tiles per token tile
   int a_rows_e;        // weight rows per expert (routed)
-  int up_rows;         // rows from a gate tile to its up tile (gate/up kinds)
+  int up_rows;         // rows from an item's first A tile to its second
+  int f_rows;          // A rows (output features) per item
   int E;               // experts (routed)
   int T;               // rows (shared)
   int ldo;             // row length of the output
@@ -108,7 +116,7 @@ struct TcGemm {
   uint8_t* hq;         // routed gate/up: e4m3 SwiGLU rows [slot][ldo]
   float* sh;           // routed gate/up: their scales [slot][ldo/128]
   bf16* out;           // expert kinds: bf16 [row][ldo]
-  float* outf;         // router: fp32 logits [row][ldo]
+  float* outf;         // router: fp32 logits [ksplit][row][ldo] (partials when ksplit > 1)
   int* status;         // device status flag (set when a wait gives up)
 };
 

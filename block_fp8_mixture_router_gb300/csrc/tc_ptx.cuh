@@ -177,6 +177,21 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, uint32_t (
       : "memory");
 }
 
+// 32 consecutive columns of two accumulators under one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (&va)[32],
+                                            uint32_t (&vb)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,"
+      "%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, "
+      "[%65];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : MOE_TC_R16(va, 0), MOE_TC_R16(va, 16), MOE_TC_R16(vb, 0), MOE_TC_R16(vb, 16)
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
 #undef MOE_TC_R16
 
 // ---- descriptors --------------------------------------------------------------
