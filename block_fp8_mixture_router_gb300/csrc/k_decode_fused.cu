@@ -139,8 +139,8 @@ struct Sched {
   int pair_of_slot[kDecodeRows * kMaxTopK];
   uint32_t tok[kMaxExperts];
   int4 chunk[kMaxExperts];   // {expert, first slot, rows, 0}
-  uint32_t cand_key[kW * kMaxTopK];
-  uint32_t cand_id[kW * kMaxTopK];
+  uint32_t cand_key[2 * kW * kMaxTopK];
+  uint32_t cand_id[2 * kW * kMaxTopK];
   float gred[kW * kDecodeRows];
   int scan[kW];
   int n_used;
@@ -503,83 +503,13 @@ __device__ void routed_unit(const KArgs& a, const Layout& L, int r, int s) {
   }
 }
 
-// ---- top-k of one row with all warps ----------------------------------------
-// Each warp takes the k best of its 32 experts (one per lane), then warp 0
-// takes the k best of those candidates; both levels use the order of
-// topk_row (larger key first, lower expert on equal keys).
-__device__ void topk_one_row(const float* lg, int E, int k, Sched* sc) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  {
-    // branch-free selects throughout: divergent branches in these short
-    // rounds cost far more than the arithmetic
-    const int e = 32 * warp + lane;
-    uint32_t key = e < E ? order_key(lg[e]) : 0u;
-    uint32_t ck = 0u, cid = 0xFFFFFFFFu;
-#pragma unroll 1
-    for (int j = 0; j < k; ++j) {
-      const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
-      const uint32_t win = __reduce_min_sync(0xffffffffu, key == mx ? (uint32_t)e : 0xFFFFFFFFu);
-      key = ((uint32_t)e == win) ? 0u : key;
-      ck = (lane == j) ? mx : ck;
-      cid = (lane == j) ? (mx ? win : 0xFFFFFFFFu) : cid;
-    }
-    if (lane < k) {
-      sc->cand_key[warp * kMaxTopK + lane] = ck;
-      sc->cand_id[warp * kMaxTopK + lane] = cid;
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // candidates of warps 0..7 (k each): lane l holds list entries l and l+32...
-    uint32_t key[kW * kMaxTopK / 32], id[kW * kMaxTopK / 32];
-#pragma unroll
-    for (int h = 0; h < kW * kMaxTopK / 32; ++h) {
-      const int i = lane + 32 * h;
-      const bool ok = (i % kMaxTopK) < k;
-      key[h] = ok ? sc->cand_key[i] : 0u;
-      id[h] = ok ? sc->cand_id[i] : 0xFFFFFFFFu;
-    }
-    uint32_t my_key = 0u, my_e = 0u;
-#pragma unroll 1
-    for (int j = 0; j < k; ++j) {
-      uint32_t bk = 0u, bid = 0xFFFFFFFFu;
-      int bh = 0;
-#pragma unroll
-      for (int h = 0; h < kW * kMaxTopK / 32; ++h) {
-        const bool better = (key[h] > bk) | ((key[h] == bk) & (id[h] < bid));
-        bk = better ? key[h] : bk;
-        bid = better ? id[h] : bid;
-        bh = better ? h : bh;
-      }
-      const uint32_t mx = __reduce_max_sync(0xffffffffu, bk);
-      const uint32_t win = __reduce_min_sync(0xffffffffu, bk == mx ? bid : 0xFFFFFFFFu);
-      const bool mine = (bk == mx) & (bid == win);
-#pragma unroll
-      for (int h = 0; h < kW * kMaxTopK / 32; ++h) {
-        const bool clr = mine & (h == bh);
-        key[h] = clr ? 0u : key[h];
-        id[h] = clr ? 0xFFFFFFFFu : id[h];
-      }
-      my_key = (lane == j) ? mx : my_key;
-      my_e = (lane == j) ? win : my_e;
-    }
-    const float top = key_value(__shfl_sync(0xffffffffu, my_key, 0));
-    const float ex = lane < k ? __expf(key_value(my_key) - top) : 0.0f;
-    const float den = warp_sum(ex);
-    if (lane < k) {
-      sc->idx[lane] = (int)my_e;
-      sc->w[lane] = __fdividef(ex, den);
-    }
-  }
-}
-
 // ---- schedule (identical in every CTA) --------------------------------------
 __device__ void build_schedule(const KArgs& a, const Layout& L, bool publish) {
   Sched* sc = L.sc;
   const int T = a.d.T, k = a.d.k, E = a.d.E;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (T == 1 && E <= 32 * kW && k <= 32) {
-    topk_one_row(L.lg, E, k, sc);
+    topk_one_row<kW>(L.lg, E, k, sc->cand_key, sc->cand_id, sc->idx, sc->w);
     // one row: its k experts are distinct, so slot = rank of the expert among them
     if (warp == 0) {
       __syncwarp();

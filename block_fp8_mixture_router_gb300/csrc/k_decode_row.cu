@@ -1,0 +1,695 @@
+// One-row decode layer (T = 1) as one kernel over every SM, split by role.
+//
+//   routed CTA (r, p), r < k, p < P = H/128: SwiGLU features [p*F, p*F + F)
+//      of the rank-r expert (F = I/P; its 2F gate/up rows are four or fewer
+//      16 KB bulk copies) and rows [128p, 128p + 128) of that expert's down
+//      projection (one contiguous 128 x I copy);
+//   shared gate/up CTA s < P: shared SwiGLU features [s*Fs, s*Fs + Fs);
+//   shared down CTA (the rest): a block of the shared expert's output rows.
+//
+// All CTAs compute router logits (experts b and b + G) while quantising x
+// and taking the shared gate's dot product from the same registers.  Results
+// move between CTAs as 64-bit {launch tag, value} words in global memory,
+// each written once per launch and polled until its tag is current:
+//   logits            every CTA computes the same top-k;
+//   routed SwiGLU h   the CTAs of one expert each read all I values and
+//                     quantise them the same way (1 x 128 groups);
+//   shared SwiGLU hs  the shared down CTAs read all Is values;
+//   down outputs      routed CTA (r, p) combines 128/k of its block's rows:
+//                     y = sum_j w_j d_j (rank order) + gamma * ds, bf16.
+// There is no grid barrier.  Weights that do not depend on x (router rows,
+// the shared expert) are requested before the kernel waits on its
+// predecessor (programmatic dependent launch); a routed CTA issues all its
+// copies as soon as the top-k is known.
+//
+// Router and top-k: PR #939 "Fish Audio Drama 3 text to speech on one CUDA
+// GPU", sections "What it adds" and "Fidelity against the PyTorch oracle"
+// (the lower index wins a tie).  Expert arithmetic: PR #939 section
+// "Precision" (e4m3 inputs per row and per 128 inputs, amax/448).  SwiGLU
+// storage: commit "one SwiGLU launch for the routed and shared experts".
+// Combine order: commit "MoE combine on 8-wide vectors".  Launch chaining:
+// PR #927, section "What this changes".
+//
+// Every wait is bounded: a poll or copy wait that does not complete within
+// the spin limit sets the context's status flag and the kernel runs to its
+// end without waiting further (its output is then undefined, and the host
+// reports MOE_ERR_DEVICE_TIMEOUT).
+#include <math.h>
+
+#include "moe_rowops.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kW = 8;
+constexpr int kThreads = 32 * kW;
+constexpr long long kSpin = 1ll << 22;
+constexpr int kSguSlots = 3;      // ring slots of a shared gate/up CTA (one unit each)
+constexpr int kSdnSlots = 6;      // ring slots of a shared down CTA
+constexpr int kSdnUnit = 32;      // shared down rows per copy
+constexpr int kMaxRowH = 2048;    // router rows live in registers: H <= 2048
+
+__device__ __forceinline__ uint32_t sa(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(sa(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(sa(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
+          "r"(sa(dst)),
+      "l"(src), "r"(bytes), "r"(sa(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(sa(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void copy_wait(uint64_t* bar, uint32_t parity, int* status) {
+  long long it = 0;
+  while (!mbar_test(bar, parity)) {
+    if (++it > kSpin) {
+      atomicExch(status, 1);
+      break;
+    }
+  }
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
+}
+
+// The value of a tagged word once its tag is current (bounded).
+__device__ __forceinline__ float poll_tagged(const unsigned long long* p, unsigned long long tag,
+                                             int* status) {
+  unsigned long long v = ld_relaxed64(p);
+  long long it = 0;
+  while ((v & 0xFFFFFFFF00000000ull) != tag) {
+    if (++it > kSpin) {
+      atomicExch(status, 1);
+      break;
+    }
+    if (it > 16) __nanosleep(32);
+    v = ld_relaxed64(p);
+  }
+  return __uint_as_float((uint32_t)v);
+}
+
+__device__ __forceinline__ void publish(unsigned long long* p, unsigned long long tag, float v) {
+  st_relaxed64(p, tag | __float_as_uint(v));
+}
+
+__device__ __forceinline__ uint4 lds16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+
+__host__ __device__ __forceinline__ size_t al16(size_t v) { return (v + 15) & ~(size_t)15; }
+
+// [src, src + n floats) widened to 16-byte boundaries for one bulk copy (the
+// scale arrays start 16-byte aligned and span whole 16-byte units).
+__device__ __forceinline__ uint32_t span16(const float* src, int n, const float** lo, int* delta) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(src) & ~(uintptr_t)15;
+  const uintptr_t a1 = (reinterpret_cast<uintptr_t>(src + n) + 15) & ~(uintptr_t)15;
+  *lo = reinterpret_cast<const float*>(a0);
+  *delta = (int)((reinterpret_cast<uintptr_t>(src) - a0) / 4);
+  return (uint32_t)(a1 - a0);
+}
+
+// ---- roles ----------------------------------------------------------------
+struct Roles {
+  int P;    // 128-row output blocks
+  int nR;   // routed CTAs (k * P)
+  int nS1;  // shared gate/up CTAs (P)
+  int nS2;  // shared down CTAs
+  int F;    // routed SwiGLU features per CTA (I / P)
+  int Fs;   // shared SwiGLU features per CTA (Is / P)
+  int R2;   // shared down rows per CTA (multiple of kSdnUnit)
+};
+
+__host__ __device__ inline Roles make_roles(int G, int H, int k, int I, int Is) {
+  Roles r;
+  r.P = H / kGroup;
+  r.nR = k * r.P;
+  r.nS1 = r.P;
+  r.nS2 = G - r.nR - r.nS1;
+  r.F = I / r.P;
+  r.Fs = Is / r.P;
+  r.R2 = r.nS2 > 0 ? ((H + r.nS2 - 1) / r.nS2 + kSdnUnit - 1) / kSdnUnit * kSdnUnit : 0;
+  return r;
+}
+
+// Bytes of weights a role keeps in shared memory at once.
+__host__ __device__ inline size_t data_bytes(const Roles& r, int H, int I, int Is) {
+  const size_t routed = (size_t)2 * r.F * H + (size_t)kGroup * I;
+  const size_t sgu = (size_t)kSguSlots * 16 * H * 2;
+  const size_t sdn = (size_t)kSdnSlots * kSdnUnit * Is * 2;
+  size_t m = routed > sgu ? routed : sgu;
+  return al16(m > sdn ? m : sdn);
+}
+
+// Shared memory after the weights.
+struct Small {
+  int idx[kMaxTopK];
+  float w[kMaxTopK];
+  int slot[kMaxTopK];
+  uint32_t cand_key[2 * kW * kMaxTopK];
+  uint32_t cand_id[2 * kW * kMaxTopK];
+  float gred[kW];
+  float gamma;
+  int tag;
+  float comb[kMaxTopK + 1][16];  // down outputs gathered for the combine
+};
+
+struct Lay {
+  uint8_t* data;
+  uint8_t* xq;    // [H] e4m3 codes of x
+  bf16* xs;       // [H] x
+  float* sx;      // [H/128]
+  float* wsc;     // routed: gate scale row, up scale row, down scales (widened)
+  float* hall;    // [max(I, Is)] exchanged SwiGLU values
+  uint8_t* hq;    // [I] their e4m3 codes (routed)
+  float* sh;      // [I/128] their scales
+  float* red;     // [kW][2][32][4] scratch
+  float* lg;      // [E]
+  uint64_t* bar;  // [8]
+  Small* sm;
+};
+
+__host__ __device__ inline size_t small_bytes(int H, int E, int I, int Is) {
+  const int nbh = H / kGroup;
+  const int M = I > Is ? I : Is;
+  return al16(H) + al16((size_t)H * 2) + al16((size_t)nbh * 4) + 3 * al16((size_t)(nbh + 8) * 4) +
+         al16((size_t)M * 4) + al16(I) + al16((size_t)(I / kGroup) * 4) +
+         (size_t)kW * 2 * 32 * 4 * 4 + al16((size_t)E * 4) + 8 * 8 + al16(sizeof(Small));
+}
+
+__device__ inline Lay make_lay(uint8_t* smem, const Roles& r, int H, int E, int I, int Is) {
+  const int nbh = H / kGroup;
+  const int M = I > Is ? I : Is;
+  Lay L;
+  uint8_t* p = smem;
+  L.data = p;
+  p += data_bytes(r, H, I, Is);
+  L.xq = p;
+  p += al16(H);
+  L.xs = reinterpret_cast<bf16*>(p);
+  p += al16((size_t)H * 2);
+  L.sx = reinterpret_cast<float*>(p);
+  p += al16((size_t)nbh * 4);
+  L.wsc = reinterpret_cast<float*>(p);
+  p += 3 * al16((size_t)(nbh + 8) * 4);
+  L.hall = reinterpret_cast<float*>(p);
+  p += al16((size_t)M * 4);
+  L.hq = p;
+  p += al16(I);
+  L.sh = reinterpret_cast<float*>(p);
+  p += al16((size_t)(I / kGroup) * 4);
+  L.red = reinterpret_cast<float*>(p);
+  p += (size_t)kW * 2 * 32 * 4 * 4;
+  L.lg = reinterpret_cast<float*>(p);
+  p += al16((size_t)E * 4);
+  L.bar = reinterpret_cast<uint64_t*>(p);
+  p += 8 * 8;
+  L.sm = reinterpret_cast<Small*>(p);
+  return L;
+}
+
+// Exchange words in the workspace (tagged 64-bit): [k][I] routed h, [k][H]
+// routed down outputs, [Is] shared hs, [H] shared down outputs.
+struct Xw {
+  unsigned long long *h, *d, *hs, *ds;
+};
+
+__device__ inline Xw xw_of(unsigned long long* base, int k, int H, int I, int Is) {
+  Xw x;
+  x.h = base;
+  x.d = x.h + (size_t)k * I;
+  x.hs = x.d + (size_t)k * H;
+  x.ds = x.hs + Is;
+  return x;
+}
+
+// ---- routed gate/up: [8 gate; 8 up] rows of one expert, a part of K --------
+// Lane (g, q) of the m16n8k32 MMAs: rows g (gate) and 8+g (up); the token
+// operand is the single quantised row (all eight columns see it; column 0 is
+// kept).  Partial products are scaled per 64-byte K slice by the weight
+// block scale and the activation group scale.
+__device__ __forceinline__ void routed_part(const uint8_t* rows, int H, const float* sg,
+                                            const float* su, const uint8_t* xq, const float* sx,
+                                            int b0, int b1, float (&acc)[4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+#pragma unroll 4
+  for (int b = b0; b < b1; ++b) {  // 64-byte slices of K
+    const int kb = b >> 1;
+    const int off = b * 64 + 16 * q;
+    const uint4 ag = lds16(rows + (size_t)g * H + off);
+    const uint4 au = lds16(rows + (size_t)(8 + g) * H + off);
+    const uint4 bx = lds16(xq + off);
+    float p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    mma_e4m3_k64(p, ag, au, bx);
+    const float s = sx[kb];
+    acc[0] = fmaf(p[0], sg[kb] * s, acc[0]);
+    acc[2] = fmaf(p[2], su[kb] * s, acc[2]);
+  }
+}
+
+// bf16 analogue over 32-element slices (shared expert; unscaled).
+__device__ __forceinline__ void shared_part(const uint8_t* rows, int H, const bf16* xs, int b0,
+                                            int b1, float (&acc)[4]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  const size_t row = (size_t)2 * H;
+#pragma unroll 4
+  for (int b = b0; b < b1; ++b) {
+    const int off = b * 32 + 8 * q;  // elements
+    const uint4 ag = lds16(rows + (size_t)g * row + 2 * off);
+    const uint4 au = lds16(rows + (size_t)(8 + g) * row + 2 * off);
+    const uint4 bx = lds16(xs + off);
+    mma_bf16_k32(acc, ag, au, bx);
+  }
+}
+
+template <int kDummy>
+__global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int G = gridDim.x, b = blockIdx.x;
+  const int H = a.d.H, E = a.d.E, k = a.d.k, I = a.d.I, Is = a.d.Is;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, q = lane & 3;
+  const int nbh = H / kGroup, nbi = I / kGroup;
+  const Roles R = make_roles(G, H, k, I, Is);
+  const Lay L = make_lay(smem, R, H, E, I, Is);
+  Small* sm = L.sm;
+  int* bar_exit = a.w.done + 3;
+  int* epoch = a.w.done + 4;
+  int* status = a.w.status;
+  const Xw X = xw_of(a.w.xw, k, H, I, Is);
+  const bool is_routed = b < R.nR;
+  const bool is_sgu = !is_routed && b < R.nR + R.nS1;
+  const bool is_sdn = !is_routed && !is_sgu;
+  const int s1 = b - R.nR, s2 = b - R.nR - R.nS1;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 8; ++i) mbar_init(&L.bar[i]);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+
+  // ---- before the wait: the shared expert's weights and the router rows ----
+  const uint32_t sgu_unit = 16u * (uint32_t)H * 2u;  // [8 gate; 8 up] bf16 rows
+  const uint32_t sdn_unit = (uint32_t)kSdnUnit * (uint32_t)Is * 2u;
+  const int sdn_m0 = is_sdn ? s2 * R.R2 : 0;
+  const int sdn_rows = is_sdn ? max(0, min(R.R2, H - sdn_m0)) : 0;
+  const int n_sdn_units = sdn_rows / kSdnUnit;
+  const int n_sgu_units = R.Fs / 8;
+  if (threadIdx.x == 0) {
+    if (is_sgu) {
+      for (int u = 0; u < n_sgu_units && u < kSguSlots; ++u) {
+        uint8_t* dst = L.data + (size_t)u * sgu_unit;
+        const int n0 = s1 * R.Fs + 8 * u;
+        mbar_expect(&L.bar[u], sgu_unit);
+        bulk_copy(dst, a.L.ws13 + (size_t)n0 * H, sgu_unit / 2, &L.bar[u]);
+        bulk_copy(dst + sgu_unit / 2, a.L.ws13 + (size_t)(Is + n0) * H, sgu_unit / 2, &L.bar[u]);
+      }
+    } else if (is_sdn) {
+      for (int u = 0; u < n_sdn_units && u < kSdnSlots; ++u) {
+        mbar_expect(&L.bar[u], sdn_unit);
+        bulk_copy(L.data + (size_t)u * sdn_unit, a.L.ws2 + (size_t)(sdn_m0 + kSdnUnit * u) * Is,
+                  sdn_unit, &L.bar[u]);
+      }
+    }
+  }
+  // router rows: experts b and b + G; each warp covers an eighth of K of both
+  const int keighth = H / 8;
+  const int k0 = warp * keighth;
+  constexpr int kMaxV = kMaxRowH / 8 / 128;
+  const int nv = keighth / 128;
+  float4 wv[2][kMaxV];
+  uint2 gw[kMaxV];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int er = b + G * h;
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i)
+      wv[h][i] = (er < E && i < nv)
+                     ? __ldg(reinterpret_cast<const float4*>(a.L.wr + (size_t)er * H + k0 +
+                                                             128 * i + 4 * lane))
+                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxV; ++i)
+    gw[i] = i < nv ? __ldg(reinterpret_cast<const uint2*>(a.L.gate + k0 + 128 * i + 4 * lane))
+                   : make_uint2(0u, 0u);
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) sm->tag = ld_acquire(epoch) + 1;
+
+  // ---- router logits, x quantisation (1 x 128 groups) and the shared gate ----
+  float acc2[2] = {0.0f, 0.0f}, gacc = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kMaxV; ++i) {
+    if (i >= nv) continue;
+    const int kk = k0 + 128 * i + 4 * lane;
+    const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(a.x + kk));
+    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+    const float x0 = __low2float(p0), x1 = __high2float(p0), x2 = __low2float(p1),
+                x3 = __high2float(p1);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float s = acc2[h];
+      s = fmaf(x0, wv[h][i].x, s);
+      s = fmaf(x1, wv[h][i].y, s);
+      s = fmaf(x2, wv[h][i].z, s);
+      s = fmaf(x3, wv[h][i].w, s);
+      acc2[h] = s;
+    }
+    float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+    m = warp_max(m);
+    const float sc = group_scale(m);
+    const uint32_t packed = quant4(x0, x1, x2, x3, sc);
+    *reinterpret_cast<uint32_t*>(L.xq + kk) = packed;
+    *reinterpret_cast<uint2*>(L.xs + kk) = raw;
+    if (lane == 0) L.sx[kk / kGroup] = sc;
+    if (b == 0) {
+      *reinterpret_cast<uint32_t*>(a.w.xq + kk) = packed;
+      if (lane == 0) a.w.sx[kk / kGroup] = sc;
+    }
+    const __nv_bfloat162 g0 = *reinterpret_cast<const __nv_bfloat162*>(&gw[i].x);
+    const __nv_bfloat162 g1 = *reinterpret_cast<const __nv_bfloat162*>(&gw[i].y);
+    gacc = fmaf(x0, __low2float(g0), gacc);
+    gacc = fmaf(x1, __high2float(g0), gacc);
+    gacc = fmaf(x2, __low2float(g1), gacc);
+    gacc = fmaf(x3, __high2float(g1), gacc);
+  }
+  {
+    const float v0 = warp_sum(acc2[0]), v1 = warp_sum(acc2[1]), vg = warp_sum(gacc);
+    if (lane == 0) {
+      L.red[warp] = v0;
+      L.red[kW + warp] = v1;
+      sm->gred[warp] = vg;
+    }
+  }
+  __syncthreads();
+  const unsigned long long tag = (unsigned long long)(unsigned)sm->tag << 32;
+  if (threadIdx.x < 2) {
+    const int ee = b + G * threadIdx.x;
+    if (ee < E) {
+      float v = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kW; ++w) v += L.red[threadIdx.x * kW + w];
+      st_relaxed64(a.w.tlog + ee, tag | __float_as_uint(v));
+    }
+  }
+  if (threadIdx.x == 32) {
+    float v = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) v += sm->gred[w];
+    sm->gamma = sigmoid_f32(v);
+    if (b == 0) a.w.gamma[0] = sm->gamma;
+  }
+  __syncthreads();  // the router scratch is reused below
+
+  if (is_routed) {
+    // ---- routed: gather the logits, top-k, then this CTA's expert slice ----
+    const int r = b / R.P, p = b % R.P;
+    for (int e = threadIdx.x; e < E; e += kThreads)
+      L.lg[e] = poll_tagged(a.w.tlog + e, tag, status);
+    __syncthreads();
+    topk_one_row<kW>(L.lg, E, k, sm->cand_key, sm->cand_id, sm->idx, sm->w);
+    __syncthreads();
+    const int e = sm->idx[r];
+    const int n0 = p * R.F;       // first feature
+    const int nu = R.F / 8;       // [8 gate; 8 up] units
+    const uint32_t uhalf = 8u * (uint32_t)H;
+    const uint8_t* W13 = a.L.w13 + (size_t)e * 2 * I * H;
+    const float* S13 = a.L.s13 + (size_t)e * (2 * I / kGroup) * nbh;
+    uint8_t* w2s = L.data + (size_t)2 * R.F * H;  // [128][I]
+    const float *lg_, *lu_, *ld_;
+    int dg, du, dd;
+    const uint32_t bg = span16(S13 + (size_t)(n0 / kGroup) * nbh, nbh, &lg_, &dg);
+    const uint32_t bu = span16(S13 + (size_t)((I + n0) / kGroup) * nbh, nbh, &lu_, &du);
+    const uint32_t bd = span16(a.L.s2 + ((size_t)e * nbh + p) * nbi, nbi, &ld_, &dd);
+    const size_t wslot = al16((size_t)(nbh + 8) * 4);
+    float* sgp = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(L.wsc)) + dg;
+    float* sup = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(L.wsc) + wslot) + du;
+    float* sdp = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(L.wsc) + 2 * wslot) + dd;
+    // copies issued by lanes of warp 0 in parallel: lane u < nu the unit u
+    // (bar u), lane nu the scales (bar 7), lane nu + 1 the down slice (bar 6)
+    if (warp == 0) {
+      if (lane < nu) {
+        uint8_t* dst = L.data + (size_t)lane * 2 * uhalf;
+        mbar_expect(&L.bar[lane], 2 * uhalf);
+        bulk_copy(dst, W13 + (size_t)(n0 + 8 * lane) * H, uhalf, &L.bar[lane]);
+        bulk_copy(dst + uhalf, W13 + (size_t)(I + n0 + 8 * lane) * H, uhalf, &L.bar[lane]);
+      } else if (lane == nu) {
+        mbar_expect(&L.bar[7], bg + bu + bd);
+        bulk_copy(L.wsc, lg_, bg, &L.bar[7]);
+        bulk_copy(reinterpret_cast<uint8_t*>(L.wsc) + wslot, lu_, bu, &L.bar[7]);
+        bulk_copy(reinterpret_cast<uint8_t*>(L.wsc) + 2 * wslot, ld_, bd, &L.bar[7]);
+      } else if (lane == nu + 1) {
+        mbar_expect(&L.bar[6], (uint32_t)kGroup * I);
+        bulk_copy(w2s, a.L.w2 + ((size_t)e * H + (size_t)kGroup * p) * I, (uint32_t)kGroup * I,
+                  &L.bar[6]);
+      }
+    }
+    // the routing and the slot order (experts by id) for the checking entry points
+    if (warp == 0 && lane < k) {
+      const int me = sm->idx[lane];
+      int s = 0;
+      for (int j = 0; j < k; ++j) s += sm->idx[j] < me;
+      sm->slot[lane] = s;
+      if (b == 0) {
+        a.w.idx[lane] = me;
+        a.w.wts[lane] = sm->w[lane];
+        a.w.slot_of_pair[lane] = s;
+        a.w.pair_of_slot[s] = lane;
+        a.w.chunks[s] = make_int4(me, s, 1, 0);
+        if (lane == 0) *a.w.n_chunks = k;
+      }
+    }
+    // gate/up: unit u by warps w with w % nu == u, each a part of K
+    const int wpu = kW / nu;
+    const int u = warp % nu, part = warp / nu;
+    const int nsl = H / 64, per = nsl / wpu;
+    copy_wait(&L.bar[7], 0, status);
+    copy_wait(&L.bar[u], 0, status);
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    routed_part(L.data + (size_t)u * 2 * uhalf, H, sgp, sup, L.xq, L.sx, part * per,
+                part * per + per, acc);
+    float* red = L.red;  // [kW][32][2]
+    red[(warp * 32 + lane) * 2 + 0] = acc[0];
+    red[(warp * 32 + lane) * 2 + 1] = acc[2];
+    __syncthreads();
+    if (warp < nu && q == 0) {
+      float zg = 0.0f, zu = 0.0f;
+      for (int pp = 0; pp < wpu; ++pp) {  // parts in K order
+        const int w = pp * nu + warp;
+        zg += red[(w * 32 + lane) * 2 + 0];
+        zu += red[(w * 32 + lane) * 2 + 1];
+      }
+      const float h = silu_f32(bf16_round(zg)) * bf16_round(zu);
+      publish(X.h + (size_t)r * I + n0 + 8 * warp + g, tag, h);
+    }
+    // all I SwiGLU values of expert r, quantised in 1 x 128 groups
+    for (int i = threadIdx.x; i < I; i += kThreads)
+      L.hall[i] = poll_tagged(X.h + (size_t)r * I + i, tag, status);
+    __syncthreads();
+    for (int grp = warp; grp < nbi; grp += kW) {
+      const float4 v = *reinterpret_cast<const float4*>(L.hall + grp * kGroup + 4 * lane);
+      float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+      m = warp_max(m);
+      const float s = group_scale(m);
+      const uint32_t packed = quant4(v.x, v.y, v.z, v.w, s);
+      *reinterpret_cast<uint32_t*>(L.hq + grp * kGroup + 4 * lane) = packed;
+      if (lane == 0) L.sh[grp] = s;
+      if (p == 0) {
+        const int slot = sm->slot[r];
+        *reinterpret_cast<uint32_t*>(a.w.hq + (size_t)slot * I + grp * kGroup + 4 * lane) = packed;
+        if (lane == 0) a.w.sh[(size_t)slot * nbi + grp] = s;
+      }
+    }
+    __syncthreads();
+    // down rows [128p + 16w, +16) of expert e over the full I
+    copy_wait(&L.bar[6], 0, status);
+    {
+      float dacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const uint8_t* rows = w2s + (size_t)(16 * warp) * I;
+      for (int bsl = 0; bsl < I / 64; ++bsl) {
+        const int grp = bsl >> 1;
+        const int off = bsl * 64 + 16 * q;
+        const uint4 a_lo = lds16(rows + (size_t)g * I + off);
+        const uint4 a_hi = lds16(rows + (size_t)(8 + g) * I + off);
+        const uint4 bx = lds16(L.hq + off);
+        float pp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        mma_e4m3_k64(pp, a_lo, a_hi, bx);
+        const float s = sdp[grp] * L.sh[grp];
+        dacc[0] = fmaf(pp[0], s, dacc[0]);
+        dacc[2] = fmaf(pp[2], s, dacc[2]);
+      }
+      if (q == 0) {
+        const int m = kGroup * p + 16 * warp + g;
+        publish(X.d + (size_t)r * H + m, tag, bf16_round(dacc[0]));
+        publish(X.d + (size_t)r * H + m + 8, tag, bf16_round(dacc[2]));
+      }
+    }
+    // combine rows [128p + (128/k) r, +128/k): sum_j w_j d_j + gamma ds
+    const int nrow = kGroup / k;
+    const int m0 = kGroup * p + nrow * r;
+    for (int i = threadIdx.x; i < (k + 1) * nrow; i += kThreads) {
+      const int j = i / nrow, t = i % nrow;
+      sm->comb[j][t] = j < k ? poll_tagged(X.d + (size_t)j * H + m0 + t, tag, status)
+                             : poll_tagged(X.ds + m0 + t, tag, status);
+    }
+    __syncthreads();
+    if (threadIdx.x < nrow) {
+      float y = 0.0f;
+      for (int j = 0; j < k; ++j) y = fmaf(sm->w[j], sm->comb[j][threadIdx.x], y);
+      y = fmaf(sm->gamma, sm->comb[k][threadIdx.x], y);
+      a.y[m0 + threadIdx.x] = __float2bfloat16_rn(y);
+    }
+  } else if (is_sgu) {
+    // ---- shared gate/up: units of [8 gate; 8 up] rows, all warps split K ----
+    const int nsl = H / 32, per = nsl / kW;
+    for (int uu = 0; uu < n_sgu_units; ++uu) {
+      const int slot = uu % kSguSlots;
+      copy_wait(&L.bar[slot], (uint32_t)((uu / kSguSlots) & 1), status);
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      shared_part(L.data + (size_t)slot * sgu_unit, H, L.xs, warp * per, warp * per + per, acc);
+      float* red = L.red;
+      red[(warp * 32 + lane) * 2 + 0] = acc[0];
+      red[(warp * 32 + lane) * 2 + 1] = acc[2];
+      __syncthreads();
+      if (threadIdx.x == 0 && uu + kSguSlots < n_sgu_units) {
+        // the slot is free again: its next unit
+        const int un = uu + kSguSlots;
+        uint8_t* dst = L.data + (size_t)slot * sgu_unit;
+        const int n0 = s1 * R.Fs + 8 * un;
+        mbar_expect(&L.bar[slot], sgu_unit);
+        bulk_copy(dst, a.L.ws13 + (size_t)n0 * H, sgu_unit / 2, &L.bar[slot]);
+        bulk_copy(dst + sgu_unit / 2, a.L.ws13 + (size_t)(Is + n0) * H, sgu_unit / 2,
+                  &L.bar[slot]);
+      }
+      if (warp == 0 && q == 0) {
+        float zg = 0.0f, zu = 0.0f;
+        for (int w = 0; w < kW; ++w) {  // parts in K order
+          zg += red[(w * 32 + lane) * 2 + 0];
+          zu += red[(w * 32 + lane) * 2 + 1];
+        }
+        const float hs = bf16_round(silu_f32(bf16_round(zg)) * bf16_round(zu));
+        const int n = s1 * R.Fs + 8 * uu + g;
+        publish(X.hs + n, tag, hs);
+      }
+      __syncthreads();
+    }
+  } else if (sdn_rows > 0) {
+    // ---- shared down: rows [sdn_m0, +sdn_rows), 32 per unit, one warp each ----
+    bf16* hsb = reinterpret_cast<bf16*>(L.hall);  // [Is] bf16
+    for (int i = threadIdx.x; i < Is; i += kThreads)
+      hsb[i] = __float2bfloat16_rn(poll_tagged(X.hs + i, tag, status));
+    __syncthreads();
+    for (int uu = warp; uu < n_sdn_units; uu += kW) {
+      const int slot = uu % kSdnSlots;
+      copy_wait(&L.bar[slot], (uint32_t)((uu / kSdnSlots) & 1), status);
+      const uint8_t* rows = L.data + (size_t)slot * sdn_unit;
+      for (int tile = 0; tile < kSdnUnit / 16; ++tile) {
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const uint8_t* tr = rows + (size_t)(16 * tile) * Is * 2;
+#pragma unroll 4
+        for (int bsl = 0; bsl < Is / 32; ++bsl) {
+          const int off = bsl * 32 + 8 * q;
+          const uint4 a_lo = lds16(tr + (size_t)g * Is * 2 + 2 * off);
+          const uint4 a_hi = lds16(tr + (size_t)(8 + g) * Is * 2 + 2 * off);
+          const uint4 bx = lds16(hsb + off);
+          mma_bf16_k32(acc, a_lo, a_hi, bx);
+        }
+        if (q == 0) {
+          const int m = sdn_m0 + kSdnUnit * uu + 16 * tile + g;
+          publish(X.ds + m, tag, bf16_round(acc[0]));
+          publish(X.ds + m + 8, tag, bf16_round(acc[2]));
+        }
+      }
+      __syncwarp();
+      // the slot is free again (only this warp read it): its next unit
+      const int un = uu + kSdnSlots;
+      if (lane == 0 && un < n_sdn_units) {
+        mbar_expect(&L.bar[slot], sdn_unit);
+        bulk_copy(L.data + (size_t)slot * sdn_unit,
+                  a.L.ws2 + (size_t)(sdn_m0 + kSdnUnit * un) * Is, sdn_unit, &L.bar[slot]);
+      }
+    }
+  }
+
+  // ---- exit: the last CTA advances the launch tag ----
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int old = atomicAdd(bar_exit, 1);
+    if (old == G - 1) {
+      *bar_exit = 0;
+      *epoch = sm->tag;
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace
+
+size_t decode_row_smem(int G, int H, int E, int k, int I, int Is) {
+  const Roles R = make_roles(G, H, k, I, Is);
+  return data_bytes(R, H, I, Is) + small_bytes(H, E, I, Is);
+}
+
+// Whether the one-row kernel covers this shape on G CTAs within `budget`
+// bytes of shared memory per CTA.
+bool decode_row_fits(int G, int H, int E, int k, int I, int Is, size_t budget) {
+  if (H % 1024 != 0 || H > kMaxRowH) return false;
+  if (E > 2 * G || E > 32 * kW || k > kMaxTopK || kGroup % k != 0 || kGroup / k > 16) return false;
+  const Roles R = make_roles(G, H, k, I, Is);
+  if (R.nS2 < 1 || I % R.P != 0 || Is % R.P != 0) return false;
+  if (R.F < 8 || R.F % 8 != 0 || kGroup % R.F != 0 || kW % (R.F / 8) != 0) return false;
+  if ((H / 64) % (kW / (R.F / 8)) != 0) return false;
+  if (R.Fs < 8 || R.Fs % 8 != 0 || (H / 32) % kW != 0) return false;
+  if (R.R2 % kSdnUnit != 0 || (size_t)R.R2 * R.nS2 < (size_t)H) return false;
+  if (I % 64 != 0 || Is % 32 != 0 || I / kGroup > 8) return false;
+  return decode_row_smem(G, H, E, k, I, Is) <= budget;
+}
+
+cudaError_t setup_decode_row(size_t max_smem) {
+  return cudaFuncSetAttribute(k_decode_row<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)max_smem);
+}
+
+cudaError_t launch_decode_row(const KArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s) {
+  return launch_pdl(k_decode_row<0>, dim3(grid), dim3(kThreads), smem, s, pdl, a);
+}
+
+}  // namespace moe

@@ -26,6 +26,7 @@ struct moe_ctx {
   int opt_path = 0;
   int opt_pdl = 1;
   int dec_grid = 0;        // persistent decode kernel: CTAs (one per SM), 0 = unavailable
+  size_t row_smem = 0;     // one-row decode kernel: shared memory per CTA, 0 = unavailable
   size_t dec_optin = 0;    // shared memory a CTA may use
   cudaStream_t last_stream = nullptr;
   std::vector<void*> allocs;
@@ -145,6 +146,7 @@ Plan make_plan(const moe_config* c) {
   p.add(router_part_rows(c) * E * 4);     // 36 router partial logits
   p.add(T * k * 4);                       // 37 schedule: rank in block
   p.add(((T + 255) / 256) * E * 4);       // 38 schedule: rows per expert per block
+  p.add((k * I + k * H + Is + H) * 8);    // 39 one-row decode exchange words
   return p;
 }
 
@@ -172,6 +174,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 bool use_decode(const moe_ctx* c, int T);
+bool use_row(const moe_ctx* c, int T);
 bool use_fused(const moe_ctx* c, int T);
 bool use_tc(const moe_ctx* c, int T);
 bool router_args(const moe_ctx* c, const void* x, int T, TcGemm* rt, int* grid);
@@ -183,6 +186,13 @@ cudaError_t launch_fused(moe_ctx* c, const KArgs& a, cudaStream_t s);
 // decode kernel routes inside the layer: run the layer into the staging
 // output and keep its published routing).
 int run_router_and_quant(moe_ctx* c, const KArgs& a, cudaStream_t s) {
+  if (use_decode(c, a.d.T) && use_row(c, a.d.T)) {
+    KArgs b = a;
+    b.y = c->stage_y;
+    return launch_decode_row(b, c->sm_count, c->row_smem, c->opt_pdl != 0, s) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+  }
   if (use_decode(c, a.d.T) && use_fused(c, a.d.T)) {
     KArgs b = a;
     b.y = c->stage_y;
@@ -241,6 +251,12 @@ int decode_plan(const moe_ctx* c, int T, size_t* smem) {
     return 0;
   *smem = decode_layer_smem(T, H, E, n);
   return n;
+}
+
+// One row on the role-split one-row kernel unless another decode kernel is
+// asked for.
+bool use_row(const moe_ctx* c, int T) {
+  return T == 1 && c->row_smem > 0 && (c->opt_path == 0 || c->opt_path == 1);
 }
 
 bool use_fused(const moe_ctx* c, int T) {
@@ -365,6 +381,10 @@ int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
                 StageRec* rec = nullptr) {
   KArgs a = make_args(c, x, y, T);
   const int grid = 2 * c->sm_count;
+  if (use_decode(c, T) && use_row(c, T)) {
+    LAUNCH(launch_decode_row(a, c->sm_count, c->row_smem, c->opt_pdl != 0, s), "decode_row");
+    return MOE_OK;
+  }
   if (use_decode(c, T) && use_fused(c, T)) {
     LAUNCH(launch_fused(c, a, s), "decode_layer");
     return MOE_OK;
@@ -511,12 +531,14 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   c->logits_part = (float*)ptrs[36];
   w.sched_rank = (int*)ptrs[37];
   w.sched_blk = (int*)ptrs[38];
+  w.xw = (unsigned long long*)ptrs[39];
   c->part_rows = (int)router_part_rows(cfg);
   // counters start at zero and are reset by the kernels that use them
   if (cudaMemset(w.gcount, 0, plan.sizes[25]) != cudaSuccess ||
       cudaMemset(w.status, 0, plan.sizes[29]) != cudaSuccess ||
       cudaMemset(w.n_chunks, 0, plan.sizes[21]) != cudaSuccess ||
-      cudaMemset(w.tlog, 0, plan.sizes[32]) != cudaSuccess) {
+      cudaMemset(w.tlog, 0, plan.sizes[32]) != cudaSuccess ||
+      cudaMemset(w.xw, 0, plan.sizes[39]) != cudaSuccess) {
     free_all(c);
     delete c;
     return MOE_ERR_CUDA;
@@ -537,6 +559,13 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
         c->dec_grid = c->sm_count;
         c->dec_optin = (size_t)optin;
       }
+      // one-row kernel: every SM one CTA, roles fixed by the shape
+      const size_t rs = decode_row_smem(c->sm_count, cfg->hidden, E, cfg->top_k, cfg->inter,
+                                        cfg->shared_inter);
+      if (decode_row_fits(c->sm_count, cfg->hidden, E, cfg->top_k, cfg->inter, cfg->shared_inter,
+                          (size_t)optin) &&
+          setup_decode_row(rs) == cudaSuccess)
+        c->row_smem = rs;
     }
     cudaGetLastError();
   }
@@ -749,7 +778,7 @@ int moe_set_option(moe_ctx* c, int option, int value) {
   if (!c) return MOE_ERR_INVALID_ARG;
   switch (option) {
     case MOE_OPT_PATH:
-      if (value < 0 || value > 4) return MOE_ERR_INVALID_ARG;
+      if (value < 0 || value > 5) return MOE_ERR_INVALID_ARG;
       c->opt_path = value;
       return MOE_OK;
     case MOE_OPT_PDL:
@@ -777,7 +806,8 @@ int moe_last_device_status(moe_ctx* c) {
     const Plan plan = make_plan(&c->cfg);
     if (cudaMemset(c->w.status, 0, plan.sizes[29]) != cudaSuccess ||
         cudaMemset(c->w.gcount, 0, plan.sizes[25]) != cudaSuccess ||
-        cudaMemset(c->w.tlog, 0, plan.sizes[32]) != cudaSuccess) {
+        cudaMemset(c->w.tlog, 0, plan.sizes[32]) != cudaSuccess ||
+        cudaMemset(c->w.xw, 0, plan.sizes[39]) != cudaSuccess) {
       cudaGetLastError();
       return MOE_ERR_CUDA;
     }

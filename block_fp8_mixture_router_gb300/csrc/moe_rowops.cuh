@@ -102,4 +102,95 @@ __device__ __forceinline__ void topk_row(const float* logits, int E, int k, int*
   }
 }
 
+// ---- top-k of one row with all warps of the CTA -------------------------------
+// kWarps warps of 32 hold experts 0..32*kWarps-1 (E <= 32*kWarps, k <= 16).
+// Level 1: each warp takes the k best of its 32 experts in k rounds; a
+// round's winner is the largest key and, among equal keys, the lowest lane,
+// i.e. the lowest expert.  Level 2 ranks the kWarps*k candidates against each
+// other in parallel.  Both levels give the order of topk_row (larger key
+// first, lower expert on equal keys).  cand_key / cand_id are shared-memory
+// scratch of 2*kWarps*16 entries each; idx_out / w_out (shared memory)
+// receive the experts in rank order and their softmax weights.  The caller
+// synchronises the CTA afterwards.
+template <int kWarps>
+__device__ void topk_one_row(const float* lg, int E, int k, uint32_t* cand_key, uint32_t* cand_id,
+                             int* idx_out, float* w_out) {
+  static_assert(kWarps <= 32, "one list per lane");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  {
+    const int e = 32 * warp + lane;
+    uint32_t key = e < E ? order_key(lg[e]) : 0u;
+    uint32_t ck = 0u, cid = 0xFFFFFFFFu;
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+      const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
+      const int wl = __ffs(__ballot_sync(0xffffffffu, key == mx)) - 1;
+      key = lane == wl ? 0u : key;
+      ck = lane == j ? mx : ck;
+      cid = lane == j ? (mx ? (uint32_t)(32 * warp + wl) : 0xFFFFFFFFu) : cid;
+    }
+    if (lane < k) {
+      cand_key[warp * kMaxTopK + lane] = ck;
+      cand_id[warp * kMaxTopK + lane] = cid;
+    }
+  }
+  __syncthreads();
+  // Level 2: candidate c = (list w, place j) of the kWarps*16 slots takes
+  // rank = number of valid candidates that beat it (larger key, or equal
+  // key and lower expert); every thread reads all slots (broadcast loads).
+  constexpr int kC = kWarps * kMaxTopK;
+  static_assert(kC <= 32 * kWarps, "one thread per candidate");
+  uint32_t* rank_key = cand_key + kC;  // callers provide 2*kC-entry scratch
+  uint32_t* rank_id = cand_id + kC;
+  if (threadIdx.x < kC) {
+    const int c = threadIdx.x;
+    const bool valid = (c % kMaxTopK) < k && cand_key[c] != 0u;
+    const uint32_t K = cand_key[c], D = cand_id[c];
+    int rank = 0;
+    if (k <= 8) {
+      // the first 8 slots of every list in registers (16-byte loads issued
+      // together: shared loads in a dependent loop are latency-bound)
+      uint4 kv[2 * kWarps], dv[2 * kWarps];
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; ++w2) {
+        kv[2 * w2] = *reinterpret_cast<const uint4*>(cand_key + w2 * kMaxTopK);
+        kv[2 * w2 + 1] = *reinterpret_cast<const uint4*>(cand_key + w2 * kMaxTopK + 4);
+        dv[2 * w2] = *reinterpret_cast<const uint4*>(cand_id + w2 * kMaxTopK);
+        dv[2 * w2 + 1] = *reinterpret_cast<const uint4*>(cand_id + w2 * kMaxTopK + 4);
+      }
+#pragma unroll
+      for (int v = 0; v < 2 * kWarps; ++v) {
+        const uint32_t K4[4] = {kv[v].x, kv[v].y, kv[v].z, kv[v].w};
+        const uint32_t D4[4] = {dv[v].x, dv[v].y, dv[v].z, dv[v].w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const bool ok2 = 4 * (v & 1) + t < k;
+          rank += (ok2 & ((K4[t] > K) | ((K4[t] == K) & (D4[t] < D)))) ? 1 : 0;
+        }
+      }
+    } else {
+      for (int w2 = 0; w2 < kWarps; ++w2)
+        for (int j2 = 0; j2 < k; ++j2) {
+          const uint32_t K2 = cand_key[w2 * kMaxTopK + j2], D2 = cand_id[w2 * kMaxTopK + j2];
+          rank += ((K2 > K) | ((K2 == K) & (D2 < D))) ? 1 : 0;
+        }
+    }
+    if (valid && rank < k) {
+      rank_key[rank] = K;
+      rank_id[rank] = D;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t my_key = lane < k ? rank_key[lane] : 0u;
+    const float top = key_value(__shfl_sync(0xffffffffu, my_key, 0));
+    const float ex = lane < k ? __expf(key_value(my_key) - top) : 0.0f;
+    const float den = warp_sum(ex);
+    if (lane < k) {
+      idx_out[lane] = (int)rank_id[lane];
+      w_out[lane] = __fdividef(ex, den);
+    }
+  }
+}
+
 }  // namespace moe

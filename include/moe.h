@@ -172,7 +172,9 @@ int moe_expert_activations(moe_ctx* ctx, int rows, uint8_t* hq, float* sh, void*
  * three chained decode kernels instead of the persistent one, 4 = always the
  * grouped prompt kernels with warp-level MMAs instead of tcgen05 (the path
  * every forward takes when a context's shape leaves no room for the tcgen05
- * kernels: hidden or inter above 4096).  MOE_OPT_PDL: 1 = launch with programmatic
+ * kernels: hidden or inter above 4096), 5 = one row on the multi-row
+ * persistent decode kernel instead of the one-row kernel (which 0 and 1 use
+ * for rows == 1 when the device has enough SMs for its roles).  MOE_OPT_PDL: 1 = launch with programmatic
  * dependent launch so a layer's immutable weight reads overlap the previous
  * kernel's tail (default), 0 = plain launches. */
 enum { MOE_OPT_PATH = 1, MOE_OPT_PDL = 2 };

@@ -116,6 +116,29 @@ def test_decode_t1_many_rows_one_by_one(full_case):
         run_and_check(full_case, x[r:r + 1].contiguous())
 
 
+@pytest.mark.parametrize("path", [m.PATH_DECODE_MULTIROW, m.PATH_DECODE_CHAINED, m.PATH_PROMPT])
+def test_decode_t1_other_kernels(full_case, path):
+    """One row on the multi-row decode kernel, the chained decode kernels and
+    the prompt kernels (the automatic path takes the one-row kernel)."""
+    x = full_case.x(3, tag="t1paths")
+    try:
+        for r in range(3):
+            run_and_check(full_case, x[r:r + 1].contiguous(), path=path)
+    finally:
+        full_case.moe.set_option(m.MOE_OPT_PATH, m.PATH_AUTO)
+
+
+def test_decode_t1_repeated_launches_bitwise(full_case):
+    """Back-to-back one-row forwards (launch tags advance every launch) give
+    identical outputs."""
+    x = full_case.x(1, tag="rep1")
+    ys = [full_case.moe.forward(x).clone() for _ in range(6)]
+    torch.cuda.synchronize()
+    for y in ys[1:]:
+        assert torch.equal(y, ys[0])
+    assert full_case.moe.device_status() == m.MOE_OK
+
+
 def test_decode_t11(dev):
     case = Case(W.WORKLOADS["decode_t11"], 64, dev)
     x = case.x(11)
