@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--workload", default="decode_t1")
     ap.add_argument("--instances", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--rows", type=int, default=None,
+                    help="rows per forward (default: the workload's); the 40-layer sweep "
+                         "is quoted at 1, 4, 16, 64, 256 and 1024")
     return ap.parse_args()
 
 
@@ -203,6 +206,31 @@ def traffic_for(kernel: str, workload: str):
     return e["bytes_per_launch"]
 
 
+# ---- replicas ---------------------------------------------------------------
+
+def reduce_max(value: float, dev=None) -> float:
+    """The largest value over all ranks (the value itself without a process
+    group): the slowest replica's time counts."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=dev if dev is not None else torch.device("cpu"))
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(seed: int, rank: int) -> int:
+    """Each replica draws its own layers and rows (independent work)."""
+    return seed + 104729 * rank
+
+
+def rows_per_second(world: int, steps: int, rows_per_step: int, seconds: float) -> float:
+    """Whole-job throughput: every replica processed steps x rows_per_step."""
+    return world * steps * rows_per_step / seconds
+
+
 # ---- reference arm: the CPU oracle -----------------------------------------
 
 def run_reference(args):
@@ -214,21 +242,28 @@ def run_reference(args):
     import workloads as W
     wl = W.WORKLOADS[args.workload]
     s = wl.shape
+    T = args.rows if args.rows else wl.rows
+    seed = W.layer_seed(wl, 0) if wl.layers > 1 else wl.seed
     oracle.build()
-    x = W.make_x(s, max(wl.rows, 1), wl.seed, wl.x_kind)
-    wr = W.make_router(s, wl.seed, wl.x_kind)
+    # a bounded sample of the workload: up to two of its rows per step, and
+    # at most about a minute of steps in all
+    sample = max(1, min(T, 2))
+    x = W.make_x(s, sample, seed, wl.x_kind)
+    wr = W.make_router(s, seed, wl.x_kind)
     idx = set()
     xb = W.bf16_bits(x)
     for r in range(xb.shape[0]):
         idx |= set(oracle.router_row(xb[r], wr.numpy(), s.top_k)[1].tolist())
-    layer = W.to_numpy_layer(W.make_layer(s, wl.seed, wl.x_kind, experts=sorted(idx)))
-    steps = args.steps if args.steps is not None else 5
-    for _ in range(max(args.warmup, 1) if args.warmup else 0):
+    layer = W.to_numpy_layer(W.make_layer(s, seed, wl.x_kind, experts=sorted(idx)))
+    steps_req = args.steps if args.steps is not None else 5
+    if args.warmup:
         oracle.moe_rows(layer, xb[:1])
-        break
+    budget_s = 60.0
+    steps = 0
     t0 = time.perf_counter()
-    for _ in range(steps):
+    while steps < steps_req and (steps == 0 or time.perf_counter() - t0 < budget_s):
         oracle.moe_rows(layer, xb)
+        steps += 1
     dt = time.perf_counter() - t0
     rows = steps * xb.shape[0]
     value = rows / dt
@@ -236,11 +271,12 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": steps, "warmup": 1, "ms_per_step": 1e3 * dt / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "rows": wl.rows, "hidden": s.hidden,
+        "config": {"workload": wl.name, "rows": T, "hidden": s.hidden,
                    "experts": s.n_experts, "top_k": s.top_k, "inter": s.inter,
                    "shared_inter": s.shared_inter},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{steps} full passes of the {wl.name} batch ({xb.shape[0]} rows)"},
+                         "sample": f"{steps} oracle passes of {xb.shape[0]} of the {T} rows "
+                                   f"of {wl.name} (steps capped at about {budget_s:.0f} s)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -280,27 +316,39 @@ def run_ours(args):
 
     wl = W.WORKLOADS[args.workload]
     s = wl.shape
-    T = wl.rows
-    L = max(1, args.instances)
+    T = args.rows if args.rows else wl.rows
+    sweep = wl.layers > 1
+    # a single-layer workload rotates over independent layer instances (L2
+    # cold); the sweep passes the rows through its layers in order
+    L = wl.layers if sweep else max(1, args.instances)
     shape = moe.LayerShape(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, s.group)
     nets, xs, ys, layers = [], [], [], []
     for i in range(L):
-        layer = W.make_layer(s, wl.seed + 7919 * i + 104729 * rank, wl.x_kind, device=dev)
+        seed = replica_seed(W.layer_seed(wl, i) if sweep else wl.seed + 7919 * i, rank)
+        layer = W.make_layer(s, seed, wl.x_kind, device=dev)
         net = moe.MoELayer(shape, max_rows=max(T, 16), device=local)
         net.load(layer)
         nets.append(net)
-        xs.append(W.make_x(s, T, wl.seed + 7919 * i + 104729 * rank, wl.x_kind, device=dev))
-        ys.append(torch.empty_like(xs[-1]))
+        if not sweep or i == 0:
+            xs.append(W.make_x(s, T, seed, wl.x_kind, device=dev))
+        ys.append(torch.empty((T, s.hidden), dtype=torch.bfloat16, device=dev))
         if i == 0:
             layers.append(layer)
         del layer
     torch.cuda.synchronize()
     stream = torch.cuda.Stream(device=dev)
-    K = args.steps if args.steps is not None else 32000 // max(1, T) * 1
+    layers_per_step = L if sweep else 1
+    K = args.steps if args.steps is not None else max(1, 32000 // (T * layers_per_step))
     K = max(1, K)
     Wm = max(3, args.warmup)
 
     def step(i):
+        if sweep:
+            src = xs[0]
+            for j in range(L):  # y of layer j is the input of layer j + 1
+                nets[j].forward(src, ys[j], stream=stream)
+                src = ys[j]
+            return
         j = i % L
         nets[j].forward(xs[j], ys[j], stream=stream)
 
@@ -317,8 +365,9 @@ def run_ours(args):
                 step(i)
         return g
 
-    full, rem = divmod(K, L)
-    g_full = capture(L) if full else None
+    per_graph = 1 if sweep else L
+    full, rem = divmod(K, per_graph)
+    g_full = capture(per_graph) if full else None
     g_rem = capture(rem) if rem else None
     with torch.cuda.stream(stream):
         if g_full:
@@ -347,20 +396,17 @@ def run_ours(args):
     if sampler:
         sampler.mark_end()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+    ms = reduce_max(e0.elapsed_time(e1), dev)
     if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     clocks = sampler.finish() if sampler else None
-    value = world * K * T / (ms / 1e3)
+    value = rows_per_second(world, K, T * layers_per_step, ms / 1e3)
 
     # per-kernel device times (events after every launch), same rotation
     stage_ms = {}
     P = min(64, max(8, L * 4))
     for i in range(P):
-        j = i % L
+        j = 0 if sweep else i % L
         for name, t in nets[j].profile(xs[j], ys[j], stream=stream):
             stage_ms.setdefault(name, []).append(t)
     stage_avg = {n: sum(v) / len(v) for n, v in stage_ms.items()}
@@ -368,7 +414,7 @@ def run_ours(args):
 
     # touched experts per instance
     Us = []
-    for j in range(L):
+    for j in range(1 if sweep else L):
         idx, _ = nets[j].route(xs[j], stream=stream)
         stream.synchronize()
         Us.append(len(set(idx.cpu().numpy().ravel().tolist())))
@@ -394,18 +440,21 @@ def run_ours(args):
                          "frac": tf / tf_peak,
                          "peak_kind": peak_kind + (" (bf16 x 2 for fp8)" if sf[0] == "fp8" else "")})
     lb = layer_bytes(s, T, U)
-    step_ms = ms / K
+    step_ms = ms / K / layers_per_step  # per layer
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": Wm, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
         "config": {"workload": wl.name, "rows": T, "hidden": s.hidden, "experts": s.n_experts,
                    "top_k": s.top_k, "inter": s.inter, "shared_inter": s.shared_inter,
                    "activations": "bf16", "expert_weights": "e4m3, fp32 128x128 block scales",
                    "layer_instances": L,
-                   "l2": f"weights rotate over {L} layer instances "
-                         f"({L * lb / 2**30:.1f} GiB touched per rotation) > 129 MB L2",
+                   "layers_per_step": layers_per_step,
+                   "l2": (f"{L} chained layers, {L * lb / 2**30:.1f} GiB touched per step"
+                          if sweep else
+                          f"weights rotate over {L} layer instances "
+                          f"({L * lb / 2**30:.1f} GiB touched per rotation)") + " > 129 MB L2",
                    "timing": "CUDA graphs of whole steps, CUDA events on the launch stream",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,
@@ -415,29 +464,40 @@ def run_ours(args):
                            "distinct_experts": U,
                            "fp8_tflops": fp8_flops(s, T) / (step_ms * 1e-3) / 1e12},
         "stages_us": {n: round(v * 1e3, 3) for n, v in stage_avg.items()},
-        "gpu_launches": K * launches_per_step,
+        "gpu_launches": K * launches_per_step * layers_per_step,
         "clocks": clocks,
     }
 
     # end to end through the C ABI with host buffers (copies inside the timed region)
     xh = [x.cpu().pin_memory() for x in xs]
-    yh = [torch.empty_like(v) for v in xh]
-    yh = [v.pin_memory() for v in yh]
+    yh = [torch.empty_like(v).pin_memory() for v in xh]
     Ke = min(K, 2000)
-    for i in range(3):
-        nets[i % L].forward_host(xh[i % L], yh[i % L], stream=stream)
-    t0 = time.perf_counter()
-    for i in range(Ke):
+
+    def e2e_step(i):
+        if sweep:  # one copy in, the layers on the device, one copy out
+            with torch.cuda.stream(stream):
+                xd = xh[0].to(dev, non_blocking=True)
+                src = xd
+                for j in range(L):
+                    nets[j].forward(src, ys[j], stream=stream)
+                    src = ys[j]
+                yh[0].copy_(src, non_blocking=True)
+            stream.synchronize()
+            return
         j = i % L
         nets[j].forward_host(xh[j], yh[j], stream=stream)
-    et = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([et], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        et = float(t.item())
-    line["e2e"] = {"value": world * Ke * T / et, "unit": UNIT,
+
+    for i in range(3):
+        e2e_step(i)
+    t0 = time.perf_counter()
+    for i in range(Ke):
+        e2e_step(i)
+    et = reduce_max(time.perf_counter() - t0, dev)
+    line["e2e"] = {"value": rows_per_second(world, Ke, T * layers_per_step, et), "unit": UNIT,
                    "h2d_bytes_per_step": T * s.hidden * 2, "d2h_bytes_per_step": T * s.hidden * 2,
-                   "steps": Ke, "api": "moe_forward_host"}
+                   "steps": Ke,
+                   "api": "moe_forward per layer, host copies per step" if sweep
+                   else "moe_forward_host"}
 
     if rank == 0 and world == 1:
         host = W.to_numpy_layer(layers[0])

@@ -223,3 +223,35 @@ def test_max_rows(dev):
     case = Case(W.WORKLOADS["tiny_t4"], 1024, dev)
     x = case.x(1024, tag="max")
     run_and_check(case, x, sample_rows=[0, 333, 1023])
+
+
+# ---- layers in sequence (the 40-layer backbone sweep, shortened) --------------
+
+@pytest.mark.parametrize("rows", [1, 17])
+def test_chained_layers_teacher_forced(dev, rows):
+    """Rows passed through three distinct layers, x_{l+1} = y_l, each layer on
+    its own context with launches chained on one stream; every layer's output
+    is checked against the oracle on that layer's GPU input (teacher forced)."""
+    wl = W.WORKLOADS["sweep40"]
+    s = wl.shape
+    layers = [W.make_layer(s, W.layer_seed(wl, l), wl.x_kind, device=dev) for l in range(3)]
+    nets = []
+    for layer in layers:
+        net = m.MoELayer(_shape(s), max_rows=64)
+        net.load(layer)
+        nets.append(net)
+    xs = [W.make_x(s, rows, W.layer_seed(wl, 0), wl.x_kind, device="cuda", tag="chain")]
+    for net in nets:
+        xs.append(net.forward(xs[-1]))
+    routes = [net.route(x) for net, x in zip(nets, xs[:-1])]
+    torch.cuda.synchronize()
+    sample = sorted({0, rows - 1})
+    for l, layer in enumerate(layers):
+        host = W.to_numpy_layer(layer)
+        ref = oracle.moe_rows(host, bits(xs[l])[sample], trace=True)
+        idx = routes[l][0].cpu().numpy()[sample]
+        near, differ = check_topk(idx, ref.trace["logits"], s.top_k)
+        assert differ.sum() == 0 or (differ & near).all(), f"layer {l} routed differently"
+        rel, mx = check_output(bits(xs[l + 1])[sample], ref.y_ref, rows_mask=~differ)
+    for net in nets:
+        net.close()
