@@ -107,9 +107,51 @@ __device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// Reciprocal of a divisor for div_shared: RN(1/s) when s is a normal number
+// in [2^-125, 2^126), else 0, which sends div_shared to the IEEE division.
+__device__ __forceinline__ float div_recip(float s) {
+  const uint32_t es = (__float_as_uint(s) >> 23) & 0xFFu;
+  return (es >= 2u && es <= 252u) ? __frcp_rn(s) : 0.0f;
+}
+
+// v / s rounded to nearest even, bit for bit the IEEE quotient, for a divisor
+// shared by many dividends (y = div_recip(s)).  One Newton step from v*y
+// leaves q within an ulp of v/s; for such a q the FMA remainder r = v - q*s
+// is exact (the property Markstein's division rests on), so comparing |r|
+// with s times half the ulp of q -- the ulp below when q is a power of two
+// and v/s lies below it -- decides between q and its neighbour.  Dividends
+// below 2^-95 or near overflow, and quotients below 2^-63, whose remainder or
+// half-ulp product could leave the normal range, take the IEEE division.
+__device__ __forceinline__ float div_shared(float v, float s, float y) {
+  const uint32_t ev = (__float_as_uint(v) >> 23) & 0xFFu;
+  if (y == 0.0f || ev > 252u || (ev < 32u && v != 0.0f)) return __fdiv_rn(v, s);
+  if (ev < 32u) return v * y;  // a signed zero
+  float q = v * y;
+  q = fmaf(fmaf(-q, s, v), y, q);
+  const float r = fmaf(-q, s, v);
+  const uint32_t qb = __float_as_uint(q);
+  const uint32_t e = (qb >> 23) & 0xFFu;
+  if (e < 64u || e > 253u) return __fdiv_rn(v, s);
+  const float half = s * __uint_as_float((e - 24u) << 23);
+  const bool down = (r < 0.0f) != (q < 0.0f);
+  const float h = (down && (qb & 0x7FFFFFu) == 0u) ? 0.5f * half : half;
+  const float ar = fabsf(r);
+  if (ar < h || (ar == h && !(qb & 1u))) return q;
+  return __uint_as_float(down ? qb - 1u : qb + 1u);
+}
+
 // Quantise four values of a group with scale s: codes of v/s (IEEE division).
 __device__ __forceinline__ uint32_t quant4(float v0, float v1, float v2, float v3, float s) {
-  return e4m3x4(__fdiv_rn(v0, s), __fdiv_rn(v1, s), __fdiv_rn(v2, s), __fdiv_rn(v3, s));
+  const float y = div_recip(s);
+  return e4m3x4(div_shared(v0, s, y), div_shared(v1, s, y), div_shared(v2, s, y),
+                div_shared(v3, s, y));
+}
+
+// The same with the reciprocal already taken (y = div_recip(s)).
+__device__ __forceinline__ uint32_t quant4r(float v0, float v1, float v2, float v3, float s,
+                                            float y) {
+  return e4m3x4(div_shared(v0, s, y), div_shared(v1, s, y), div_shared(v2, s, y),
+                div_shared(v3, s, y));
 }
 
 // silu(z) = z / (1 + e^-z) with the fast exponential and divide; the
@@ -138,7 +180,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // Scale of one quantisation group from its amax: amax / 448 (IEEE division),
 // 1 for an all-zero group.
 __device__ __forceinline__ float group_scale(float amax) {
-  return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  return amax > 0.0f ? div_shared(amax, 448.0f, 0x1.24924ap-9f) : 1.0f;  // RN(1/448)
 }
 
 }  // namespace moe
