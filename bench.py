@@ -76,6 +76,7 @@ def stage_bytes(s, T: int, U: int) -> dict:
         # decode path: one persistent kernel for the whole layer
         "decode_layer": layer_bytes(s, T, U),
         "decode_row": layer_bytes(s, T, U),
+        "decode_rows": layer_bytes(s, T, U),
         # decode path, chained variant (three kernels)
         "route_decode": 4 * E * H + 2 * T * H + 4 * T * E + T * H + 4 * T * (H // G) + 2 * H
         + 8 * T * k,

@@ -36,113 +36,20 @@
 // reports MOE_ERR_DEVICE_TIMEOUT).
 #include <math.h>
 
-#include "moe_rowops.cuh"
+#include "decode_common.cuh"
 
 namespace moe {
 
 namespace {
 
+using namespace dec;
+
 constexpr int kW = 8;
 constexpr int kThreads = 32 * kW;
-constexpr long long kSpin = 1ll << 22;
 constexpr int kSguSlots = 3;      // ring slots of a shared gate/up CTA (one unit each)
 constexpr int kSdnSlots = 6;      // ring slots of a shared down CTA
 constexpr int kSdnUnit = 32;      // shared down rows per copy
 constexpr int kMaxRowH = 2048;    // router rows live in registers: H <= 2048
-
-__device__ __forceinline__ uint32_t sa(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(sa(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(sa(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
-          "r"(sa(dst)),
-      "l"(src), "r"(bytes), "r"(sa(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(sa(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ void copy_wait(uint64_t* bar, uint32_t parity, int* status) {
-  long long it = 0;
-  while (!mbar_test(bar, parity)) {
-    if (++it > kSpin) {
-      atomicExch(status, 1);
-      break;
-    }
-  }
-}
-
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_relaxed64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
-}
-
-// The value of a tagged word once its tag is current (bounded).
-__device__ __forceinline__ float poll_tagged(const unsigned long long* p, unsigned long long tag,
-                                             int* status) {
-  unsigned long long v = ld_relaxed64(p);
-  long long it = 0;
-  while ((v & 0xFFFFFFFF00000000ull) != tag) {
-    if (++it > kSpin) {
-      atomicExch(status, 1);
-      break;
-    }
-    if (it > 16) __nanosleep(32);
-    v = ld_relaxed64(p);
-  }
-  return __uint_as_float((uint32_t)v);
-}
-
-__device__ __forceinline__ void publish(unsigned long long* p, unsigned long long tag, float v) {
-  st_relaxed64(p, tag | __float_as_uint(v));
-}
-
-__device__ __forceinline__ uint4 lds16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
-
-__host__ __device__ __forceinline__ size_t al16(size_t v) { return (v + 15) & ~(size_t)15; }
-
-// [src, src + n floats) widened to 16-byte boundaries for one bulk copy (the
-// scale arrays start 16-byte aligned and span whole 16-byte units).
-__device__ __forceinline__ uint32_t span16(const float* src, int n, const float** lo, int* delta) {
-  const uintptr_t a0 = reinterpret_cast<uintptr_t>(src) & ~(uintptr_t)15;
-  const uintptr_t a1 = (reinterpret_cast<uintptr_t>(src + n) + 15) & ~(uintptr_t)15;
-  *lo = reinterpret_cast<const float*>(a0);
-  *delta = (int)((reinterpret_cast<uintptr_t>(src) - a0) / 4);
-  return (uint32_t)(a1 - a0);
-}
 
 // ---- roles ----------------------------------------------------------------
 struct Roles {

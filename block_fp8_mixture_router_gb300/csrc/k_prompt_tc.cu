@@ -53,7 +53,6 @@ struct Cfg {
   static constexpr bool kSwiGLU = kKind == kTcRoutedGateUp || kKind == kTcSharedGateUp;
   static constexpr bool kPair = kSwiGLU || kKind == kTcRoutedDown;
   static constexpr bool kRouted = kF8;
-  static constexpr bool kRouter = kKind == kTcRouter;
   // Tokens per tile (N).  The block-FP8 kinds keep their promoted
   // accumulators in registers (gate and up: 2 x kN/4 per epilogue thread,
   // within the ~100 registers a thread has at 18 warps per CTA); the bf16

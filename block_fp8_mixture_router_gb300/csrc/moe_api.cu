@@ -27,6 +27,7 @@ struct moe_ctx {
   int opt_pdl = 1;
   int dec_grid = 0;        // persistent decode kernel: CTAs (one per SM), 0 = unavailable
   size_t row_smem = 0;     // one-row decode kernel: shared memory per CTA, 0 = unavailable
+  size_t rows_smem = 0;    // 2..16-row decode kernel: shared memory per CTA, 0 = unavailable
   size_t dec_optin = 0;    // shared memory a CTA may use
   cudaStream_t last_stream = nullptr;
   std::vector<void*> allocs;
@@ -146,7 +147,7 @@ Plan make_plan(const moe_config* c) {
   p.add(router_part_rows(c) * E * 4);     // 36 router partial logits
   p.add(T * k * 4);                       // 37 schedule: rank in block
   p.add(((T + 255) / 256) * E * 4);       // 38 schedule: rows per expert per block
-  p.add((k * I + k * H + Is + H) * 8);    // 39 one-row decode exchange words
+  p.add(kDecodeRows * (k * I + k * H + Is + H) * 8);  // 39 decode exchange words
   return p;
 }
 
@@ -175,6 +176,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 bool use_decode(const moe_ctx* c, int T);
 bool use_row(const moe_ctx* c, int T);
+bool use_rows(const moe_ctx* c, int T);
 bool use_fused(const moe_ctx* c, int T);
 bool use_tc(const moe_ctx* c, int T);
 bool router_args(const moe_ctx* c, const void* x, int T, TcGemm* rt, int* grid);
@@ -190,6 +192,13 @@ int run_router_and_quant(moe_ctx* c, const KArgs& a, cudaStream_t s) {
     KArgs b = a;
     b.y = c->stage_y;
     return launch_decode_row(b, c->sm_count, c->row_smem, c->opt_pdl != 0, s) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+  }
+  if (use_decode(c, a.d.T) && use_rows(c, a.d.T)) {
+    KArgs b = a;
+    b.y = c->stage_y;
+    return launch_decode_rows(b, c->sm_count, c->rows_smem, c->opt_pdl != 0, s) == cudaSuccess
                ? MOE_OK
                : MOE_ERR_CUDA;
   }
@@ -257,6 +266,12 @@ int decode_plan(const moe_ctx* c, int T, size_t* smem) {
 // asked for.
 bool use_row(const moe_ctx* c, int T) {
   return T == 1 && c->row_smem > 0 && (c->opt_path == 0 || c->opt_path == 1);
+}
+
+// 2..16 rows on the role-split multi-row kernel unless another decode kernel
+// is asked for.
+bool use_rows(const moe_ctx* c, int T) {
+  return T >= 2 && T <= kDecodeRows && c->rows_smem > 0 && (c->opt_path == 0 || c->opt_path == 1);
 }
 
 bool use_fused(const moe_ctx* c, int T) {
@@ -383,6 +398,10 @@ int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
   const int grid = 2 * c->sm_count;
   if (use_decode(c, T) && use_row(c, T)) {
     LAUNCH(launch_decode_row(a, c->sm_count, c->row_smem, c->opt_pdl != 0, s), "decode_row");
+    return MOE_OK;
+  }
+  if (use_decode(c, T) && use_rows(c, T)) {
+    LAUNCH(launch_decode_rows(a, c->sm_count, c->rows_smem, c->opt_pdl != 0, s), "decode_rows");
     return MOE_OK;
   }
   if (use_decode(c, T) && use_fused(c, T)) {
@@ -566,6 +585,11 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
                           (size_t)optin) &&
           setup_decode_row(rs) == cudaSuccess)
         c->row_smem = rs;
+      const size_t rr = decode_rows_smem(cfg->hidden);
+      if (decode_rows_fits(c->sm_count, cfg->hidden, E, cfg->top_k, cfg->inter, cfg->shared_inter,
+                           (size_t)optin) &&
+          setup_decode_rows(rr) == cudaSuccess)
+        c->rows_smem = rr;
     }
     cudaGetLastError();
   }

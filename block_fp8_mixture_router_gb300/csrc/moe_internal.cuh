@@ -63,7 +63,7 @@ struct DevWork {
   int* status;          // [1] device status flag
   int* done;            // [12] barrier counters (self-resetting) and the decode launch tag
   unsigned long long* tlog;  // [kDecodeRows][E] decode logits as {launch tag, value} words
-  unsigned long long* xw;  // one-row decode exchange words: [k][I] h, [k][H] d, [Is] hs, [H] ds
+  unsigned long long* xw;  // decode exchange words: [16k][I] h, [16k][H] d, [16][Is] hs, [16][H] ds
   int* sched_rank;      // [T*k] rank of each pair among its expert's rows in its 256-row block
   int* sched_blk;       // [ceil(T/256)][E] rows per expert in each 256-row block
 };
@@ -97,6 +97,12 @@ size_t decode_row_smem(int G, int H, int E, int k, int I, int Is);
 bool decode_row_fits(int G, int H, int E, int k, int I, int Is, size_t budget);
 cudaError_t setup_decode_row(size_t max_smem);
 cudaError_t launch_decode_row(const KArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s);
+
+// ---- 2..16-row decode kernel (k_decode_rows.cu) ---------------------------------
+size_t decode_rows_smem(int H);
+bool decode_rows_fits(int G, int H, int E, int k, int I, int Is, size_t budget);
+cudaError_t setup_decode_rows(size_t max_smem);
+cudaError_t launch_decode_rows(const KArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s);
 
 // ---- prompt path on tcgen05 tensor cores (k_prompt_tc.cu) -------------------
 enum { kTcRoutedGateUp = 0, kTcRoutedDown = 1, kTcSharedGateUp = 2, kTcSharedDown = 3,

@@ -172,9 +172,11 @@ int moe_expert_activations(moe_ctx* ctx, int rows, uint8_t* hq, float* sh, void*
  * three chained decode kernels instead of the persistent one, 4 = always the
  * grouped prompt kernels with warp-level MMAs instead of tcgen05 (the path
  * every forward takes when a context's shape leaves no room for the tcgen05
- * kernels: hidden or inter above 4096), 5 = one row on the multi-row
- * persistent decode kernel instead of the one-row kernel (which 0 and 1 use
- * for rows == 1 when the device has enough SMs for its roles).  MOE_OPT_PDL: 1 = launch with programmatic
+ * kernels: hidden or inter above 4096), 5 = rows <= 16 on the persistent
+ * multi-row decode kernel with one grid barrier instead of the role-split
+ * decode kernels (which 0 and 1 use when the device has enough SMs for
+ * their roles: the one-row kernel for rows == 1, the multi-row role-split
+ * kernel for 2..16 rows).  MOE_OPT_PDL: 1 = launch with programmatic
  * dependent launch so a layer's immutable weight reads overlap the previous
  * kernel's tail (default), 0 = plain launches. */
 enum { MOE_OPT_PATH = 1, MOE_OPT_PDL = 2 };

@@ -89,7 +89,7 @@ def test_tiny_layer_every_path(dev, path, rows):
     run_and_check(case, case.x(rows, tag=f"p{rows}"), path=path)
 
 
-@pytest.mark.parametrize("path", [m.PATH_PROMPT, m.PATH_DECODE_CHAINED])
+@pytest.mark.parametrize("path", [m.PATH_PROMPT, m.PATH_DECODE_CHAINED, m.PATH_DECODE_MULTIROW])
 def test_full_layer_other_paths(full_case, path):
     x = full_case.x(11, tag="paths")
     try:
