@@ -32,6 +32,9 @@ METRIC = "MoE-layer rows/s"
 UNIT = "rows/s"
 
 
+PATHS = {"auto": 0, "prompt": 2, "chained": 3, "prompt_mma": 4, "multirow": 5, "rows": 6}
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -44,6 +47,8 @@ def parse():
     ap.add_argument("--rows", type=int, default=None,
                     help="rows per forward (default: the workload's); the 40-layer sweep "
                          "is quoted at 1, 4, 16, 64, 256 and 1024")
+    ap.add_argument("--path", choices=tuple(PATHS), default="auto",
+                    help="kernel path (MOE_OPT_PATH): auto picks by row count")
     return ap.parse_args()
 
 
@@ -329,6 +334,7 @@ def run_ours(args):
         layer = W.make_layer(s, seed, wl.x_kind, device=dev)
         net = moe.MoELayer(shape, max_rows=max(T, 16), device=local)
         net.load(layer)
+        net.set_option(moe.MOE_OPT_PATH, PATHS[args.path])
         nets.append(net)
         if not sweep or i == 0:
             xs.append(W.make_x(s, T, seed, wl.x_kind, device=dev))
@@ -457,6 +463,7 @@ def run_ours(args):
                           f"weights rotate over {L} layer instances "
                           f"({L * lb / 2**30:.1f} GiB touched per rotation)") + " > 129 MB L2",
                    "timing": "CUDA graphs of whole steps, CUDA events on the launch stream",
+                   "kernel_path": args.path,
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,
         "layer_roofline": {"bound": "hbm", "algorithmic_bytes_per_step": lb,

@@ -31,6 +31,7 @@ MOE_OPT_PATH = 1
 MOE_OPT_PDL = 2
 PATH_AUTO, PATH_DECODE, PATH_PROMPT, PATH_DECODE_CHAINED, PATH_PROMPT_MMA = 0, 1, 2, 3, 4
 PATH_DECODE_MULTIROW = 5  # the persistent multi-row decode kernel with a grid barrier
+PATH_DECODE_ROWS = 6  # the role-split multi-row decode kernel for 2..16 rows
 
 EXPORTED = ("moe_create", "moe_load_weights", "moe_forward", "moe_forward_host", "moe_route",
             "moe_quantize", "moe_expert_activations", "moe_set_option", "moe_required_bytes",

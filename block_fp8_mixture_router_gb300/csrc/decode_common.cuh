@@ -24,11 +24,16 @@ __device__ __forceinline__ void mbar_expect(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.  The
+// lines it reads are marked evict-first in L2: weights stream through once
+// per launch, and without the hint they push out what every launch reuses
+// (the kernel's code, x, the exchange words).
 __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
-          "r"(sa(dst)),
+      "{\n .reg .b64 pol;\n createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n"
+      " cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], pol;\n}\n" ::"r"(sa(dst)),
       "l"(src), "r"(bytes), "r"(sa(bar))
       : "memory");
 }

@@ -272,29 +272,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_rows(KArgs a) {
   // ---- router logits, x quantisation and the shared gates, all rows ----------
   RArea A = r_area(L.data, H, I);
   uint8_t* xs = L.data + 2 * kSlot;  // shared gate/up: x rows (bf16)
-  // every row's x loads first, all in flight together (one round trip); the
-  // per-row warp reductions below are interleaved across rows, so their
-  // shuffle chains overlap instead of running one row after another
-  constexpr int kTR = 8 * NT;  // rows this instance handles at most
-  uint2 xall[kMaxV][kTR];
-#pragma unroll
-  for (int i = 0; i < kMaxV; ++i)
-#pragma unroll
-    for (int t = 0; t < kTR; ++t)
-      xall[i][t] = (i < nv && t < T)
-                       ? __ldcg(reinterpret_cast<const uint2*>(a.x + (size_t)t * H + k0 + 128 * i +
-                                                               4 * lane))
-                       : make_uint2(0u, 0u);
-  {
-    // 1 x 128 quantisation: group amax of every (slice, row), reduced together
-    float gm[kMaxV][kTR];
+  // Rows go through in groups of kGR, in a loop that is not unrolled: the
+  // pass runs once per launch, so its code is fetched cold every time and
+  // must stay small.  The next group's x loads are in flight while the
+  // current group is quantised and multiplied; within a group the per-row
+  // warp reductions are interleaved so their shuffle chains overlap.
+  constexpr int kGR = 4;
+  uint2 xc[kMaxV][kGR], xn[kMaxV][kGR];
+  auto load_group = [&](uint2 (&dst)[kMaxV][kGR], int t0) {
 #pragma unroll
     for (int i = 0; i < kMaxV; ++i)
 #pragma unroll
-      for (int t = 0; t < kTR; ++t) {
-        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&xall[i][t].x);
-        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&xall[i][t].y);
-        gm[i][t] = fmaxf(fmaxf(fabsf(__low2float(p0)), fabsf(__high2float(p0))),
+      for (int j = 0; j < kGR; ++j)
+        dst[i][j] = (i < nv && t0 + j < T)
+                        ? __ldcg(reinterpret_cast<const uint2*>(a.x + (size_t)(t0 + j) * H + k0 +
+                                                                128 * i + 4 * lane))
+                        : make_uint2(0u, 0u);
+  };
+  load_group(xc, 0);
+#pragma unroll 1
+  for (int t0 = 0; t0 < T; t0 += kGR) {
+    if (t0 + kGR < T) load_group(xn, t0 + kGR);
+    // 1 x 128 quantisation: group amax of every (slice, row), reduced together
+    float gm[kMaxV][kGR];
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i)
+#pragma unroll
+      for (int j = 0; j < kGR; ++j) {
+        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&xc[i][j].x);
+        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&xc[i][j].y);
+        gm[i][j] = fmaxf(fmaxf(fabsf(__low2float(p0)), fabsf(__high2float(p0))),
                          fmaxf(fabsf(__low2float(p1)), fabsf(__high2float(p1))));
       }
 #pragma unroll
@@ -302,63 +309,54 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_rows(KArgs a) {
 #pragma unroll
       for (int i = 0; i < kMaxV; ++i)
 #pragma unroll
-        for (int t = 0; t < kTR; ++t) gm[i][t] = fmaxf(gm[i][t], __shfl_xor_sync(0xffffffffu, gm[i][t], o));
+        for (int j = 0; j < kGR; ++j)
+          gm[i][j] = fmaxf(gm[i][j], __shfl_xor_sync(0xffffffffu, gm[i][j], o));
+    // router dot products (experts b, b + G) and the shared gate
+    float acc[3][kGR];
+#pragma unroll
+    for (int j = 0; j < kGR; ++j) acc[0][j] = acc[1][j] = acc[2][j] = 0.0f;
 #pragma unroll
     for (int i = 0; i < kMaxV; ++i) {
       if (i >= nv) continue;
       const int kk = k0 + 128 * i + 4 * lane;
-#pragma unroll
-      for (int t = 0; t < kTR; ++t) {
-        if (t >= T) break;
-        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&xall[i][t].x);
-        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&xall[i][t].y);
-        const float sc = group_scale(gm[i][t]);
-        const uint32_t packed =
-            quant4(__low2float(p0), __high2float(p0), __low2float(p1), __high2float(p1), sc);
-        if (is_routed) {
-          *reinterpret_cast<uint32_t*>(A.xq + (size_t)t * xq_stride(H) + kk) = packed;
-          if (lane == 0) L.sx[t * nbh + kk / kGroup] = sc;
-        } else if (is_sgu) {
-          *reinterpret_cast<uint2*>(xs + (size_t)t * xs_stride(H) + 2 * kk) = xall[i][t];
-        }
-        if (b == 0) {
-          *reinterpret_cast<uint32_t*>(a.w.xq + (size_t)t * H + kk) = packed;
-          if (lane == 0) a.w.sx[(size_t)t * nbh + kk / kGroup] = sc;
-        }
-      }
-    }
-  }
-  {
-    // router dot products (experts b, b + G) and the shared gate, every row
-    float acc[3][kTR];
-#pragma unroll
-    for (int t = 0; t < kTR; ++t) acc[0][t] = acc[1][t] = acc[2][t] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kMaxV; ++i) {
-      if (i >= nv) continue;
       const __nv_bfloat162 g0 = *reinterpret_cast<const __nv_bfloat162*>(&gw[i].x);
       const __nv_bfloat162 g1 = *reinterpret_cast<const __nv_bfloat162*>(&gw[i].y);
 #pragma unroll
-      for (int t = 0; t < kTR; ++t) {
-        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&xall[i][t].x);
-        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&xall[i][t].y);
+      for (int j = 0; j < kGR; ++j) {
+        const int t = t0 + j;
+        const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&xc[i][j].x);
+        const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&xc[i][j].y);
         const float x0 = __low2float(p0), x1 = __high2float(p0), x2 = __low2float(p1),
                     x3 = __high2float(p1);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          float s = acc[h][t];
-          s = fmaf(x0, wv[h][i].x, s);
-          s = fmaf(x1, wv[h][i].y, s);
-          s = fmaf(x2, wv[h][i].z, s);
-          s = fmaf(x3, wv[h][i].w, s);
-          acc[h][t] = s;
+          float v = acc[h][j];
+          v = fmaf(x0, wv[h][i].x, v);
+          v = fmaf(x1, wv[h][i].y, v);
+          v = fmaf(x2, wv[h][i].z, v);
+          v = fmaf(x3, wv[h][i].w, v);
+          acc[h][j] = v;
         }
-        float gs = acc[2][t];
+        float gs = acc[2][j];
         gs = fmaf(x0, __low2float(g0), gs);
         gs = fmaf(x1, __high2float(g0), gs);
         gs = fmaf(x2, __low2float(g1), gs);
         gs = fmaf(x3, __high2float(g1), gs);
-        acc[2][t] = gs;
+        acc[2][j] = gs;
+        if (t < T) {
+          const float sc = group_scale(gm[i][j]);
+          const uint32_t packed = quant4(x0, x1, x2, x3, sc);
+          if (is_routed) {
+            *reinterpret_cast<uint32_t*>(A.xq + (size_t)t * xq_stride(H) + kk) = packed;
+            if (lane == 0) L.sx[t * nbh + kk / kGroup] = sc;
+          } else if (is_sgu) {
+            *reinterpret_cast<uint2*>(xs + (size_t)t * xs_stride(H) + 2 * kk) = xc[i][j];
+          }
+          if (b == 0) {
+            *reinterpret_cast<uint32_t*>(a.w.xq + (size_t)t * H + kk) = packed;
+            if (lane == 0) a.w.sx[(size_t)t * nbh + kk / kGroup] = sc;
+          }
+        }
       }
     }
 #pragma unroll
@@ -366,16 +364,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_rows(KArgs a) {
 #pragma unroll
       for (int h = 0; h < 3; ++h)
 #pragma unroll
-        for (int t = 0; t < kTR; ++t) acc[h][t] += __shfl_xor_sync(0xffffffffu, acc[h][t], o);
+        for (int j = 0; j < kGR; ++j) acc[h][j] += __shfl_xor_sync(0xffffffffu, acc[h][j], o);
     if (lane == 0) {
 #pragma unroll
-      for (int t = 0; t < kTR; ++t) {
+      for (int j = 0; j < kGR; ++j) {
+        const int t = t0 + j;
         if (t >= T) break;
-        L.red[(0 * kW + warp) * kR + t] = acc[0][t];
-        L.red[(1 * kW + warp) * kR + t] = acc[1][t];
-        sm->gred[warp * kR + t] = acc[2][t];
+        L.red[(0 * kW + warp) * kR + t] = acc[0][j];
+        L.red[(1 * kW + warp) * kR + t] = acc[1][j];
+        sm->gred[warp * kR + t] = acc[2][j];
       }
     }
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i)
+#pragma unroll
+      for (int j = 0; j < kGR; ++j) xc[i][j] = xn[i][j];
   }
   __syncthreads();
   const unsigned long long tag = (unsigned long long)(unsigned)sm->tag << 32;

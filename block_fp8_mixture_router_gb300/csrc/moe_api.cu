@@ -268,15 +268,21 @@ bool use_row(const moe_ctx* c, int T) {
   return T == 1 && c->row_smem > 0 && (c->opt_path == 0 || c->opt_path == 1);
 }
 
-// 2..16 rows on the role-split multi-row kernel unless another decode kernel
-// is asked for.
+// 2..kRowsAuto rows on the role-split multi-row kernel unless another decode
+// kernel is asked for.  Above that the three chained kernels are faster on
+// GB300: they spread the routed work over every SM instead of the routed
+// role's share (measured at 6, 8, 11 and 16 rows).
+constexpr int kRowsAuto = 5;
+
 bool use_rows(const moe_ctx* c, int T) {
-  return T >= 2 && T <= kDecodeRows && c->rows_smem > 0 && (c->opt_path == 0 || c->opt_path == 1);
+  if (T < 2 || T > kDecodeRows || c->rows_smem <= 0) return false;
+  return c->opt_path == 6 || ((c->opt_path == 0 || c->opt_path == 1) && T <= kRowsAuto);
 }
 
+// The persistent multi-row kernel only when asked for.
 bool use_fused(const moe_ctx* c, int T) {
   size_t smem = 0;
-  return c->opt_path != 3 && c->dec_grid > 0 && decode_plan(c, T, &smem) >= 2;
+  return c->opt_path == 5 && c->dec_grid > 0 && decode_plan(c, T, &smem) >= 2;
 }
 
 cudaError_t launch_fused(moe_ctx* c, const KArgs& a, cudaStream_t s) {
@@ -802,7 +808,7 @@ int moe_set_option(moe_ctx* c, int option, int value) {
   if (!c) return MOE_ERR_INVALID_ARG;
   switch (option) {
     case MOE_OPT_PATH:
-      if (value < 0 || value > 5) return MOE_ERR_INVALID_ARG;
+      if (value < 0 || value > 6) return MOE_ERR_INVALID_ARG;
       c->opt_path = value;
       return MOE_OK;
     case MOE_OPT_PDL:

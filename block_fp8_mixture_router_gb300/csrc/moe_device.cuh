@@ -114,6 +114,10 @@ __device__ __forceinline__ float div_recip(float s) {
   return (es >= 2u && es <= 252u) ? __frcp_rn(s) : 0.0f;
 }
 
+// The IEEE division kept out of line, so that the rare operands div_shared
+// hands to it do not grow the code of every call site.
+static __device__ __noinline__ float div_ieee(float v, float s) { return __fdiv_rn(v, s); }
+
 // v / s rounded to nearest even, bit for bit the IEEE quotient, for a divisor
 // shared by many dividends (y = div_recip(s)).  One Newton step from v*y
 // leaves q within an ulp of v/s; for such a q the FMA remainder r = v - q*s
@@ -124,14 +128,14 @@ __device__ __forceinline__ float div_recip(float s) {
 // half-ulp product could leave the normal range, take the IEEE division.
 __device__ __forceinline__ float div_shared(float v, float s, float y) {
   const uint32_t ev = (__float_as_uint(v) >> 23) & 0xFFu;
-  if (y == 0.0f || ev > 252u || (ev < 32u && v != 0.0f)) return __fdiv_rn(v, s);
+  if (y == 0.0f || ev > 252u || (ev < 32u && v != 0.0f)) return div_ieee(v, s);
   if (ev < 32u) return v * y;  // a signed zero
   float q = v * y;
   q = fmaf(fmaf(-q, s, v), y, q);
   const float r = fmaf(-q, s, v);
   const uint32_t qb = __float_as_uint(q);
   const uint32_t e = (qb >> 23) & 0xFFu;
-  if (e < 64u || e > 253u) return __fdiv_rn(v, s);
+  if (e < 64u || e > 253u) return div_ieee(v, s);
   const float half = s * __uint_as_float((e - 24u) << 23);
   const bool down = (r < 0.0f) != (q < 0.0f);
   const float h = (down && (qb & 0x7FFFFFu) == 0u) ? 0.5f * half : half;
@@ -140,18 +144,40 @@ __device__ __forceinline__ float div_shared(float v, float s, float y) {
   return __uint_as_float(down ? qb - 1u : qb + 1u);
 }
 
-// Quantise four values of a group with scale s: codes of v/s (IEEE division).
-__device__ __forceinline__ uint32_t quant4(float v0, float v1, float v2, float v3, float s) {
+// Codes of v/s through the IEEE quotients, out of line (the rare groups
+// quant4 cannot settle from the product).
+static __device__ __noinline__ uint32_t quant4_exact(float v0, float v1, float v2, float v3,
+                                                     float s) {
   const float y = div_recip(s);
   return e4m3x4(div_shared(v0, s, y), div_shared(v1, s, y), div_shared(v2, s, y),
                 div_shared(v3, s, y));
 }
 
-// The same with the reciprocal already taken (y = div_recip(s)).
-__device__ __forceinline__ uint32_t quant4r(float v0, float v1, float v2, float v3, float s,
-                                            float y) {
-  return e4m3x4(div_shared(v0, s, y), div_shared(v1, s, y), div_shared(v2, s, y),
-                div_shared(v3, s, y));
+// Does the e4m3 rounding of a quotient need more than the product q = v*y
+// (y within a few ulps of 1/s)?  q is then within 4 fp32 ulps of the IEEE
+// quotient, and the two round to the same e4m3 code unless an e4m3 rounding
+// midpoint lies between them: for |q| in e4m3's normal range the midpoints
+// are the floats whose 20 mantissa bits below the kept 3 read 0x80000, so a
+// window of 8 ulps around them is flagged, and so is e4m3's subnormal range
+// (|q| < 2^-6, q != 0).  Saturation needs nothing: everything above 448
+// becomes 448.
+__device__ __forceinline__ bool e4m3_undecided(float q) {
+  const uint32_t u = __float_as_uint(q) & 0x7FFFFFFFu;
+  return (u - 1u < 0x3C800000u - 1u) | ((u & 0xFFFFFu) - 0x7FFF8u < 16u);
+}
+
+// Quantise four values of a group with scale s: the e4m3 codes of the IEEE
+// quotients v/s, taken from the products v * rcp(s) wherever those decide
+// them (all but a few groups in a million), else from the exact quotients.
+__device__ __forceinline__ uint32_t quant4(float v0, float v1, float v2, float v3, float s) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(s));
+  const float q0 = v0 * y, q1 = v1 * y, q2 = v2 * y, q3 = v3 * y;
+  const uint32_t es = (__float_as_uint(s) >> 23) & 0xFFu;
+  if ((es - 2u > 250u) | e4m3_undecided(q0) | e4m3_undecided(q1) | e4m3_undecided(q2) |
+      e4m3_undecided(q3))
+    return quant4_exact(v0, v1, v2, v3, s);
+  return e4m3x4(q0, q1, q2, q3);
 }
 
 // silu(z) = z / (1 + e^-z) with the fast exponential and divide; the

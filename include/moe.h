@@ -166,19 +166,21 @@ int moe_quantize(moe_ctx* ctx, const void* x, int rows, uint8_t* codes, float* s
  * pointers.  Asynchronous; call on the stream of that forward. */
 int moe_expert_activations(moe_ctx* ctx, int rows, uint8_t* hq, float* sh, void* stream);
 
-/* Options.  MOE_OPT_PATH: 0 = automatic (rows <= 16: the persistent decode
- * kernel, else the grouped prompt kernels on the tcgen05 tensor cores),
- * 1 = the same as 0, 2 = always the grouped prompt kernels, 3 = rows <= 16 on
- * three chained decode kernels instead of the persistent one, 4 = always the
- * grouped prompt kernels with warp-level MMAs instead of tcgen05 (the path
- * every forward takes when a context's shape leaves no room for the tcgen05
- * kernels: hidden or inter above 4096), 5 = rows <= 16 on the persistent
- * multi-row decode kernel with one grid barrier instead of the role-split
- * decode kernels (which 0 and 1 use when the device has enough SMs for
- * their roles: the one-row kernel for rows == 1, the multi-row role-split
- * kernel for 2..16 rows).  MOE_OPT_PDL: 1 = launch with programmatic
- * dependent launch so a layer's immutable weight reads overlap the previous
- * kernel's tail (default), 0 = plain launches. */
+/* Options.  MOE_OPT_PATH: 0 = automatic (rows <= 16 on the decode kernels:
+ * the role-split one-row kernel for 1 row, the role-split multi-row kernel
+ * for 2..5 rows, three chained decode kernels for 6..16 rows; more rows on
+ * the grouped prompt kernels on the tcgen05 tensor cores), 1 = the same as
+ * 0, 2 = always the grouped prompt kernels, 3 = rows <= 16 on the three
+ * chained decode kernels, 4 = always the grouped prompt kernels with
+ * warp-level MMAs instead of tcgen05 (the path every forward takes when a
+ * context's shape leaves no room for the tcgen05 kernels: hidden or inter
+ * above 4096), 5 = rows <= 16 on the persistent multi-row decode kernel with
+ * one grid barrier, 6 = 2..16 rows on the role-split multi-row kernel.  A
+ * role-split kernel needs the device to have enough SMs for its roles;
+ * without them 0, 1 and 6 take the chained kernels.
+ * MOE_OPT_PDL: 1 = launch with programmatic dependent launch so a layer's
+ * immutable weight reads overlap the previous kernel's tail (default), 0 =
+ * plain launches. */
 enum { MOE_OPT_PATH = 1, MOE_OPT_PDL = 2 };
 int moe_set_option(moe_ctx* ctx, int option, int value);
 

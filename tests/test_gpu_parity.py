@@ -105,6 +105,43 @@ def full_case(dev):
     return Case(W.WORKLOADS["decode_t1"], 1024, dev)
 
 
+def test_quantize_rounding_edges(full_case):
+    """Groups whose quotients v/s fall exactly on e4m3 rounding midpoints (ties
+    to even), on e4m3 values, in e4m3's subnormal range, and all-zero groups:
+    the kernels' codes and scales equal the oracle's bit for bit."""
+    H = full_case.shape.hidden
+    rng = np.random.default_rng(11)
+    table = oracle.e4m3_table()
+    mags = np.unique(np.abs(table[np.isfinite(table)]))
+    mids = 0.5 * (mags[:-1] + mags[1:])
+    rows = 16
+    x = np.zeros((rows, H), np.float64)
+    for t in range(rows):
+        for g in range(H // 128):
+            scale = 2.0 ** int(rng.integers(-8, 8))  # amax = 448 * scale: s = scale exactly
+            kind = (t + g) % 4
+            if kind == 0:
+                vals = rng.choice(mids, 128)
+            elif kind == 1:
+                vals = rng.choice(mags, 128)
+            elif kind == 2:
+                vals = rng.choice(np.concatenate([mids[:10], mags[:10]]), 128)
+            else:
+                vals = np.zeros(128) if g % 2 else rng.choice(mids, 128)
+            vals = vals * scale * rng.choice([-1.0, 1.0], 128)
+            if kind != 3 or g % 2 == 0:
+                vals[int(rng.integers(0, 128))] = 448.0 * scale
+            x[t, g * 128:(g + 1) * 128] = vals
+    xt = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16)
+    assert np.array_equal(xt.float().numpy().astype(np.float64), x)  # exact in bf16
+    codes, scales = full_case.moe.quantize(xt.cuda())
+    torch.cuda.synchronize()
+    for t in range(rows):
+        rc, rs = oracle.quant_row(x[t].astype(np.float32))
+        assert np.array_equal(codes[t].cpu().numpy(), rc), t
+        assert np.array_equal(scales[t].cpu().numpy(), rs), t
+
+
 def test_decode_t1(full_case):
     x = full_case.x(1)
     run_and_check(full_case, x)
@@ -139,16 +176,35 @@ def test_decode_t1_repeated_launches_bitwise(full_case):
     assert full_case.moe.device_status() == m.MOE_OK
 
 
-def test_decode_t11(dev):
-    case = Case(W.WORKLOADS["decode_t11"], 64, dev)
-    x = case.x(11)
-    run_and_check(case, x)
-    idx, _ = case.moe.route(x)
+@pytest.fixture(scope="module")
+def t11_case(dev):
+    return Case(W.WORKLOADS["decode_t11"], 64, dev)
+
+
+@pytest.mark.parametrize("path", [m.PATH_AUTO, m.PATH_DECODE_ROWS, m.PATH_DECODE_MULTIROW])
+def test_decode_t11(t11_case, path):
+    """Eleven rows with overlapping expert sets on the automatic path (the
+    chained decode kernels), the role-split multi-row kernel and the
+    persistent multi-row kernel."""
+    x = t11_case.x(11)
+    try:
+        run_and_check(t11_case, x, path=path)
+        idx, _ = t11_case.moe.route(x)
+    finally:
+        t11_case.moe.set_option(m.MOE_OPT_PATH, m.PATH_AUTO)
     distinct = len(set(idx.cpu().numpy().ravel().tolist()))
     assert distinct < 11 * 8, "rows were meant to share experts"
 
 
-@pytest.mark.parametrize("rows", [2, 4, 16, 17, 64, 255])
+def test_path_option_range(t11_case):
+    assert t11_case.moe.ctx is not None
+    assert m.moe_set_option(t11_case.moe.ctx, m.MOE_OPT_PATH, 7) == m.MOE_ERR_INVALID_ARG
+    assert m.moe_set_option(t11_case.moe.ctx, m.MOE_OPT_PATH, -1) == m.MOE_ERR_INVALID_ARG
+    assert m.moe_set_option(t11_case.moe.ctx, m.MOE_OPT_PATH, m.PATH_DECODE_ROWS) == m.MOE_OK
+    assert m.moe_set_option(t11_case.moe.ctx, m.MOE_OPT_PATH, m.PATH_AUTO) == m.MOE_OK
+
+
+@pytest.mark.parametrize("rows", [2, 4, 5, 6, 16, 17, 64, 255])
 def test_ragged_rows(full_case, rows):
     x = full_case.x(rows, tag=f"r{rows}")
     sample = sorted(set([0, rows - 1] + list(range(0, rows, max(1, rows // 6)))))
