@@ -417,7 +417,14 @@ def run_ours(args):
         for name, t in nets[j].profile(xs[j], ys[j], stream=stream):
             stage_ms.setdefault(name, []).append(t)
     stage_avg = {n: sum(v) / len(v) for n, v in stage_ms.items()}
+    stage_prof = dict(stage_avg)
     launches_per_step = len(stage_avg)
+    duration_source = "per-kernel CUDA events of a profiled forward (moe_profile_forward)"
+    if launches_per_step == 1:
+        # one kernel per layer forward: its launches are the timed region's
+        # launches, so their average duration is the timed region's
+        stage_avg = {n: ms / K / layers_per_step for n in stage_avg}
+        duration_source = "CUDA events over the timed region (one launch per layer forward)"
 
     # touched experts per instance
     Us = []
@@ -435,7 +442,8 @@ def run_ours(args):
     sf = stage_flops(s, T).get(dom)
     roof = {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": hbm, "unit": "GB/s",
             "frac": dom_gbs / hbm, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": sb[dom],
-            "avg_launch_us": stage_avg[dom] * 1e3, "traffic": traffic_for(dom, wl.name)}
+            "avg_launch_us": stage_avg[dom] * 1e3, "duration_source": duration_source,
+            "traffic": traffic_for(dom, wl.name)}
     if sf is not None:
         tf_peak = bf16_tf * (2.0 if sf[0] == "fp8" else 1.0)
         tf = sf[1] / (stage_avg[dom] * 1e-3) / 1e12
@@ -471,7 +479,7 @@ def run_ours(args):
                            "frac": lb / (step_ms * 1e-3) / 1e9 / hbm,
                            "distinct_experts": U,
                            "fp8_tflops": fp8_flops(s, T) / (step_ms * 1e-3) / 1e12},
-        "stages_us": {n: round(v * 1e3, 3) for n, v in stage_avg.items()},
+        "stages_us": {n: round(v * 1e3, 3) for n, v in stage_prof.items()},
         "gpu_launches": K * launches_per_step * layers_per_step,
         "clocks": clocks,
     }

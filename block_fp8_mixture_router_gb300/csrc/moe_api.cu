@@ -44,6 +44,10 @@ struct moe_ctx {
   int part_rows = 0;             // splits x rows the partial buffer holds
   uint8_t* xg = nullptr;   // e4m3 activations in slot order [max_rows*k][H]
   float* sxg = nullptr;    // their scales [max_rows*k][H/128]
+  // prompt path: the shared expert runs on a second stream, forked from and
+  // joined back into the caller's stream within each forward
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 
 namespace {
@@ -154,6 +158,11 @@ Plan make_plan(const moe_config* c) {
 void free_all(moe_ctx* c) {
   for (void* ptr : c->allocs) cudaFree(ptr);
   c->allocs.clear();
+  if (c->ev_join) cudaEventDestroy(c->ev_join);
+  if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+  if (c->side) cudaStreamDestroy(c->side);
+  c->ev_join = c->ev_fork = nullptr;
+  c->side = nullptr;
 }
 
 int check_launch(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -432,20 +441,38 @@ int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
     const int tiles = (T + 127) / 128;
     const int g_sgu = std::min(c->sm_count, tiles * sgu.n_f);
     const int g_sdn = std::min(c->sm_count, tiles * sdn.n_f);
+    // The shared expert needs only x: it runs on the side stream alongside
+    // the routing kernels and the routed GEMMs, and the combine waits for
+    // it.  A profiled forward keeps every kernel on the caller's stream so
+    // that each stage is timed alone.
+    const bool fork = rec == nullptr && c->side != nullptr;
+    if (fork) {
+      if (cudaEventRecord(c->ev_fork, s) != cudaSuccess ||
+          cudaStreamWaitEvent(c->side, c->ev_fork, 0) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      if (launch_tc_gemm(kTcSharedGateUp, sgu, g_sgu, c->tc_smem[kTcSharedGateUp], c->side) !=
+              cudaSuccess ||
+          launch_tc_gemm(kTcSharedDown, sdn, g_sdn, c->tc_smem[kTcSharedDown], c->side) !=
+              cudaSuccess ||
+          cudaEventRecord(c->ev_join, c->side) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    } else {
+      LAUNCH(launch_tc_gemm(kTcSharedGateUp, sgu, g_sgu, c->tc_smem[kTcSharedGateUp], s),
+             "shared_gateup_tc");
+      LAUNCH(launch_tc_gemm(kTcSharedDown, sdn, g_sdn, c->tc_smem[kTcSharedDown], s),
+             "shared_down_tc");
+    }
     LAUNCH(launch_tc_gemm(kTcRouter, rt, g_rt, c->tc_smem[kTcRouter], s), "router_tc");
     LAUNCH(launch_topk_after_router(a, c, rt, s), "topk");
     LAUNCH(launch_schedule(a, s), "schedule");
     LAUNCH(launch_quant_scatter(a, c->xg, c->sxg, s), "quant_scatter");
-    LAUNCH(launch_tc_gemm(kTcSharedGateUp, sgu, g_sgu, c->tc_smem[kTcSharedGateUp], s),
-           "shared_gateup_tc");
     LAUNCH(launch_tc_gemm(kTcRoutedGateUp, c->tc[kTcRoutedGateUp], c->sm_count,
                           c->tc_smem[kTcRoutedGateUp], s),
            "gateup_tc");
-    LAUNCH(launch_tc_gemm(kTcSharedDown, sdn, g_sdn, c->tc_smem[kTcSharedDown], s),
-           "shared_down_tc");
     LAUNCH(launch_tc_gemm(kTcRoutedDown, c->tc[kTcRoutedDown], c->sm_count,
                           c->tc_smem[kTcRoutedDown], s),
            "down_tc");
+    if (fork && cudaStreamWaitEvent(s, c->ev_join, 0) != cudaSuccess) return MOE_ERR_CUDA;
     LAUNCH(launch_combine(a, s), "combine");
     return MOE_OK;
   }
@@ -558,6 +585,14 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
   w.sched_blk = (int*)ptrs[38];
   w.xw = (unsigned long long*)ptrs[39];
   c->part_rows = (int)router_part_rows(cfg);
+  if (cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    free_all(c);
+    delete c;
+    return MOE_ERR_CUDA;
+  }
   // counters start at zero and are reset by the kernels that use them
   if (cudaMemset(w.gcount, 0, plan.sizes[25]) != cudaSuccess ||
       cudaMemset(w.status, 0, plan.sizes[29]) != cudaSuccess ||
