@@ -281,11 +281,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
 
   // ---- router logits, x quantisation (1 x 128 groups) and the shared gate ----
   float acc2[2] = {0.0f, 0.0f}, gacc = 0.0f;
+  // both slices' x loads in flight together (the stores below could alias
+  // x as far as the compiler knows, so it would not hoist the second)
+  uint2 xr[kMaxV];
+#pragma unroll
+  for (int i = 0; i < kMaxV; ++i)
+    xr[i] = i < nv ? __ldcg(reinterpret_cast<const uint2*>(a.x + k0 + 128 * i + 4 * lane))
+                   : make_uint2(0u, 0u);
 #pragma unroll
   for (int i = 0; i < kMaxV; ++i) {
     if (i >= nv) continue;
     const int kk = k0 + 128 * i + 4 * lane;
-    const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(a.x + kk));
+    const uint2 raw = xr[i];
     const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
     const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
     const float x0 = __low2float(p0), x1 = __high2float(p0), x2 = __low2float(p1),

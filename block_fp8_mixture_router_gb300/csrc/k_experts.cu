@@ -424,6 +424,8 @@ __global__ void __launch_bounds__(256) k_combine(KArgs a) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= a.d.T * per_row) return;
   const int t = i / per_row, m = (i % per_row) * 8;
+  pdl_wait();
+  pdl_trigger();
   float acc[8] = {};
   for (int j = 0; j < k; ++j) {
     const int slot = __ldcg(a.w.slot_of_pair + t * k + j);
@@ -450,10 +452,9 @@ __global__ void __launch_bounds__(256) k_combine(KArgs a) {
   *reinterpret_cast<uint4*>(a.y + (size_t)t * H + m) = out;
 }
 
-cudaError_t launch_combine(const KArgs& a, cudaStream_t s) {
+cudaError_t launch_combine(const KArgs& a, cudaStream_t s, bool pdl) {
   const int n = a.d.T * (a.d.H / 8);
-  k_combine<<<(n + 255) / 256, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_combine, dim3((n + 255) / 256), dim3(256), 0, s, pdl, a);
 }
 
 // ---- re-quantised SwiGLU rows by (row, rank), for checking -----------------

@@ -36,7 +36,10 @@ namespace moe {
 
 namespace {
 
-constexpr int kEpiWarps = 16;                    // 4 per TMEM lane quarter
+// Epilogue warps, 2 per TMEM lane quarter: with the TMA and MMA warps that is
+// 10 warps, at most 3 on one SM sub-partition, so each thread may hold up to
+// 168 registers (the block-FP8 epilogue keeps 2 x 32 promoted accumulators)
+constexpr int kEpiWarps = 8;
 constexpr int kTcThreads = 64 + 32 * kEpiWarps;  // + the TMA and MMA warps
 constexpr int kTile = 128;        // output features per tile (M)
 constexpr int kKBytes = 128;      // bytes of K per stage (one 128B swizzle row)
@@ -199,6 +202,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
     tc::tmem_alloc(s_tmem, kTmemCols);
     tc::tmem_relinquish();
   }
+  // everything above touches no data of the previous kernel
+  pdl_wait();
+  pdl_trigger();
   int n_tiles;
   if constexpr (kRouted) {
     // token tiles per expert and their prefix (warp 0; E <= 256, 8 per lane)
@@ -364,18 +370,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
         tc::fence_after_sync();
         const uint32_t ta0 = tmem + tl + tb * kAcc + c0;
         if constexpr (kF8) {
-          // block-FP8: partial x (weight block scale x token scale), all
-          // kCols columns of both tiles under one TMEM wait
-          static_assert(kCols == 16, "one x16 load per tile");
+          // block-FP8: partial x (weight block scale x token scale), 16
+          // columns of both tiles under one TMEM wait at a time
+          static_assert(kCols % 16 == 0, "x16 loads per tile");
           const float wg = s_wg[kb], wu = s_wu[kb];
-          if (c0 < n16) {
-            uint32_t va[16], vb[16];
-            tc::tmem_ld16x2(ta0, ta0 + kN, va, vb);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float s = sc_tok[(c0 + i) * n_k + kb];
-              acc0[i] = fmaf(__uint_as_float(va[i]), wg * s, acc0[i]);
-              acc1[i] = fmaf(__uint_as_float(vb[i]), wu * s, acc1[i]);
+          for (int c4 = 0; c4 < kCols / 16; ++c4) {
+            if (c0 + 16 * c4 < n16) {
+              uint32_t va[16], vb[16];
+              tc::tmem_ld16x2(ta0 + 16 * c4, ta0 + kN + 16 * c4, va, vb);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float s = sc_tok[(c0 + 16 * c4 + i) * n_k + kb];
+                acc0[16 * c4 + i] = fmaf(__uint_as_float(va[i]), wg * s, acc0[16 * c4 + i]);
+                acc1[16 * c4 + i] = fmaf(__uint_as_float(vb[i]), wu * s, acc1[16 * c4 + i]);
+              }
             }
           }
         } else {
@@ -519,6 +528,8 @@ __global__ void __launch_bounds__(256) k_quant_scatter(KArgs a, uint8_t* xg, flo
   __shared__ float red[8];
   const int t = blockIdx.x, H = a.d.H, k = a.d.k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x < k) slots[threadIdx.x] = a.w.slot_of_pair[t * k + threadIdx.x];
   __syncthreads();
   const bf16* xr = a.x + (size_t)t * H;
@@ -598,15 +609,27 @@ cudaError_t setup_tc_gemm(int kind, size_t smem) {
                               (int)smem);
 }
 
-cudaError_t launch_tc_gemm(int kind, const TcGemm& g, int grid, size_t smem, cudaStream_t s) {
+cudaError_t launch_tc_gemm(int kind, const TcGemm& g, int grid, size_t smem, cudaStream_t s,
+                           bool pdl) {
   if (grid < 1) return cudaSuccess;
   void* args[] = {const_cast<TcGemm*>(&g)};
-  return cudaLaunchKernel(kernel_of(kind), dim3(grid), dim3(kTcThreads), args, smem, s);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, kernel_of(kind), args);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_quant_scatter(const KArgs& a, uint8_t* xg, float* sxg, cudaStream_t s) {
-  k_quant_scatter<<<a.d.T, 256, 0, s>>>(a, xg, sxg);
-  return cudaGetLastError();
+cudaError_t launch_quant_scatter(const KArgs& a, uint8_t* xg, float* sxg, cudaStream_t s,
+                                 bool pdl) {
+  return launch_pdl(k_quant_scatter, dim3(a.d.T), dim3(256), 0, s, pdl, a, xg, sxg);
 }
 
 // Tensor map of a row-major 2-D array [rows][cols] (element size `esize`),

@@ -73,13 +73,14 @@ cudaError_t launch_quant_gamma(const KArgs& a, cudaStream_t s) {
 __global__ void __launch_bounds__(256) k_topk(KArgs a) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= a.d.T) return;
+  pdl_wait();
+  pdl_trigger();
   topk_row(a.w.logits + (size_t)t * a.d.E, a.d.E, a.d.k, a.w.idx + (size_t)t * a.d.k,
            a.w.wts + (size_t)t * a.d.k);
 }
 
-cudaError_t launch_topk(const KArgs& a, cudaStream_t s) {
-  k_topk<<<(a.d.T + 7) / 8, 256, 0, s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_topk(const KArgs& a, cudaStream_t s, bool pdl) {
+  return launch_pdl(k_topk, dim3((a.d.T + 7) / 8), dim3(256), 0, s, pdl, a);
 }
 
 // One warp per row: logits[t][e] = sum over splits s = 0..ks-1, in that
@@ -88,6 +89,8 @@ __global__ void __launch_bounds__(256) k_topk_splits(KArgs a, const float* __res
                                                      int ks) {
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= a.d.T) return;
+  pdl_wait();
+  pdl_trigger();
   const int E = a.d.E, lane = threadIdx.x & 31;
   float* row = a.w.logits + (size_t)t * E;
   const size_t stride = (size_t)a.d.T * E;
@@ -119,9 +122,9 @@ __global__ void __launch_bounds__(256) k_topk_splits(KArgs a, const float* __res
   topk_row(row, E, a.d.k, a.w.idx + (size_t)t * a.d.k, a.w.wts + (size_t)t * a.d.k);
 }
 
-cudaError_t launch_topk_splits(const KArgs& a, const float* part, int ks, cudaStream_t s) {
-  k_topk_splits<<<(a.d.T + 7) / 8, 256, 0, s>>>(a, part, ks);
-  return cudaGetLastError();
+cudaError_t launch_topk_splits(const KArgs& a, const float* part, int ks, cudaStream_t s,
+                               bool pdl) {
+  return launch_pdl(k_topk_splits, dim3((a.d.T + 7) / 8), dim3(256), 0, s, pdl, a, part, ks);
 }
 
 // ---- schedule: stable slots sorted by (expert, row), and expert chunks ----
@@ -142,6 +145,8 @@ __global__ void __launch_bounds__(256) k_sched_count(KArgs a, int* __restrict__ 
   const int T = a.d.T, k = a.d.k, E = a.d.E, b = blockIdx.x, tid = threadIdx.x;
   const int t0 = b * kSchedRows, nt = min(kSchedRows, T - t0);
   for (int i = tid; i < E * (kSchedRows / 32); i += 256) (&bm[0][0])[i] = 0u;
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   const int p0 = t0 * k, np = nt * k;
   for (int i = tid; i < np; i += 256) {
@@ -173,6 +178,8 @@ __global__ void __launch_bounds__(256) k_sched_finish(KArgs a, const int* __rest
   const int T = a.d.T, k = a.d.k, E = a.d.E, b = blockIdx.x, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   int tot = 0, chs = 0;
+  pdl_wait();
+  pdl_trigger();
   if (tid < E) {
     int pre = 0, rest = 0;
     for (int bb = 0; bb < b; ++bb) pre += __ldg(blk_cnt + (size_t)bb * E + tid);
@@ -245,14 +252,14 @@ __global__ void __launch_bounds__(256) k_sched_finish(KArgs a, const int* __rest
 
 cudaError_t setup_schedule() { return cudaSuccess; }
 
-cudaError_t launch_schedule(const KArgs& a, cudaStream_t s) {
+cudaError_t launch_schedule(const KArgs& a, cudaStream_t s, bool pdl) {
   const int nb = (a.d.T + kSchedRows - 1) / kSchedRows;
   int* rank = a.w.sched_rank;
   int* blk = a.w.sched_blk;
-  k_sched_count<<<nb, 256, 0, s>>>(a, rank, blk);
-  if (cudaGetLastError() != cudaSuccess) return cudaErrorLaunchFailure;
-  k_sched_finish<<<nb, 256, 0, s>>>(a, rank, blk, nb);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(k_sched_count, dim3(nb), dim3(256), 0, s, pdl, a, rank, blk);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_sched_finish, dim3(nb), dim3(256), 0, s, pdl, a, (const int*)rank,
+                    (const int*)blk, nb);
 }
 
 }  // namespace moe

@@ -190,7 +190,7 @@ bool use_fused(const moe_ctx* c, int T);
 bool use_tc(const moe_ctx* c, int T);
 bool router_args(const moe_ctx* c, const void* x, int T, TcGemm* rt, int* grid);
 cudaError_t launch_topk_after_router(const KArgs& a, const moe_ctx* c, const TcGemm& rt,
-                                     cudaStream_t s);
+                                     cudaStream_t s, bool pdl);
 cudaError_t launch_fused(moe_ctx* c, const KArgs& a, cudaStream_t s);
 
 // Routing with the kernels the forward of T rows would use (the persistent
@@ -223,7 +223,7 @@ int run_router_and_quant(moe_ctx* c, const KArgs& a, cudaStream_t s) {
     int g_rt = 0;
     if (!router_args(c, a.x, a.d.T, &rt, &g_rt)) return MOE_ERR_CUDA;
     if (launch_tc_gemm(kTcRouter, rt, g_rt, c->tc_smem[kTcRouter], s) != cudaSuccess ||
-        launch_topk_after_router(a, c, rt, s) != cudaSuccess)
+        launch_topk_after_router(a, c, rt, s, false) != cudaSuccess)
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
@@ -403,8 +403,9 @@ bool router_args(const moe_ctx* c, const void* x, int T, TcGemm* rt, int* grid) 
 }
 
 cudaError_t launch_topk_after_router(const KArgs& a, const moe_ctx* c, const TcGemm& rt,
-                                     cudaStream_t s) {
-  return rt.ksplit > 1 ? launch_topk_splits(a, c->logits_part, rt.ksplit, s) : launch_topk(a, s);
+                                     cudaStream_t s, bool pdl) {
+  return rt.ksplit > 1 ? launch_topk_splits(a, c->logits_part, rt.ksplit, s, pdl)
+                       : launch_topk(a, s, pdl);
 }
 
 int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
@@ -462,18 +463,24 @@ int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
       LAUNCH(launch_tc_gemm(kTcSharedDown, sdn, g_sdn, c->tc_smem[kTcSharedDown], s),
              "shared_down_tc");
     }
-    LAUNCH(launch_tc_gemm(kTcRouter, rt, g_rt, c->tc_smem[kTcRouter], s), "router_tc");
-    LAUNCH(launch_topk_after_router(a, c, rt, s), "topk");
-    LAUNCH(launch_schedule(a, s), "schedule");
-    LAUNCH(launch_quant_scatter(a, c->xg, c->sxg, s), "quant_scatter");
+    // the main stream's kernels are chained by programmatic dependent launch:
+    // each waits for its predecessor before touching its data, and its
+    // prologue (barriers, tensor memory, descriptor prefetch) overlaps the
+    // predecessor's tail
+    const bool pdl = c->opt_pdl != 0;
+    LAUNCH(launch_tc_gemm(kTcRouter, rt, g_rt, c->tc_smem[kTcRouter], s, pdl), "router_tc");
+    LAUNCH(launch_topk_after_router(a, c, rt, s, pdl), "topk");
+    LAUNCH(launch_schedule(a, s, pdl), "schedule");
+    LAUNCH(launch_quant_scatter(a, c->xg, c->sxg, s, pdl), "quant_scatter");
     LAUNCH(launch_tc_gemm(kTcRoutedGateUp, c->tc[kTcRoutedGateUp], c->sm_count,
-                          c->tc_smem[kTcRoutedGateUp], s),
+                          c->tc_smem[kTcRoutedGateUp], s, pdl),
            "gateup_tc");
     LAUNCH(launch_tc_gemm(kTcRoutedDown, c->tc[kTcRoutedDown], c->sm_count,
-                          c->tc_smem[kTcRoutedDown], s),
+                          c->tc_smem[kTcRoutedDown], s, pdl),
            "down_tc");
     if (fork && cudaStreamWaitEvent(s, c->ev_join, 0) != cudaSuccess) return MOE_ERR_CUDA;
-    LAUNCH(launch_combine(a, s), "combine");
+    // after the join the combine waits on the side stream as well: plain launch
+    LAUNCH(launch_combine(a, s, pdl && !fork), "combine");
     return MOE_OK;
   }
   LAUNCH(launch_router(a, s), "router");

@@ -82,15 +82,16 @@ inline int max_chunks(int T, int k, int E) { return (T * k + kChunk - 1) / kChun
 // Launchers (return cudaGetLastError()).
 cudaError_t launch_router(const KArgs& a, cudaStream_t s);
 cudaError_t launch_quant_gamma(const KArgs& a, cudaStream_t s);
-cudaError_t launch_topk(const KArgs& a, cudaStream_t s);
+cudaError_t launch_topk(const KArgs& a, cudaStream_t s, bool pdl = false);
 // top-k of logits given as `ks` partial sums part[ks][T][E], summed in split
 // order into the workspace logits first
-cudaError_t launch_topk_splits(const KArgs& a, const float* part, int ks, cudaStream_t s);
-cudaError_t launch_schedule(const KArgs& a, cudaStream_t s);
+cudaError_t launch_topk_splits(const KArgs& a, const float* part, int ks, cudaStream_t s,
+                               bool pdl = false);
+cudaError_t launch_schedule(const KArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t setup_schedule();
 cudaError_t launch_gateup(const KArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_down(const KArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_combine(const KArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const KArgs& a, cudaStream_t s, bool pdl = false);
 
 // ---- one-row decode kernel (k_decode_row.cu) ---------------------------------
 size_t decode_row_smem(int G, int H, int E, int k, int I, int Is);
@@ -135,8 +136,10 @@ struct TcGemm {
 
 size_t tc_gemm_smem(int kind, int n_k);
 cudaError_t setup_tc_gemm(int kind, size_t smem);
-cudaError_t launch_tc_gemm(int kind, const TcGemm& g, int grid, size_t smem, cudaStream_t s);
-cudaError_t launch_quant_scatter(const KArgs& a, uint8_t* xg, float* sxg, cudaStream_t s);
+cudaError_t launch_tc_gemm(int kind, const TcGemm& g, int grid, size_t smem, cudaStream_t s,
+                           bool pdl = false);
+cudaError_t launch_quant_scatter(const KArgs& a, uint8_t* xg, float* sxg, cudaStream_t s,
+                                 bool pdl = false);
 cudaError_t launch_split_router(const float* wr, bf16* out, int E, int Epad, int H, cudaStream_t s);
 bool make_tc_map(CUtensorMap* m, bool bf16_elems, const void* ptr, uint64_t rows, uint64_t cols,
                  uint32_t box_rows);

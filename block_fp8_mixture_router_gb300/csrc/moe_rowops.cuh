@@ -112,9 +112,115 @@ __device__ __forceinline__ void topk_row(const float* logits, int E, int k, int*
 // scratch of 2*kWarps*16 entries each; idx_out / w_out (shared memory)
 // receive the experts in rank order and their softmax weights.  The caller
 // synchronises the CTA afterwards.
+// Fast variant for k <= 8 and a multiple of four warps: every thread ranks
+// its own expert among its warp's 32 (counting the keys that beat it, read
+// from shared memory as broadcast vectors, no serial rounds); the k best of
+// each warp go to slots [warp][rank]; then four threads per candidate count,
+// over a quarter of the lists each, the candidates that beat it, and the
+// candidates ranked below k write the result.  Same order as below.
 template <int kWarps>
-__device__ void topk_one_row(const float* lg, int E, int k, uint32_t* cand_key, uint32_t* cand_id,
-                             int* idx_out, float* w_out) {
+__device__ void topk_one_row_fast(const float* lg, int E, int k, uint32_t* cand_key,
+                                  uint32_t* cand_id, int* idx_out, float* w_out) {
+  static_assert(kWarps % 4 == 0, "lists split in quarters");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = 32 * warp + lane;
+  const uint32_t my = e < E ? order_key(lg[e]) : 0u;
+  {
+    int r = 0;
+    const int base = 32 * warp;
+    if (base + 32 <= E) {
+      const float4* row = reinterpret_cast<const float4*>(lg + base);
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 v = row[j4];
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t kj = order_key(vv[c]);
+          const int j = 4 * j4 + c;
+          r += ((kj > my) | ((kj == my) & (j < lane))) ? 1 : 0;
+        }
+      }
+    } else {
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t kj = base + j < E ? order_key(lg[base + j]) : 0u;
+        r += ((kj > my) | ((kj == my) & (j < lane))) ? 1 : 0;
+      }
+    }
+    if (r < k) {
+      cand_key[warp * 8 + r] = my;
+      cand_id[warp * 8 + r] = (uint32_t)e;
+    }
+  }
+  __syncthreads();
+  uint32_t* rank_key = cand_key + 8 * kWarps;
+  uint32_t* rank_id = cand_id + 8 * kWarps;
+  {
+    const int c = threadIdx.x >> 2, part = threadIdx.x & 3;
+    int rank = 0;
+    uint32_t K = 0u, D = 0u;
+    const bool have = c < 8 * kWarps;
+    if (have) {
+      K = cand_key[c];
+      D = cand_id[c];
+      constexpr int kPer = kWarps / 4;
+#pragma unroll
+      for (int w = 0; w < kPer; ++w) {
+        const int w2 = part * kPer + w;
+        const uint4 k0 = *reinterpret_cast<const uint4*>(cand_key + w2 * 8);
+        const uint4 k1 = *reinterpret_cast<const uint4*>(cand_key + w2 * 8 + 4);
+        const uint4 d0 = *reinterpret_cast<const uint4*>(cand_id + w2 * 8);
+        const uint4 d1 = *reinterpret_cast<const uint4*>(cand_id + w2 * 8 + 4);
+        const uint32_t K8[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        const uint32_t D8[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2)
+          rank += ((s2 < k) & ((K8[s2] > K) | ((K8[s2] == K) & (D8[s2] < D)))) ? 1 : 0;
+      }
+    }
+    rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+    rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+    if (have && part == 0 && (c & 7) < k && rank < k) {
+      rank_key[rank] = K;
+      rank_id[rank] = D;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t my_key = lane < k ? rank_key[lane] : 0u;
+    const float top = key_value(__shfl_sync(0xffffffffu, my_key, 0));
+    const float ex = lane < k ? __expf(key_value(my_key) - top) : 0.0f;
+    const float den = warp_sum(ex);
+    if (lane < k) {
+      idx_out[lane] = (int)rank_id[lane];
+      w_out[lane] = __fdividef(ex, den);
+    }
+  }
+}
+
+template <int kWarps>
+__device__ __noinline__ void topk_one_row_general(const float* lg, int E, int k,
+                                                  uint32_t* cand_key, uint32_t* cand_id,
+                                                  int* idx_out, float* w_out);
+
+template <int kWarps>
+__device__ __forceinline__ void topk_one_row(const float* lg, int E, int k, uint32_t* cand_key,
+                                             uint32_t* cand_id, int* idx_out, float* w_out) {
+  if constexpr (kWarps % 4 == 0) {
+    if (k <= 8 && E <= 32 * kWarps) {
+      topk_one_row_fast<kWarps>(lg, E, k, cand_key, cand_id, idx_out, w_out);
+      return;
+    }
+  }
+  topk_one_row_general<kWarps>(lg, E, k, cand_key, cand_id, idx_out, w_out);
+}
+
+// The general path (any k <= 16), out of line so that its code stays out of
+// the fast path's way.
+template <int kWarps>
+__device__ __noinline__ void topk_one_row_general(const float* lg, int E, int k,
+                                                  uint32_t* cand_key, uint32_t* cand_id,
+                                                  int* idx_out, float* w_out) {
   static_assert(kWarps <= 32, "one list per lane");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   {
