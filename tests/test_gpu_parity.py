@@ -177,6 +177,65 @@ def test_decode_t1_repeated_launches_bitwise(full_case):
 
 
 @pytest.fixture(scope="module")
+def tie_layer(dev):
+    """A full-width layer whose router repeats rows: experts 100 and 200 copy
+    expert 3's row, 7 and 250 copy expert 5's, so their logits tie exactly
+    on both sides for every input."""
+    s = W.FULL
+    layer = W.make_layer(s, 4242, device=dev)
+    wr = layer["router"]
+    for a, b in ((3, 100), (3, 200), (5, 7), (5, 250)):
+        wr[b] = wr[a]
+    net = m.MoELayer(_shape(s), max_rows=64)
+    net.load(layer)
+    return layer, net, W.to_numpy_layer(layer)
+
+
+@pytest.mark.parametrize("rows,path", [(1, m.PATH_AUTO), (1, m.PATH_DECODE_MULTIROW),
+                                       (1, m.PATH_DECODE_CHAINED), (3, m.PATH_AUTO),
+                                       (8, m.PATH_AUTO), (8, m.PATH_DECODE_ROWS),
+                                       (40, m.PATH_AUTO), (40, m.PATH_PROMPT_MMA)])
+def test_exact_ties(tie_layer, rows, path):
+    """Exact ties take the lower expert first at every rank, with no near-tie
+    slack: rows along router row 3 put the tie group {3, 100, 200} on top,
+    rows along rows 5 and 3 put {5, 7, 250} first, and all-zero rows tie all
+    256 experts (experts 0..7, equal weights, zero codes with scale 1)."""
+    layer, net, host = tie_layer
+    wr = layer["router"].float().cpu()
+    x = torch.zeros((rows, wr.shape[1]))
+    for t in range(rows):
+        if t % 3 == 1:
+            x[t] = wr[3] * 40.0
+        elif t % 3 == 2:
+            x[t] = wr[5] * 40.0 + wr[3] * 10.0
+    x = x.to(torch.bfloat16).cuda()
+    net.set_option(m.MOE_OPT_PATH, path)
+    try:
+        y = net.forward(x)
+        idx, w = net.route(x)
+        codes, scales = net.quantize(x)
+        torch.cuda.synchronize()
+    finally:
+        net.set_option(m.MOE_OPT_PATH, m.PATH_AUTO)
+    ref = oracle.moe_rows(host, bits(x), trace=True)
+    gi = idx.cpu().numpy()
+    for t in range(rows):
+        if t % 3 == 0:
+            assert gi[t].tolist() == list(range(8)), (t, gi[t])
+            assert np.allclose(w.cpu().numpy()[t], 0.125, rtol=0, atol=1e-7)
+        elif t % 3 == 1:
+            assert gi[t][:3].tolist() == [3, 100, 200], (t, gi[t])
+        else:
+            assert gi[t][:3].tolist() == [5, 7, 250], (t, gi[t])
+    near, differ = check_topk(gi, ref.trace["logits"], 8)
+    assert not differ.any()
+    assert np.array_equal(gi, ref.trace["idx"])
+    assert np.array_equal(codes.cpu().numpy(), ref.trace["xq"])
+    assert np.array_equal(scales.cpu().numpy(), ref.trace["sx"])
+    check_output(bits(y), ref.y_ref)
+
+
+@pytest.fixture(scope="module")
 def t11_case(dev):
     return Case(W.WORKLOADS["decode_t11"], 64, dev)
 
