@@ -74,9 +74,14 @@ __host__ __device__ inline Roles make_roles(int G, int H, int k, int I, int Is) 
   return r;
 }
 
+// Routed weight rows sit in shared memory 16 bytes apart from a multiple of
+// 128: the eight rows an MMA fragment reads at once then fall in different
+// banks (a row per bulk copy).
+constexpr int kRowPad = 16;
+
 // Bytes of weights a role keeps in shared memory at once.
 __host__ __device__ inline size_t data_bytes(const Roles& r, int H, int I, int Is) {
-  const size_t routed = (size_t)2 * r.F * H + (size_t)kGroup * I;
+  const size_t routed = (size_t)2 * r.F * (H + kRowPad) + (size_t)kGroup * (I + kRowPad);
   const size_t sgu = (size_t)kSguSlots * 16 * H * 2;
   const size_t sdn = (size_t)kSdnSlots * kSdnUnit * Is * 2;
   size_t m = routed > sgu ? routed : sgu;
@@ -170,7 +175,7 @@ __device__ inline Xw xw_of(unsigned long long* base, int k, int H, int I, int Is
 // operand is the single quantised row (all eight columns see it; column 0 is
 // kept).  Partial products are scaled per 64-byte K slice by the weight
 // block scale and the activation group scale.
-__device__ __forceinline__ void routed_part(const uint8_t* rows, int H, const float* sg,
+__device__ __forceinline__ void routed_part(const uint8_t* rows, int ld, const float* sg,
                                             const float* su, const uint8_t* xq, const float* sx,
                                             int b0, int b1, float (&acc)[4]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
@@ -178,8 +183,8 @@ __device__ __forceinline__ void routed_part(const uint8_t* rows, int H, const fl
   for (int b = b0; b < b1; ++b) {  // 64-byte slices of K
     const int kb = b >> 1;
     const int off = b * 64 + 16 * q;
-    const uint4 ag = lds16(rows + (size_t)g * H + off);
-    const uint4 au = lds16(rows + (size_t)(8 + g) * H + off);
+    const uint4 ag = lds16(rows + (size_t)g * ld + off);
+    const uint4 au = lds16(rows + (size_t)(8 + g) * ld + off);
     const uint4 bx = lds16(xq + off);
     float p[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     mma_e4m3_k64(p, ag, au, bx);
@@ -363,10 +368,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     const int e = sm->idx[r];
     const int n0 = p * R.F;       // first feature
     const int nu = R.F / 8;       // [8 gate; 8 up] units
-    const uint32_t uhalf = 8u * (uint32_t)H;
+    const uint32_t uhalf = 8u * (uint32_t)H;          // bytes of 8 rows (copied)
+    const int ldu = H + kRowPad;                        // row stride in shared memory
+    const size_t ubytes = (size_t)16 * ldu;             // one [8 gate; 8 up] unit
+    const int ldd = I + kRowPad;
     const uint8_t* W13 = a.L.w13 + (size_t)e * 2 * I * H;
     const float* S13 = a.L.s13 + (size_t)e * (2 * I / kGroup) * nbh;
-    uint8_t* w2s = L.data + (size_t)2 * R.F * H;  // [128][I]
+    uint8_t* w2s = L.data + (size_t)nu * ubytes;  // [128][ldd]
     const float *lg_, *lu_, *ld_;
     int dg, du, dd;
     const uint32_t bg = span16(S13 + (size_t)(n0 / kGroup) * nbh, nbh, &lg_, &dg);
@@ -376,24 +384,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     float* sgp = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(L.wsc)) + dg;
     float* sup = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(L.wsc) + wslot) + du;
     float* sdp = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(L.wsc) + 2 * wslot) + dd;
-    // copies issued by lanes of warp 0 in parallel: lane u < nu the unit u
-    // (bar u), lane nu the scales (bar 7), lane nu + 1 the down slice (bar 6)
+    // copies, one row each, issued in parallel: warp 0 the gate/up rows of
+    // the units (bar u), warp 1 the down rows (bar 6), warp 2 the scales
+    // (bar 7); each barrier's byte count is set before its copies
     if (warp == 0) {
-      if (lane < nu) {
-        uint8_t* dst = L.data + (size_t)lane * 2 * uhalf;
-        mbar_expect(&L.bar[lane], 2 * uhalf);
-        bulk_copy(dst, W13 + (size_t)(n0 + 8 * lane) * H, uhalf, &L.bar[lane]);
-        bulk_copy(dst + uhalf, W13 + (size_t)(I + n0 + 8 * lane) * H, uhalf, &L.bar[lane]);
-      } else if (lane == nu) {
-        mbar_expect(&L.bar[7], bg + bu + bd);
-        bulk_copy(L.wsc, lg_, bg, &L.bar[7]);
-        bulk_copy(reinterpret_cast<uint8_t*>(L.wsc) + wslot, lu_, bu, &L.bar[7]);
-        bulk_copy(reinterpret_cast<uint8_t*>(L.wsc) + 2 * wslot, ld_, bd, &L.bar[7]);
-      } else if (lane == nu + 1) {
-        mbar_expect(&L.bar[6], (uint32_t)kGroup * I);
-        bulk_copy(w2s, a.L.w2 + ((size_t)e * H + (size_t)kGroup * p) * I, (uint32_t)kGroup * I,
-                  &L.bar[6]);
+      if (lane < nu) mbar_expect(&L.bar[lane], 2 * uhalf);
+      __syncwarp();
+      for (int i = lane; i < 16 * nu; i += 32) {
+        const int uu = i >> 4, j = i & 15;
+        const int n = (j < 8 ? 0 : I) + n0 + 8 * uu + (j & 7);
+        bulk_copy(L.data + (size_t)uu * ubytes + (size_t)j * ldu, W13 + (size_t)n * H,
+                  (uint32_t)H, &L.bar[uu]);
       }
+    } else if (warp == 1) {
+      if (lane == 0) mbar_expect(&L.bar[6], (uint32_t)kGroup * I);
+      __syncwarp();
+      const uint8_t* W2 = a.L.w2 + ((size_t)e * H + (size_t)kGroup * p) * I;
+      for (int m = lane; m < kGroup; m += 32)
+        bulk_copy(w2s + (size_t)m * ldd, W2 + (size_t)m * I, (uint32_t)I, &L.bar[6]);
+    } else if (warp == 2 && lane == 0) {
+      mbar_expect(&L.bar[7], bg + bu + bd);
+      bulk_copy(L.wsc, lg_, bg, &L.bar[7]);
+      bulk_copy(reinterpret_cast<uint8_t*>(L.wsc) + wslot, lu_, bu, &L.bar[7]);
+      bulk_copy(reinterpret_cast<uint8_t*>(L.wsc) + 2 * wslot, ld_, bd, &L.bar[7]);
     }
     // the routing and the slot order (experts by id) for the checking entry points
     if (warp == 0 && lane < k) {
@@ -417,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     copy_wait(&L.bar[7], 0, status);
     copy_wait(&L.bar[u], 0, status);
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    routed_part(L.data + (size_t)u * 2 * uhalf, H, sgp, sup, L.xq, L.sx, part * per,
+    routed_part(L.data + (size_t)u * ubytes, ldu, sgp, sup, L.xq, L.sx, part * per,
                 part * per + per, acc);
     float* red = L.red;  // [kW][32][2]
     red[(warp * 32 + lane) * 2 + 0] = acc[0];
@@ -456,12 +469,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     copy_wait(&L.bar[6], 0, status);
     {
       float dacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      const uint8_t* rows = w2s + (size_t)(16 * warp) * I;
+      const uint8_t* rows = w2s + (size_t)(16 * warp) * ldd;
       for (int bsl = 0; bsl < I / 64; ++bsl) {
         const int grp = bsl >> 1;
         const int off = bsl * 64 + 16 * q;
-        const uint4 a_lo = lds16(rows + (size_t)g * I + off);
-        const uint4 a_hi = lds16(rows + (size_t)(8 + g) * I + off);
+        const uint4 a_lo = lds16(rows + (size_t)g * ldd + off);
+        const uint4 a_hi = lds16(rows + (size_t)(8 + g) * ldd + off);
         const uint4 bx = lds16(L.hq + off);
         float pp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         mma_e4m3_k64(pp, a_lo, a_hi, bx);
