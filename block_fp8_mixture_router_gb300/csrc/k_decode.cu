@@ -140,12 +140,17 @@ __global__ void __launch_bounds__(256) k_route_decode(KArgs a) {
     if (i >= nv) break;
     if (128 * i + 4 * lane >= quarter) continue;
     const int kk = k0 + 128 * i + 4 * lane;
+    // every row's x for this slice in flight at once (one round trip per
+    // slice instead of one per row)
+    uint2 raw[kDecodeRows];
+#pragma unroll
+    for (int t = 0; t < kDecodeRows; ++t)
+      raw[t] = t < T ? __ldcg(reinterpret_cast<const uint2*>(a.x + (size_t)t * H + kk))
+                     : make_uint2(0u, 0u);
 #pragma unroll
     for (int t = 0; t < kDecodeRows; ++t) {
-      if (t >= T) break;
-      const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(a.x + (size_t)t * H + kk));
-      const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-      const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+      const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw[t].x);
+      const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw[t].y);
       float s = acc[t];
       s = fmaf(__low2float(p0), wv[i].x, s);
       s = fmaf(__high2float(p0), wv[i].y, s);
@@ -226,6 +231,8 @@ __global__ void __launch_bounds__(256) k_down_combine_decode(KArgs a) {
       }
       const int n_nt = ntok > 8 ? 2 : 1;
       float acc[2][4] = {};
+      // unrolled so the loads of several K slices are in flight together
+#pragma unroll 8
       for (int b = 0; b < I / 64; ++b) {
         const int kb = (b * 64) / kGroup;
         const int off = b * 64 + 16 * q;
@@ -266,6 +273,7 @@ __global__ void __launch_bounds__(256) k_down_combine_decode(KArgs a) {
       }
       const int n_nt = T > 8 ? 2 : 1;
       float acc[2][4] = {};
+#pragma unroll 8
       for (int b = 0; b < kh / 32; ++b) {
         const int off = b * 32 + 8 * q;
         const uint4 a0 = ld_stream16(r0 + off), a1 = ld_stream16(r1 + off);

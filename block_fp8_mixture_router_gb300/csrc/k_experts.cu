@@ -72,6 +72,8 @@ __device__ void gateup_routed(const KArgs& a, Smem& sm, int chunk_id, int mp) {
 
   float acc[2][2][4] = {};
   const int nblk = H / 64;
+  // unrolled so the loads of several K slices are in flight together
+#pragma unroll 4
   for (int b = warp; b < nblk; b += kWarps) {
     const int kb = (b * 64) / kGroup;
     const int off = b * 64 + 16 * q;
