@@ -45,17 +45,14 @@ __device__ int block_exscan256(int v, int* total, int* scratch /*[8]*/) {
   return base + inc - v;
 }
 
-// The last router CTA: top-k per row, then the schedule in the layout the
-// expert kernels read (slots sorted by (expert, row); one chunk per selected
-// expert, since an expert holds at most 16 rows here).
+// The schedule in the layout the expert kernels read (slots sorted by
+// (expert, row); one chunk per selected expert, since an expert holds at
+// most 16 rows here), from every row's top-k in a.w.idx.
 __device__ void decode_schedule(const KArgs& a) {
   __shared__ int s_idx[kDecodeRows * kMaxTopK];
   __shared__ uint32_t s_tok[kMaxExperts];
   __shared__ int s_scan[8];
   const int T = a.d.T, k = a.d.k, E = a.d.E;
-  const int warp = threadIdx.x >> 5;
-  for (int t = warp; t < T; t += 8)
-    topk_row(a.w.logits + (size_t)t * E, E, k, a.w.idx + (size_t)t * k, a.w.wts + (size_t)t * k);
   for (int e = threadIdx.x; e < kMaxExperts; e += blockDim.x) s_tok[e] = 0u;
   __threadfence_block();
   __syncthreads();
@@ -90,14 +87,25 @@ __device__ void decode_schedule(const KArgs& a) {
 
 }  // namespace
 
+constexpr long long kRouteSpin = 1ll << 22;  // tries before the logit wait gives up
+
 // ---- D1: router logits, x quantisation, top-k, schedule ---------------------
 // CTAs [0, n_router): two experts each; warp w covers expert 2b + w/4 over the
-// K quarter w%4.  CTAs [n_router, n_router + T): one row's quantisation and
-// shared gate.  The last router CTA to finish builds the schedule.
+// K quarter w%4; each counts itself done (done[0]) once its logits are out.
+// CTAs [n_router, n_router + T): row t's quantisation and shared gate, then,
+// once every router CTA is done (a bounded wait: all CTAs of this grid are
+// resident together), row t's top-k with the whole CTA; the last of them
+// (done[1]) builds the schedule and resets both counters.
 __global__ void __launch_bounds__(256) k_route_decode(KArgs a) {
   __shared__ float red[8][kDecodeRows];
   __shared__ int s_last;
-  const int T = a.d.T, H = a.d.H, E = a.d.E;
+  // the top-k reads these as 16-byte vectors
+  __shared__ __align__(16) float s_lg[kMaxExperts];
+  __shared__ __align__(16) uint32_t s_ck[2 * 8 * kMaxTopK];
+  __shared__ __align__(16) uint32_t s_cid[2 * 8 * kMaxTopK];
+  __shared__ int s_idx1[kMaxTopK];
+  __shared__ float s_w1[kMaxTopK];
+  const int T = a.d.T, H = a.d.H, E = a.d.E, k = a.d.k;
   const int n_router = (E + 1) / 2;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
@@ -110,7 +118,42 @@ __global__ void __launch_bounds__(256) k_route_decode(KArgs a) {
   if (blockIdx.x >= n_router) {
     pdl_wait();
     pdl_trigger();
-    quant_row_and_gate(a, blockIdx.x - n_router);
+    const int t = blockIdx.x - n_router;
+    quant_row_and_gate(a, t);
+    if (threadIdx.x == 0) {
+      long long it = 0;
+      for (;;) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(a.w.done) : "memory");
+        if (v >= n_router) break;
+        if (++it > kRouteSpin) {
+          atomicExch(a.w.status, 1);
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_lg[e] = __ldcg(a.w.logits + (size_t)t * E + e);
+    __syncthreads();
+    topk_one_row<8>(s_lg, E, k, s_ck, s_cid, s_idx1, s_w1);
+    __syncthreads();
+    if (threadIdx.x < k) {
+      a.w.idx[(size_t)t * k + threadIdx.x] = s_idx1[threadIdx.x];
+      a.w.wts[(size_t)t * k + threadIdx.x] = s_w1[threadIdx.x];
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&a.w.done[1], 1) == T - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    decode_schedule(a);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      a.w.done[0] = 0;
+      a.w.done[1] = 0;
+    }
     return;
   }
 
@@ -176,15 +219,7 @@ __global__ void __launch_bounds__(256) k_route_decode(KArgs a) {
   }
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const int old = atomicAdd(&a.w.done[0], 1);
-    s_last = old == n_router - 1;
-    if (s_last) a.w.done[0] = 0;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  decode_schedule(a);
+  if (threadIdx.x == 0) atomicAdd(&a.w.done[0], 1);
 }
 
 cudaError_t launch_route_decode(const KArgs& a, bool pdl, cudaStream_t s) {

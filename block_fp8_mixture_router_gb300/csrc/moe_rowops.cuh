@@ -112,6 +112,8 @@ __device__ __forceinline__ void topk_row(const float* logits, int E, int k, int*
 // scratch of 2*kWarps*16 entries each; idx_out / w_out (shared memory)
 // receive the experts in rank order and their softmax weights.  The caller
 // synchronises the CTA afterwards.
+// lg, cand_key and cand_id must be 16-byte aligned (they are read as
+// vectors).
 // Fast variant for k <= 8 and a multiple of four warps: every thread ranks
 // its own expert among its warp's 32 (counting the keys that beat it, read
 // from shared memory as broadcast vectors, no serial rounds); the k best of
