@@ -534,13 +534,22 @@ __global__ void __launch_bounds__(256) k_quant_scatter(KArgs a, uint8_t* xg, flo
   __syncthreads();
   const bf16* xr = a.x + (size_t)t * H;
   const int ngroups = H / kGroup;
+  // the shared gate's dot product from the same registers as the codes
+  float acc = 0.0f;
   for (int gi = warp; gi < ngroups; gi += 8) {
     const int base = gi * kGroup + 4 * lane;
     const uint2 raw = *reinterpret_cast<const uint2*>(xr + base);
+    const uint2 graw = *reinterpret_cast<const uint2*>(a.L.gate + base);
     const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
     const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+    const __nv_bfloat162 g0 = *reinterpret_cast<const __nv_bfloat162*>(&graw.x);
+    const __nv_bfloat162 g1 = *reinterpret_cast<const __nv_bfloat162*>(&graw.y);
     const float v0 = __low2float(p0), v1 = __high2float(p0), v2 = __low2float(p1),
                 v3 = __high2float(p1);
+    acc = fmaf(v0, __low2float(g0), acc);
+    acc = fmaf(v1, __high2float(g0), acc);
+    acc = fmaf(v2, __low2float(g1), acc);
+    acc = fmaf(v3, __high2float(g1), acc);
     float m = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
     m = warp_max(m);
     const float s = group_scale(m);
@@ -550,9 +559,6 @@ __global__ void __launch_bounds__(256) k_quant_scatter(KArgs a, uint8_t* xg, flo
       if (lane == 0) sxg[(size_t)slots[j] * ngroups + gi] = s;
     }
   }
-  float acc = 0.0f;
-  for (int i = threadIdx.x; i < H; i += 256)
-    acc = fmaf(__bfloat162float(xr[i]), __bfloat162float(a.L.gate[i]), acc);
   acc = warp_sum(acc);
   if (lane == 0) red[warp] = acc;
   __syncthreads();

@@ -130,14 +130,13 @@ cudaError_t launch_topk_splits(const KArgs& a, const float* part, int ks, cudaSt
 // ---- schedule: stable slots sorted by (expert, row), and expert chunks ----
 // A pair p = t*k + j routes row t to expert e = idx[p].  Rows pick distinct
 // experts, so an expert's slots in row order are its rank among the rows
-// that chose it.  Two kernels, each one CTA per block of 256 rows:
+// that chose it.  Two kernels, each one CTA per block of kSchedRows rows:
 //   count:  a bitmap of the block's rows per expert gives every pair its rank
 //           within the block and each expert's count in the block;
 //   finish: slot = (rows of all experts before e) + (rows of e in earlier
 //           blocks) + (rank in the block).  Block 0 also writes the per-expert
 //           counts, offsets and the chunk list of the warp-MMA kernels.
 // Nothing depends on timing: every sum has a fixed order.
-constexpr int kSchedRows = 256;  // rows per block (8 bitmap words)
 
 __global__ void __launch_bounds__(256) k_sched_count(KArgs a, int* __restrict__ rank,
                                                      int* __restrict__ blk_cnt) {
@@ -182,7 +181,10 @@ __global__ void __launch_bounds__(256) k_sched_finish(KArgs a, const int* __rest
   pdl_trigger();
   if (tid < E) {
     int pre = 0, rest = 0;
+    // unrolled so the blocks' counts are loaded several at a time
+#pragma unroll 8
     for (int bb = 0; bb < b; ++bb) pre += __ldg(blk_cnt + (size_t)bb * E + tid);
+#pragma unroll 8
     for (int bb = b; bb < nb; ++bb) rest += __ldg(blk_cnt + (size_t)bb * E + tid);
     s_pre[tid] = pre;
     tot = pre + rest;

@@ -150,7 +150,7 @@ Plan make_plan(const moe_config* c) {
   p.add(((E + 127) / 128) * 128 * 3 * H * 2);  // 35 router3
   p.add(router_part_rows(c) * E * 4);     // 36 router partial logits
   p.add(T * k * 4);                       // 37 schedule: rank in block
-  p.add(((T + 255) / 256) * E * 4);       // 38 schedule: rows per expert per block
+  p.add(((T + kSchedRows - 1) / kSchedRows) * E * 4);  // 38 schedule: rows per expert per block
   p.add(kDecodeRows * (k * I + k * H + Is + H) * 8);  // 39 decode exchange words
   return p;
 }

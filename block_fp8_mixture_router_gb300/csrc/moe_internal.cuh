@@ -17,6 +17,7 @@ typedef __nv_bfloat16 bf16;
 
 constexpr int kGroup = 128;       // activation group = weight block edge
 constexpr int kChunk = 16;        // tokens per expert chunk (two n8 MMA tiles)
+constexpr int kSchedRows = 128;   // rows per block of the prompt schedule (4 bitmap words)
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 16;
 constexpr int kDecodeRows = 16;   // rows at or below which the decode kernels run

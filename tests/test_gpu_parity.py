@@ -176,6 +176,23 @@ def test_decode_t1_repeated_launches_bitwise(full_case):
     assert full_case.moe.device_status() == m.MOE_OK
 
 
+@pytest.mark.parametrize("rows", [1, 3, 11, 64])
+def test_plain_launches_match_chained(full_case, rows):
+    """With programmatic dependent launch off (MOE_OPT_PDL = 0) every path
+    gives bit-identical outputs to the chained launches, and matches the
+    oracle."""
+    x = full_case.x(rows, tag=f"pdl{rows}")
+    y_on = full_case.moe.forward(x).clone()
+    full_case.moe.set_option(m.MOE_OPT_PDL, 0)
+    try:
+        y_off = full_case.moe.forward(x).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(y_on, y_off)
+        run_and_check(full_case, x, sample_rows=[0, rows - 1])
+    finally:
+        full_case.moe.set_option(m.MOE_OPT_PDL, 1)
+
+
 @pytest.fixture(scope="module")
 def tie_layer(dev):
     """A full-width layer whose router repeats rows: experts 100 and 200 copy
