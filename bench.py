@@ -426,10 +426,12 @@ def run_ours(args):
         stage_avg = {n: ms / K / layers_per_step for n in stage_avg}
         duration_source = "CUDA events over the timed region (one launch per layer forward)"
 
-    # touched experts per instance
+    # touched experts per layer instance; in the sweep each layer's input is
+    # the previous layer's output (ys[j - 1] after the timed steps)
     Us = []
-    for j in range(1 if sweep else L):
-        idx, _ = nets[j].route(xs[j], stream=stream)
+    for j in range(L):
+        src = (xs[0] if j == 0 else ys[j - 1]) if sweep else xs[j]
+        idx, _ = nets[j].route(src, stream=stream)
         stream.synchronize()
         Us.append(len(set(idx.cpu().numpy().ravel().tolist())))
     U = sum(Us) / len(Us)
