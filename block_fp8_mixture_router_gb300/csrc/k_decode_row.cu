@@ -44,7 +44,7 @@ namespace {
 
 using namespace dec;
 
-constexpr int kW = 8;
+constexpr int kW = 16;  // warps per CTA: more warps hide more of each phase's latency
 constexpr int kThreads = 32 * kW;
 constexpr int kSguSlots = 3;      // ring slots of a shared gate/up CTA (one unit each)
 constexpr int kSdnSlots = 6;      // ring slots of a shared down CTA
@@ -110,7 +110,7 @@ struct Lay {
   float* hall;    // [max(I, Is)] exchanged SwiGLU values
   uint8_t* hq;    // [I] their e4m3 codes (routed)
   float* sh;      // [I/128] their scales
-  float* red;     // [kW][2][32][4] scratch
+  float* red;     // [kW][32][2] scratch
   float* lg;      // [E]
   uint64_t* bar;  // [8]
   Small* sm;
@@ -121,7 +121,7 @@ __host__ __device__ inline size_t small_bytes(int H, int E, int I, int Is) {
   const int M = I > Is ? I : Is;
   return al16(H) + al16((size_t)H * 2) + al16((size_t)nbh * 4) + 3 * al16((size_t)(nbh + 8) * 4) +
          al16((size_t)M * 4) + al16(I) + al16((size_t)(I / kGroup) * 4) +
-         (size_t)kW * 2 * 32 * 4 * 4 + al16((size_t)E * 4) + 8 * 8 + al16(sizeof(Small));
+         (size_t)kW * 32 * 2 * 4 + al16((size_t)E * 4) + 8 * 8 + al16(sizeof(Small));
 }
 
 __device__ inline Lay make_lay(uint8_t* smem, const Roles& r, int H, int E, int I, int Is) {
@@ -146,7 +146,7 @@ __device__ inline Lay make_lay(uint8_t* smem, const Roles& r, int H, int E, int 
   L.sh = reinterpret_cast<float*>(p);
   p += al16((size_t)(I / kGroup) * 4);
   L.red = reinterpret_cast<float*>(p);
-  p += (size_t)kW * 2 * 32 * 4 * 4;
+  p += (size_t)kW * 32 * 2 * 4;
   L.lg = reinterpret_cast<float*>(p);
   p += al16((size_t)E * 4);
   L.bar = reinterpret_cast<uint64_t*>(p);
@@ -259,10 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
       }
     }
   }
-  // router rows: experts b and b + G; each warp covers an eighth of K of both
-  const int keighth = H / 8;
+  // router rows: experts b and b + G; each warp covers a 1/kW share of K of both
+  const int keighth = H / kW;
   const int k0 = warp * keighth;
-  constexpr int kMaxV = kMaxRowH / 8 / 128;
+  constexpr int kMaxV = kMaxRowH / kW / 128 > 0 ? kMaxRowH / kW / 128 : 1;
   const int nv = keighth / 128;
   float4 wv[2][kMaxV];
   uint2 gw[kMaxV];
@@ -363,7 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     for (int e = threadIdx.x; e < E; e += kThreads)
       L.lg[e] = poll_tagged(a.w.tlog + e, tag, status);
     __syncthreads();
-    topk_one_row<kW>(L.lg, E, k, sm->cand_key, sm->cand_id, sm->idx, sm->w);
+    // the top-k on the first 8 warps (the others wait at the barrier below)
+    if (k <= 8 && E <= 256) {
+      if (warp < 8) topk_one_row_fast<8>(L.lg, E, k, sm->cand_key, sm->cand_id, sm->idx, sm->w);
+    } else {
+      topk_one_row<kW>(L.lg, E, k, sm->cand_key, sm->cand_id, sm->idx, sm->w);
+    }
     __syncthreads();
     const int e = sm->idx[r];
     const int n0 = p * R.F;       // first feature
@@ -468,9 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     // down rows [128p + 16w, +16) of expert e over the full I
     copy_wait(&L.bar[6], 0, status);
     {
+      // 128 rows = 8 m-tiles: warp w takes m-tile w % 8 over K half w / 8;
+      // the second half's sums are added through shared memory
+      constexpr int kMT = kGroup / 16;
+      const int mt = warp % kMT, kh = warp / kMT, nkh = kW / kMT;
+      const int per_h = (I / 64) / nkh;
       float dacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      const uint8_t* rows = w2s + (size_t)(16 * warp) * ldd;
-      for (int bsl = 0; bsl < I / 64; ++bsl) {
+      const uint8_t* rows = w2s + (size_t)(16 * mt) * ldd;
+      for (int bsl = kh * per_h; bsl < kh * per_h + per_h; ++bsl) {
         const int grp = bsl >> 1;
         const int off = bsl * 64 + 16 * q;
         const uint4 a_lo = lds16(rows + (size_t)g * ldd + off);
@@ -482,10 +492,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
         dacc[0] = fmaf(pp[0], s, dacc[0]);
         dacc[2] = fmaf(pp[2], s, dacc[2]);
       }
-      if (q == 0) {
-        const int m = kGroup * p + 16 * warp + g;
-        publish(X.d + (size_t)r * H + m, tag, bf16_round(dacc[0]));
-        publish(X.d + (size_t)r * H + m + 8, tag, bf16_round(dacc[2]));
+      float* dred = L.red;  // [kW][32][2]
+      dred[(warp * 32 + lane) * 2 + 0] = dacc[0];
+      dred[(warp * 32 + lane) * 2 + 1] = dacc[2];
+      __syncthreads();
+      if (kh == 0 && q == 0) {
+        float d0 = 0.0f, d1 = 0.0f;
+        for (int hh = 0; hh < nkh; ++hh) {  // K halves in order
+          const int w = hh * kMT + mt;
+          d0 += dred[(w * 32 + lane) * 2 + 0];
+          d1 += dred[(w * 32 + lane) * 2 + 1];
+        }
+        const int m = kGroup * p + 16 * mt + g;
+        publish(X.d + (size_t)r * H + m, tag, bf16_round(d0));
+        publish(X.d + (size_t)r * H + m + 8, tag, bf16_round(d1));
       }
     }
     // combine rows [128p + (128/k) r, +128/k): sum_j w_j d_j + gamma ds
@@ -598,11 +618,12 @@ size_t decode_row_smem(int G, int H, int E, int k, int I, int Is) {
 // Whether the one-row kernel covers this shape on G CTAs within `budget`
 // bytes of shared memory per CTA.
 bool decode_row_fits(int G, int H, int E, int k, int I, int Is, size_t budget) {
-  if (H % 1024 != 0 || H > kMaxRowH) return false;
+  if (H % (kW * 128) != 0 || H > kMaxRowH) return false;
   if (E > 2 * G || E > 32 * kW || k > kMaxTopK || kGroup % k != 0 || kGroup / k > 16) return false;
   const Roles R = make_roles(G, H, k, I, Is);
   if (R.nS2 < 1 || I % R.P != 0 || Is % R.P != 0) return false;
   if (R.F < 8 || R.F % 8 != 0 || kGroup % R.F != 0 || kW % (R.F / 8) != 0) return false;
+  if (kW % (kGroup / 16) != 0 || (I / 64) % (kW / (kGroup / 16)) != 0) return false;
   if ((H / 64) % (kW / (R.F / 8)) != 0) return false;
   if (R.Fs < 8 || R.Fs % 8 != 0 || (H / 32) % kW != 0) return false;
   if (R.R2 % kSdnUnit != 0 || (size_t)R.R2 * R.nS2 < (size_t)H) return false;

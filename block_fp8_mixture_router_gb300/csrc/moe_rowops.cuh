@@ -112,8 +112,15 @@ __device__ __forceinline__ void topk_row(const float* logits, int E, int k, int*
 // scratch of 2*kWarps*16 entries each; idx_out / w_out (shared memory)
 // receive the experts in rank order and their softmax weights.  The caller
 // synchronises the CTA afterwards.
+// Barrier of the first kWarps warps of the CTA (named barrier 2): the fast
+// top-k below synchronises only the warps that run it.
+template <int kWarps>
+__device__ __forceinline__ void topk_bar() {
+  asm volatile("bar.sync 2, %0;\n" ::"n"(32 * kWarps) : "memory");
+}
+
 // lg, cand_key and cand_id must be 16-byte aligned (they are read as
-// vectors).
+// vectors).  Run by the first kWarps warps of the CTA (all of them call it).
 // Fast variant for k <= 8 and a multiple of four warps: every thread ranks
 // its own expert among its warp's 32 (counting the keys that beat it, read
 // from shared memory as broadcast vectors, no serial rounds); the k best of
@@ -154,7 +161,7 @@ __device__ void topk_one_row_fast(const float* lg, int E, int k, uint32_t* cand_
       cand_id[warp * 8 + r] = (uint32_t)e;
     }
   }
-  __syncthreads();
+  topk_bar<kWarps>();
   uint32_t* rank_key = cand_key + 8 * kWarps;
   uint32_t* rank_id = cand_id + 8 * kWarps;
   {
@@ -187,7 +194,7 @@ __device__ void topk_one_row_fast(const float* lg, int E, int k, uint32_t* cand_
       rank_id[rank] = D;
     }
   }
-  __syncthreads();
+  topk_bar<kWarps>();
   if (warp == 0) {
     const uint32_t my_key = lane < k ? rank_key[lane] : 0u;
     const float top = key_value(__shfl_sync(0xffffffffu, my_key, 0));
