@@ -232,7 +232,11 @@ cudaError_t launch_route_decode(const KArgs& a, bool pdl, cudaStream_t s) {
 // 16 x I slice of the down weights against those rows' re-quantised SwiGLU
 // codes) and the shared expert's slice in two K halves.  Items go to warps
 // round-robin, each covering its full K, so no cross-warp reduction is needed.
-__global__ void __launch_bounds__(256) k_down_combine_decode(KArgs a) {
+// 16 warps: every item is a chain of dependent loads, so the more items run
+// side by side in a CTA the more of that latency is hidden.
+constexpr int kDcWarps = 16;
+
+__global__ void __launch_bounds__(32 * kDcWarps) k_down_combine_decode(KArgs a) {
   __shared__ float s_d[kDecodeRows * kMaxTopK][16];
   __shared__ float s_ds[2][kDecodeRows][16];
   const int T = a.d.T, H = a.d.H, I = a.d.I, Is = a.d.Is, k = a.d.k;
@@ -242,7 +246,7 @@ __global__ void __launch_bounds__(256) k_down_combine_decode(KArgs a) {
   pdl_wait();
   pdl_trigger();
   const int U = *a.w.n_chunks;
-  for (int it = warp; it < U + 2; it += 8) {
+  for (int it = warp; it < U + 2; it += kDcWarps) {
     if (it < U) {
       const int4 ch = a.w.chunks[it];
       const int e = ch.x, s0 = ch.y, ntok = ch.z;
@@ -342,7 +346,7 @@ __global__ void __launch_bounds__(256) k_down_combine_decode(KArgs a) {
 }
 
 cudaError_t launch_down_combine_decode(const KArgs& a, bool pdl, cudaStream_t s) {
-  return launch_pdl(k_down_combine_decode, dim3(a.d.H / 16), dim3(256), 0, s, pdl, a);
+  return launch_pdl(k_down_combine_decode, dim3(a.d.H / 16), dim3(32 * kDcWarps), 0, s, pdl, a);
 }
 
 }  // namespace moe
