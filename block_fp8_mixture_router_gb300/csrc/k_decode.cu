@@ -24,9 +24,10 @@ namespace moe {
 
 namespace {
 
-// Block-wide exclusive prefix sum over 256 threads (one value each).
-__device__ int block_exscan256(int v, int* total, int* scratch /*[8]*/) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Block-wide exclusive prefix sum over the CTA's threads (one value each,
+// up to 32 warps).
+__device__ int block_exscan(int v, int* total, int* scratch /*[32]*/) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int inc = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -36,7 +37,7 @@ __device__ int block_exscan256(int v, int* total, int* scratch /*[8]*/) {
   if (lane == 31) scratch[warp] = inc;
   __syncthreads();
   int base = 0, all = 0;
-  for (int w = 0; w < 8; ++w) {
+  for (int w = 0; w < nw; ++w) {
     if (w < warp) base += scratch[w];
     all += scratch[w];
   }
@@ -51,7 +52,7 @@ __device__ int block_exscan256(int v, int* total, int* scratch /*[8]*/) {
 __device__ void decode_schedule(const KArgs& a) {
   __shared__ int s_idx[kDecodeRows * kMaxTopK];
   __shared__ uint32_t s_tok[kMaxExperts];
-  __shared__ int s_scan[8];
+  __shared__ int s_scan[32];
   const int T = a.d.T, k = a.d.k, E = a.d.E;
   for (int e = threadIdx.x; e < kMaxExperts; e += blockDim.x) s_tok[e] = 0u;
   __threadfence_block();
@@ -66,8 +67,8 @@ __device__ void decode_schedule(const KArgs& a) {
   const uint32_t mask = e < E ? s_tok[e] : 0u;
   const int cnt = __popc(mask);
   int n_slots, n_used;
-  const int slot0 = block_exscan256(cnt, &n_slots, s_scan);
-  const int u = block_exscan256(cnt > 0 ? 1 : 0, &n_used, s_scan);
+  const int slot0 = block_exscan(cnt, &n_slots, s_scan);
+  const int u = block_exscan(cnt > 0 ? 1 : 0, &n_used, s_scan);
   if (cnt > 0) {
     a.w.chunks[u] = make_int4(e, slot0, cnt, 0);
     uint32_t m = mask;
@@ -96,13 +97,15 @@ constexpr long long kRouteSpin = 1ll << 22;  // tries before the logit wait give
 // once every router CTA is done (a bounded wait: all CTAs of this grid are
 // resident together), row t's top-k with the whole CTA; the last of them
 // (done[1]) builds the schedule and resets both counters.
-__global__ void __launch_bounds__(256) k_route_decode(KArgs a) {
-  __shared__ float red[8][kDecodeRows];
+constexpr int kRtWarps = 16;  // warps per router CTA: K in eighths of two experts
+
+__global__ void __launch_bounds__(32 * kRtWarps) k_route_decode(KArgs a) {
+  __shared__ float red[kRtWarps][kDecodeRows];
   __shared__ int s_last;
   // the top-k reads these as 16-byte vectors
   __shared__ __align__(16) float s_lg[kMaxExperts];
-  __shared__ __align__(16) uint32_t s_ck[2 * 8 * kMaxTopK];
-  __shared__ __align__(16) uint32_t s_cid[2 * 8 * kMaxTopK];
+  __shared__ __align__(16) uint32_t s_ck[2 * kRtWarps * kMaxTopK];
+  __shared__ __align__(16) uint32_t s_cid[2 * kRtWarps * kMaxTopK];
   __shared__ int s_idx1[kMaxTopK];
   __shared__ float s_w1[kMaxTopK];
   const int T = a.d.T, H = a.d.H, E = a.d.E, k = a.d.k;
@@ -136,7 +139,12 @@ __global__ void __launch_bounds__(256) k_route_decode(KArgs a) {
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_lg[e] = __ldcg(a.w.logits + (size_t)t * E + e);
     __syncthreads();
-    topk_one_row<8>(s_lg, E, k, s_ck, s_cid, s_idx1, s_w1);
+    // the top-k on the first 8 warps (named barrier), the rest wait below
+    if (k <= 8 && E <= 256) {
+      if (warp < 8) topk_one_row_fast<8>(s_lg, E, k, s_ck, s_cid, s_idx1, s_w1);
+    } else {
+      topk_one_row<kRtWarps>(s_lg, E, k, s_ck, s_cid, s_idx1, s_w1);
+    }
     __syncthreads();
     if (threadIdx.x < k) {
       a.w.idx[(size_t)t * k + threadIdx.x] = s_idx1[threadIdx.x];
@@ -157,9 +165,10 @@ __global__ void __launch_bounds__(256) k_route_decode(KArgs a) {
     return;
   }
 
-  const int e = 2 * blockIdx.x + (warp >> 2);
-  const int quarter = H / 4;
-  const int k0 = (warp & 3) * quarter;
+  constexpr int kParts = kRtWarps / 2;  // K parts per expert
+  const int e = 2 * blockIdx.x + warp / kParts;
+  const int quarter = H / kParts;
+  const int k0 = (warp % kParts) * quarter;
   const bool valid = e < E;
   const float* wrow = a.L.wr + (size_t)(valid ? e : 0) * H + k0;
   // router rows do not depend on the previous kernel: load before waiting
@@ -213,7 +222,8 @@ __global__ void __launch_bounds__(256) k_route_decode(KArgs a) {
     const int h = threadIdx.x / T, t = threadIdx.x % T;
     const int ee = 2 * blockIdx.x + h;
     if (ee < E) {
-      const float v = ((red[4 * h][t] + red[4 * h + 1][t]) + red[4 * h + 2][t]) + red[4 * h + 3][t];
+      float v = 0.0f;
+      for (int pp = 0; pp < kParts; ++pp) v += red[kParts * h + pp][t];  // K parts in order
       a.w.logits[(size_t)t * E + ee] = v;
     }
   }
@@ -224,7 +234,7 @@ __global__ void __launch_bounds__(256) k_route_decode(KArgs a) {
 
 cudaError_t launch_route_decode(const KArgs& a, bool pdl, cudaStream_t s) {
   const int grid = (a.d.E + 1) / 2 + a.d.T;
-  return launch_pdl(k_route_decode, dim3(grid), dim3(256), 0, s, pdl, a);
+  return launch_pdl(k_route_decode, dim3(grid), dim3(32 * kRtWarps), 0, s, pdl, a);
 }
 
 // ---- D3: down projections + combine -----------------------------------------

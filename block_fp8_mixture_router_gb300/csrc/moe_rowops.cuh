@@ -9,16 +9,17 @@
 namespace moe {
 
 // ---- activation quantisation (1 x 128 groups) and the shared gate ----------
-// One 256-thread CTA per row.  Warp w quantises groups w, w+8, ...; each lane holds 4
-// consecutive values of the group.  The gate dot product x . g is reduced in a
-// fixed order (per-thread strided sums, then warps 0..7).
+// One CTA per row (any multiple of 32 threads up to 1024).  Warp w quantises
+// groups w, w + nw, ...; each lane holds 4 consecutive values of the group.
+// The gate dot product x . g is reduced in a fixed order (per-thread strided
+// sums, then warps 0..nw-1).
 __device__ __forceinline__ void quant_row_and_gate(const KArgs& a, int t) {
-  __shared__ float red[8];
+  __shared__ float red[32];
   const int H = a.d.H;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const bf16* xr = a.x + (size_t)t * H;
   const int ngroups = H / kGroup;
-  for (int gi = warp; gi < ngroups; gi += 8) {
+  for (int gi = warp; gi < ngroups; gi += nw) {
     const int base = gi * kGroup + 4 * lane;
     uint2 raw = *reinterpret_cast<const uint2*>(xr + base);
     __nv_bfloat162 p0 = *reinterpret_cast<__nv_bfloat162*>(&raw.x);
@@ -32,14 +33,14 @@ __device__ __forceinline__ void quant_row_and_gate(const KArgs& a, int t) {
     if (lane == 0) a.w.sx[(size_t)t * ngroups + gi] = s;
   }
   float acc = 0.0f;
-  for (int i = threadIdx.x; i < H; i += 256)
+  for (int i = threadIdx.x; i < H; i += blockDim.x)
     acc = fmaf(__bfloat162float(xr[i]), __bfloat162float(a.L.gate[i]), acc);
   acc = warp_sum(acc);
   if (lane == 0) red[warp] = acc;
   __syncthreads();
   if (threadIdx.x == 0) {
     float v = 0.0f;
-    for (int w = 0; w < 8; ++w) v += red[w];
+    for (int w = 0; w < nw; ++w) v += red[w];
     a.w.gamma[t] = sigmoid_f32(v);
   }
 }
