@@ -1,0 +1,51 @@
+"""The algorithmic work bench.py divides by, against the closed forms of the
+layer (no GPU).
+
+Per touched expert: 2I*H + H*I bytes of e4m3 weights plus fp32 128x128 block
+scales.  Per layer: the fp32 router [E, H], the bf16 shared expert
+[2Is, H] + [H, Is], the bf16 gate vector [H], and bf16 x and y.  FP8 flops:
+2 * T * k * (2I*H + H*I).
+"""
+from __future__ import annotations
+
+import bench
+import workloads as W
+
+
+def test_one_row_layer_bytes():
+    s = W.FULL
+    per_expert = 3 * 512 * 2048 + 4 * (8 * 16 + 16 * 4)
+    assert per_expert == 3_146_496
+    fixed = 4 * 256 * 2048 + 2 * 3 * 512 * 2048 + 2 * 2048
+    assert bench.layer_bytes(s, 1, 8) == 8 * per_expert + fixed + 2 * 2 * 2048
+    assert bench.layer_bytes(s, 1, 8) == 33_572_864
+
+
+def test_layer_bytes_grow_with_rows_and_experts():
+    s = W.FULL
+    base = bench.layer_bytes(s, 11, 29)
+    assert bench.layer_bytes(s, 12, 29) - base == 2 * 2 * 2048       # x and y of one row
+    assert bench.layer_bytes(s, 11, 30) - base == 3_146_496          # one more expert
+
+
+def test_fp8_flops():
+    s = W.FULL
+    assert bench.fp8_flops(s, 1) == 2 * 8 * (2 * 512 * 2048 + 2048 * 512)
+    assert bench.fp8_flops(s, 1024) == 1024 * bench.fp8_flops(s, 1)
+
+
+def test_stage_bytes_cover_every_timed_stage():
+    """Every stage name a forward can report has a byte count."""
+    s = W.FULL
+    sb = bench.stage_bytes(s, 1024, 173.3)
+    for name in ("decode_row", "decode_rows", "decode_layer", "route_decode", "gateup_decode",
+                 "down_combine_decode", "router_tc", "topk", "schedule", "quant_scatter",
+                 "shared_gateup_tc", "gateup_tc", "shared_down_tc", "down_tc", "combine"):
+        assert name in sb and sb[name] > 0, name
+    # the whole-layer kernels move the layer's bytes
+    assert sb["decode_row"] == bench.layer_bytes(s, 1024, 173.3)
+
+
+def test_rows_per_second_is_whole_job():
+    assert bench.rows_per_second(1, 100, 11, 0.5) == 100 * 11 / 0.5
+    assert bench.rows_per_second(4, 100, 11, 0.5) == 4 * 100 * 11 / 0.5
