@@ -848,14 +848,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_rows(KArgs a) {
   }
 
   // ---- exit: the last CTA advances the launch tag ----
+  // No fence is needed: the next launch reads the tag, the outputs and the
+  // exchange words only after this grid has completed, and stale exchange
+  // words carry an older tag.
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
     const int old = atomicAdd(bar_exit, 1);
     if (old == G - 1) {
       *bar_exit = 0;
       *epoch = sm->tag;
-      __threadfence();
     }
   }
 }
