@@ -27,8 +27,12 @@ namespace {
 
 constexpr int kWarps = 8;
 
+constexpr int kMaxNbh = 4096 / kGroup;  // 128-wide K groups of H at most
+
 struct __align__(16) Smem {
   float red[kWarps][2][2][4][32];  // [warp][tile][n-tile][c][lane]
+  float sxs[kChunk][kMaxNbh];      // a routed unit's token scales [row][K group]
+  float swg[kMaxNbh], swu[kMaxNbh];  // its gate and up weight-block scales
   int flag;
 };
 
@@ -55,19 +59,38 @@ __device__ void gateup_routed(const KArgs& a, Smem& sm, int chunk_id, int mp) {
 
   const uint8_t* xb[2];
   bool bval[2];
-  const float* sxc[2][2];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
     int tb = 8 * nt + g;
     bval[nt] = tb < ntok;
     int t = bval[nt] ? a.w.pair_of_slot[s0 + tb] / k : 0;
     xb[nt] = a.w.xq + (size_t)t * H;
+  }
+  // the unit's scales into shared memory once (coalesced), instead of
+  // scattered loads inside the K loop; hidden sizes beyond kMaxNbh groups
+  // keep the direct loads
+  const bool staged = nbh <= kMaxNbh;
+  const float* sxc[2][2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
-      int tc = 8 * nt + 2 * q + c;
-      sxc[nt][c] = tc < ntok ? a.w.sx + (size_t)(a.w.pair_of_slot[s0 + tc] / k) * nbh : nullptr;
+      const int tc = 8 * nt + 2 * q + c;
+      sxc[nt][c] = !staged && tc < ntok
+                       ? a.w.sx + (size_t)(a.w.pair_of_slot[s0 + tc] / k) * nbh
+                       : nullptr;
+    }
+  if (staged) {
+    for (int i = threadIdx.x; i < ntok * nbh; i += blockDim.x) {
+      const int tok = i / nbh, kbb = i - tok * nbh;
+      sm.sxs[tok][kbb] = __ldcg(a.w.sx + (size_t)(a.w.pair_of_slot[s0 + tok] / k) * nbh + kbb);
+    }
+    for (int i = threadIdx.x; i < nbh; i += blockDim.x) {
+      sm.swg[i] = __ldg(Sg + i);
+      sm.swu[i] = __ldg(Su + i);
     }
   }
+  __syncthreads();
   const int n_nt = ntok > 8 ? 2 : 1;
 
   float acc[2][2][4] = {};
@@ -79,13 +102,21 @@ __device__ void gateup_routed(const KArgs& a, Smem& sm, int chunk_id, int mp) {
     const int off = b * 64 + 16 * q;
     const uint4 ag0 = ld_stream16(rg0 + off), au0 = ld_stream16(ru0 + off);
     const uint4 ag1 = ld_stream16(rg1 + off), au1 = ld_stream16(ru1 + off);
-    const float sg = __ldg(Sg + kb), su = __ldg(Su + kb);
+    const float sg = staged ? sm.swg[kb] : __ldg(Sg + kb);
+    const float su = staged ? sm.swu[kb] : __ldg(Su + kb);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       if (nt >= n_nt) break;
       const uint4 bx = bval[nt] ? ld_cg16(xb[nt] + off) : make_uint4(0u, 0u, 0u, 0u);
-      const float sa = sxc[nt][0] ? __ldcg(sxc[nt][0] + kb) : 0.0f;
-      const float sb = sxc[nt][1] ? __ldcg(sxc[nt][1] + kb) : 0.0f;
+      const int tc0 = 8 * nt + 2 * q;
+      float sa, sb;
+      if (staged) {
+        sa = tc0 < ntok ? sm.sxs[tc0][kb] : 0.0f;
+        sb = tc0 + 1 < ntok ? sm.sxs[tc0 + 1][kb] : 0.0f;
+      } else {
+        sa = sxc[nt][0] ? __ldcg(sxc[nt][0] + kb) : 0.0f;
+        sb = sxc[nt][1] ? __ldcg(sxc[nt][1] + kb) : 0.0f;
+      }
       float p0[4] = {}, p1[4] = {};
       mma_e4m3_k64(p0, ag0, au0, bx);
       mma_e4m3_k64(p1, ag1, au1, bx);
