@@ -34,6 +34,10 @@ MUT_SCALE_TRANSPOSE = 6
 MUT_GATE_SIGN = 7
 MUT_NO_RENORM = 8
 MUT_ENC_TIE_UP = 9
+MUT_NORM_EPS_OUTSIDE = 10
+MUT_NORM_NO_RESIDUAL = 11
+MUT_NORM_GAMMA_PLUS_ONE = 12
+MUT_NORM_QUANT_UNROUNDED = 13
 
 
 def build(force: bool = False) -> str:
@@ -85,6 +89,10 @@ def lib():
         L.orc_bf16_to_double.restype = ctypes.c_double
         L.orc_quant_row.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_void_p, ctypes.c_void_p]
+        L.orc_add_rmsnorm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p]
         L.orc_router.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                  ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                  ctypes.c_void_p, ctypes.c_void_p]
@@ -152,6 +160,26 @@ def quant_row(values, group: int = 128):
     scales = np.zeros(n // group, np.float32)
     lib().orc_quant_row(_p(v), n, group, _p(codes), _p(scales))
     return codes, scales
+
+
+def add_rmsnorm(residual_bits, x_bits, gamma_bits, eps: float, group: int = 128):
+    """Residual add, plain-gamma RMS norm and the FP8 groups of the normed rows.
+
+    bf16 bit arrays residual, x [T, H] and gamma [H] -> (h uint16 [T, H],
+    xn uint16 [T, H], codes uint8 [T, H], scales f32 [T, H/group]).
+    """
+    r = _c(residual_bits, np.uint16)
+    x = _c(x_bits, np.uint16)
+    g = _c(gamma_bits, np.uint16).ravel()
+    T, H = x.shape
+    assert r.shape == x.shape and g.size == H and H % group == 0
+    h = np.zeros((T, H), np.uint16)
+    xn = np.zeros((T, H), np.uint16)
+    codes = np.zeros((T, H), np.uint8)
+    scales = np.zeros((T, H // group), np.float32)
+    lib().orc_add_rmsnorm(_p(r), _p(x), _p(g), T, H, group, float(eps), _p(h), _p(xn),
+                          _p(codes), _p(scales))
+    return h, xn, codes, scales
 
 
 def router_row(x_bf16_bits, wr, k: int):

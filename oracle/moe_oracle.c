@@ -27,6 +27,13 @@
  *   [E] PR #939, section "Fidelity against the PyTorch oracle", prompt pass:
  *       the router's 8th and 9th experts can be 6e-5 apart or exactly tied,
  *       so the top-k tie rule matters; ties go to the lower expert index.
+ *   [F] PR #925/#927 commit "add-norm fused with the routed experts' FP8
+ *       activation quantization": the residual add and RMS norm before the
+ *       MoE also write the normed rows' FP8 groups, rounded exactly as the
+ *       separate quantisation of those (bf16) rows would round them.
+ *   [G] PR #939, section "Kernel contract": the backbone's RMS norm is the
+ *       plain-gamma form (x / rms(x) * gamma, no 1 + gamma offset); section
+ *       "Precision": bf16 residual stream.
  *
  * Readings taken where the pages are silent (each listed in the design notes):
  * router logits fp32-rounded for selection, softmax over the selected logits
@@ -55,6 +62,10 @@ enum {
   MUT_GATE_SIGN = 7,       /* shared gate sigmoid(-x.g) */
   MUT_NO_RENORM = 8,       /* routing weights = full softmax, not renormalised */
   MUT_ENC_TIE_UP = 9,      /* e4m3 encode ties away from zero instead of to even */
+  MUT_NORM_EPS_OUTSIDE = 10,   /* 1 / (sqrt(ms) + eps) instead of 1 / sqrt(ms + eps) */
+  MUT_NORM_NO_RESIDUAL = 11,   /* residual left out of the add */
+  MUT_NORM_GAMMA_PLUS_ONE = 12,/* (1 + gamma) offset form instead of plain gamma */
+  MUT_NORM_QUANT_UNROUNDED = 13,/* FP8 groups from the normed value before its bf16 rounding */
 };
 static int g_mut = 0;
 void orc_set_mutation(int m) { g_mut = m; }
@@ -186,6 +197,51 @@ void orc_quant_row(const float* v, int n, int group, uint8_t* codes, float* scal
       codes[g0 + i] = orc_e4m3_encode(q);
     }
   }
+}
+
+/* ---- residual add + RMS norm + activation quantisation ([F], [G]) -------- */
+/* Per row t of H values:
+ *   h_i  = bf16(residual_i + x_i)                  (the new residual stream)
+ *   r    = 1 / sqrt(sum_i h_i^2 / H + eps)          (double)
+ *   xn_i = bf16(h_i * r * gamma_i)                   (the normed row)
+ * and the FP8 groups of xn exactly as orc_quant_row gives them for the bf16
+ * row.  A zero row with eps = 0 divides by zero (NaN), as the formula does. */
+void orc_add_rmsnorm(const uint16_t* residual, const uint16_t* x, const uint16_t* gamma,
+                     int T, int H, int group, double eps, uint16_t* h_out, uint16_t* xn_out,
+                     uint8_t* codes, float* scales) {
+  double* h = (double*)malloc(sizeof(double) * (size_t)H);
+  float* xf = (float*)malloc(sizeof(float) * (size_t)H);
+  if (!h || !xf) {
+    free(h);
+    free(xf);
+    return;
+  }
+  for (int t = 0; t < T; ++t) {
+    const uint16_t* rr = residual + (size_t)t * H;
+    const uint16_t* xr = x + (size_t)t * H;
+    double ss = 0.0;
+    for (int i = 0; i < H; ++i) {
+      const double sum = g_mut == MUT_NORM_NO_RESIDUAL
+                             ? orc_bf16_to_double(xr[i])
+                             : orc_bf16_to_double(rr[i]) + orc_bf16_to_double(xr[i]);
+      h_out[(size_t)t * H + i] = orc_bf16_from_double(sum);
+      h[i] = bf16r(sum);
+      ss += h[i] * h[i];
+    }
+    const double ms = ss / H;
+    const double r = g_mut == MUT_NORM_EPS_OUTSIDE ? 1.0 / (sqrt(ms) + eps)
+                                                   : 1.0 / sqrt(ms + eps);
+    for (int i = 0; i < H; ++i) {
+      double g = orc_bf16_to_double(gamma[i]);
+      if (g_mut == MUT_NORM_GAMMA_PLUS_ONE) g += 1.0;
+      const double v = h[i] * r * g;
+      xn_out[(size_t)t * H + i] = orc_bf16_from_double(v);
+      xf[i] = g_mut == MUT_NORM_QUANT_UNROUNDED ? (float)v : (float)bf16r(v);
+    }
+    orc_quant_row(xf, H, group, codes + (size_t)t * H, scales + (size_t)t * (H / group));
+  }
+  free(h);
+  free(xf);
 }
 
 /* ---- router ([A], [E]) --------------------------------------------------- */

@@ -355,11 +355,63 @@ def pin_layer_shared_only():
     assert np.array_equal(r.y_ref, 0.5 * ds)
 
 
+def _addnorm_expected_from_xn(xn_bits):
+    """Codes and scales of bf16 rows, through the PyTorch restatement."""
+    codes, scales, _ = torch_quant_groups(bits_to_f64(xn_bits).astype(np.float32))
+    return codes, scales
+
+
+def pin_addnorm_constant_rows():
+    """Constant rows with eps = 0 normalise to sign(h) exactly, so xn is
+    +-gamma bit for bit and its FP8 groups are gamma's."""
+    H = 256
+    res = np.array([-3.0, 0.5, 2.0])[:, None] * np.ones((1, H))
+    x = np.array([1.0, 0.25, -6.0])[:, None] * np.ones((1, H))
+    gam = torch.from_numpy(1.0 + 0.1 * np.random.default_rng(4).standard_normal(H))
+    gbits = W.bf16_bits(gam.to(torch.bfloat16))
+    rb = W.bf16_bits(torch.from_numpy(res).to(torch.bfloat16))
+    xb = W.bf16_bits(torch.from_numpy(x).to(torch.bfloat16))
+    h, xn, codes, scales = oracle.add_rmsnorm(rb, xb, gbits, 0.0)
+    assert np.array_equal(bits_to_f64(h), res + x)
+    want = np.sign(res + x) * bits_to_f64(gbits)[None, :]
+    assert np.array_equal(bits_to_f64(xn), want)
+    c, s = _addnorm_expected_from_xn(W.bf16_bits(torch.from_numpy(want).to(torch.bfloat16)))
+    assert np.array_equal(codes, c) and np.array_equal(scales, s)
+
+
+def pin_addnorm_eps_inside_root():
+    """h = 2 everywhere and eps = 3 * 2^2: 1 / sqrt(4 + 12) = 1/4, so xn = gamma / 2."""
+    H = 256
+    gam = torch.from_numpy(1.0 + 0.1 * np.random.default_rng(5).standard_normal(H))
+    gbits = W.bf16_bits(gam.to(torch.bfloat16))
+    rb = W.bf16_bits(torch.full((1, H), 2.0, dtype=torch.bfloat16))
+    xb = W.bf16_bits(torch.zeros((1, H), dtype=torch.bfloat16))
+    _, xn, _, _ = oracle.add_rmsnorm(rb, xb, gbits, 12.0)
+    assert np.array_equal(bits_to_f64(xn)[0], bits_to_f64(gbits) / 2)
+
+
+def pin_addnorm_vs_library():
+    """Seeded rows against PyTorch's float64 RMS norm (torch.nn.functional.rms_norm),
+    numpy's bf16 rounding of the sums, and the PyTorch group quantiser."""
+    shape = W.FULL
+    r, x, g = W.make_addnorm(shape, 5, 7)
+    h, xn, codes, scales = oracle.add_rmsnorm(W.bf16_bits(r), W.bf16_bits(x), W.bf16_bits(g),
+                                              W.NORM_EPS)
+    hs = np_bf16_round(r.double().numpy() + x.double().numpy())
+    assert np.array_equal(bits_to_f64(h), hs)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(hs), (shape.hidden,),
+                                       weight=g.double(), eps=W.NORM_EPS).numpy()
+    assert np.array_equal(bits_to_f64(xn), np_bf16_round(ref))
+    c, s = _addnorm_expected_from_xn(xn)
+    assert np.array_equal(codes, c) and np.array_equal(scales, s)
+
+
 PINS = [pin_e4m3_table_vs_torch, pin_e4m3_spec_points, pin_e4m3_roundtrip,
         pin_e4m3_boundaries, pin_e4m3_random_vs_torch, pin_bf16_vs_torch,
         pin_quant_special_cases, pin_quant_vs_torch, pin_router_topk_vs_full_sort,
         pin_router_softmax, pin_block_fp8_dot, pin_layer_brute_force,
-        pin_layer_closed_form_all_selected, pin_layer_shared_only]
+        pin_layer_closed_form_all_selected, pin_layer_shared_only,
+        pin_addnorm_constant_rows, pin_addnorm_eps_inside_root, pin_addnorm_vs_library]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -371,7 +423,9 @@ def test_pin(pin):
                                  oracle.MUT_ENC_TRUNC, oracle.MUT_DROP_EXPERT,
                                  oracle.MUT_SWAP_GATE_UP, oracle.MUT_SCALE_TRANSPOSE,
                                  oracle.MUT_GATE_SIGN, oracle.MUT_NO_RENORM,
-                                 oracle.MUT_ENC_TIE_UP])
+                                 oracle.MUT_ENC_TIE_UP, oracle.MUT_NORM_EPS_OUTSIDE,
+                                 oracle.MUT_NORM_NO_RESIDUAL, oracle.MUT_NORM_GAMMA_PLUS_ONE,
+                                 oracle.MUT_NORM_QUANT_UNROUNDED])
 def test_planted_mistake_turns_a_pin_red(mut):
     failed = []
     with oracle.mutation(mut):

@@ -162,6 +162,20 @@ def make_x(shape: MoEShape, rows: int, seed: int, x_kind: str = "normal", device
     return x.to(torch.bfloat16).contiguous()
 
 
+NORM_EPS = 1e-6
+
+
+def make_addnorm(shape: MoEShape, rows: int, seed: int, device="cpu"):
+    """Inputs of the residual add + RMS norm in front of the layer, all bf16:
+    the residual stream [rows, H] ~ N(0, 1), the preceding block's output
+    [rows, H] ~ N(0, 0.5^2), and the norm weight gamma [H] ~ 1 + N(0, 0.1^2)."""
+    H = shape.hidden
+    residual = _randn((rows, H), device, seed, "residual").to(torch.bfloat16).contiguous()
+    x = (0.5 * _randn((rows, H), device, seed, "block_out")).to(torch.bfloat16).contiguous()
+    gamma = (1.0 + 0.1 * _randn((H,), device, seed, "norm_gamma")).to(torch.bfloat16)
+    return residual, x, gamma.contiguous()
+
+
 def layer_seed(workload: Workload, layer: int) -> int:
     return workload.seed + layer if workload.layers > 1 else workload.seed
 
