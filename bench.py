@@ -212,6 +212,207 @@ def traffic_for(kernel: str, workload: str):
     return e["bytes_per_launch"]
 
 
+# ---- the fused residual add + RMS norm + FP8 groups in front of the layer -----
+
+ADDNORM_ROWS = {"addnorm_t1": 1, "addnorm_t11": 11, "addnorm_t1024": 1024}
+ADDNORM_METRIC = "add-norm rows/s"
+
+
+def addnorm_bytes(H: int, T: int) -> int:
+    """Algorithmic bytes of one add-norm launch: read residual and x (bf16),
+    write the new residual and the normed row (bf16), the codes (e4m3) and
+    the group scales (fp32) of every row, plus gamma (bf16) once."""
+    return T * (4 * 2 * H + H + 4 * (H // 128)) + 2 * H
+
+
+def run_addnorm(args):
+    import torch
+    import torch.distributed as dist
+
+    import block_fp8_mixture_router_gb300 as moe
+    import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from block_fp8_mixture_router_gb300.build import build
+    build()
+    moe.load_library()
+    s = W.FULL
+    H = s.hidden
+    T = args.rows if args.rows else ADDNORM_ROWS[args.workload]
+    net = moe.MoELayer(moe.LayerShape(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter,
+                                      s.group), max_rows=1, device=local)
+    # independent input sets (row blocks of one large draw) rotate so that
+    # every launch reads from HBM: at least 512 MB pass per rotation
+    per_set = addnorm_bytes(H, T)
+    R = max(2, -(-(512 << 20) // per_set))
+    r_all, x_all, g = W.make_addnorm(s, R * T, replica_seed(5000, rank), device=dev)
+    h_all, xn_all = torch.empty_like(x_all), torch.empty_like(x_all)
+    c_all = torch.empty((R * T, H), dtype=torch.uint8, device=dev)
+    s_all = torch.empty((R * T, H // 128), dtype=torch.float32, device=dev)
+    sets = [tuple(t[i * T:(i + 1) * T] if t is not g else g
+                  for t in (r_all, x_all, g, h_all, xn_all, c_all, s_all)) for i in range(R)]
+    ctx = net.ctx
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        r, x, g, h, xn, c, sc = sets[i % R]
+        rc = moe.moe_add_rmsnorm_quantize(ctx, r, x, g, W.NORM_EPS, T, h, xn, c, sc, stream)
+        if rc != moe.MOE_OK:
+            raise moe.MoEError(rc, "moe_add_rmsnorm_quantize")
+
+    # about 0.3 s of launches, whole rotations (a launch takes at least ~2.5 us)
+    est = max(2.5e-6, per_set / 5e12)
+    K = args.steps if args.steps is not None else R * max(1, round(0.3 / est / R))
+    Wm = max(3, args.warmup)
+    with torch.cuda.stream(stream):
+        for i in range(Wm):
+            step(i)
+    stream.synchronize()
+    g_rot = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_rot, stream=stream):
+        for i in range(R):
+            step(i)
+    full, rem = divmod(K, R)
+    g_rem = None
+    if rem:
+        g_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rem, stream=stream):
+            for i in range(rem):
+                step(i)
+    with torch.cuda.stream(stream):
+        g_rot.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark_start()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(full):
+            g_rot.replay()
+        if g_rem:
+            g_rem.replay()
+        e1.record(stream)
+    e1.synchronize()
+    if sampler:
+        sampler.mark_end()
+    torch.cuda.synchronize()
+    ms = reduce_max(e0.elapsed_time(e1), dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.finish() if sampler else None
+    value = rows_per_second(world, K, T, ms / 1e3)
+    hbm, _, peak_kind = measured_peaks()
+    launch_us = ms / K * 1e3
+    ab = addnorm_bytes(H, T)
+    gbs = ab / (launch_us * 1e-6) / 1e9
+    line = {
+        "metric": ADDNORM_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "rows": T, "hidden": H, "eps": W.NORM_EPS,
+                   "inputs": "residual N(0,1), block output N(0,0.25), gamma 1 + N(0,0.01), bf16",
+                   "l2": f"inputs rotate over {R} independent row blocks "
+                         f"({R * per_set / 2**20:.0f} MiB per rotation) > 129 MB L2",
+                   "timing": "CUDA graphs of whole rotations, CUDA events on the launch stream",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "add_rmsnorm_quant", "achieved": gbs, "peak": hbm,
+                     "unit": "GB/s", "frac": gbs / hbm, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": ab, "avg_launch_us": launch_us,
+                     "duration_source": "CUDA events over the timed region (one launch per step)",
+                     "traffic": traffic_for("add_rmsnorm_quant", args.workload)},
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+
+    # end to end: residual and x from pinned host memory, all four outputs back
+    r, x, g, h, xn, c, sc = sets[0]
+    rh, xh = r.cpu().pin_memory(), x.cpu().pin_memory()
+    outs_h = [t.cpu().pin_memory() for t in (h, xn, c, sc)]
+    Ke = min(K, 2000)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            r.copy_(rh, non_blocking=True)
+            x.copy_(xh, non_blocking=True)
+            step(0)
+            for dst, src in zip(outs_h, (h, xn, c, sc)):
+                dst.copy_(src, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    t0 = time.perf_counter()
+    for _ in range(Ke):
+        e2e_step()
+    et = reduce_max(time.perf_counter() - t0, dev)
+    line["e2e"] = {"value": rows_per_second(world, Ke, T, et), "unit": UNIT,
+                   "h2d_bytes_per_step": 2 * T * H * 2,
+                   "d2h_bytes_per_step": T * (2 * H * 2 + H + 4 * (H // 128)),
+                   "steps": Ke, "api": "moe_add_rmsnorm_quantize, host copies per step"}
+    if rank == 0 and world == 1:
+        v, n = cpu_addnorm(r.cpu(), x.cpu(), g.cpu(), args.cpu_seconds)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{n} oracle rows of input set 0 ({args.workload}), "
+                                          f"{args.cpu_seconds:.0f} s budget"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    net.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def cpu_addnorm(r, x, g, budget_s: float):
+    """The oracle's add-norm, one row at a time, for about budget_s seconds."""
+    import oracle
+    import workloads as W
+    oracle.build()
+    rb, xb, gb = W.bf16_bits(r), W.bf16_bits(x), W.bf16_bits(g)
+    rows = 0
+    t0 = time.perf_counter()
+    while rows == 0 or time.perf_counter() - t0 < budget_s:
+        i = rows % rb.shape[0]
+        oracle.add_rmsnorm(rb[i:i + 1], xb[i:i + 1], gb, W.NORM_EPS)
+        rows += 1
+    return rows / (time.perf_counter() - t0), rows
+
+
+def reference_addnorm(args):
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads as W
+    T = args.rows if args.rows else ADDNORM_ROWS[args.workload]
+    r, x, g = W.make_addnorm(W.FULL, T, replica_seed(5000, 0))
+    steps = args.steps if args.steps is not None else 5
+    budget = min(60.0, args.cpu_seconds)
+    t0 = time.perf_counter()
+    v, n = cpu_addnorm(r, x, g, budget / steps)
+    for _ in range(steps - 1):
+        cpu_addnorm(r, x, g, budget / steps)
+    dt = time.perf_counter() - t0
+    line = {
+        "impl": "reference", "metric": ADDNORM_METRIC, "value": v, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": steps, "warmup": 0, "ms_per_step": 1e3 * dt / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "rows": T, "hidden": W.FULL.hidden},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"the oracle's add-norm row by row, {budget:.0f} s in all"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ---- replicas ---------------------------------------------------------------
 
 def reduce_max(value: float, dev=None) -> float:
@@ -534,7 +735,9 @@ def run_ours(args):
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.workload in ADDNORM_ROWS:
+        (reference_addnorm if args.impl == "reference" else run_addnorm)(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -36,7 +36,7 @@ PATH_DECODE_ROWS = 6  # the role-split multi-row decode kernel for 2..16 rows
 EXPORTED = ("moe_create", "moe_load_weights", "moe_forward", "moe_forward_host", "moe_route",
             "moe_quantize", "moe_expert_activations", "moe_set_option", "moe_required_bytes",
             "moe_last_device_status", "moe_destroy", "moe_status_string",
-            "moe_profile_forward", "moe_route_static")
+            "moe_profile_forward", "moe_route_static", "moe_add_rmsnorm_quantize")
 
 MOE_ROUTE_STATIC_MAX_LOGITS = 262144
 
@@ -78,6 +78,8 @@ def load_library(path: str = LIB_PATH):
     L.moe_forward_host.argtypes = [vp, vp, vp, i, vp]
     L.moe_route.argtypes = [vp, vp, i, vp, vp, vp]
     L.moe_quantize.argtypes = [vp, vp, i, vp, vp, vp]
+    L.moe_add_rmsnorm_quantize.argtypes = [vp, vp, vp, vp, ctypes.c_float, i, vp, vp, vp, vp,
+                                           vp]
     L.moe_route_static.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
     L.moe_expert_activations.argtypes = [vp, i, vp, vp, vp]
     L.moe_set_option.argtypes = [vp, i, i]
@@ -151,6 +153,13 @@ def moe_route_static(x, router, rows: int, hidden: int, n_experts: int, top_k: i
 def moe_quantize(ctx, x, rows: int, codes, scales, stream=None) -> int:
     return load_library().moe_quantize(ctx, _ptr(x), rows, _ptr(codes), _ptr(scales),
                                        _stream(stream))
+
+
+def moe_add_rmsnorm_quantize(ctx, residual, x, gamma, eps: float, rows: int, h_out, xn_out,
+                             codes, scales, stream=None) -> int:
+    return load_library().moe_add_rmsnorm_quantize(
+        ctx, _ptr(residual), _ptr(x), _ptr(gamma), float(eps), rows, _ptr(h_out), _ptr(xn_out),
+        _ptr(codes), _ptr(scales), _stream(stream))
 
 
 def moe_expert_activations(ctx, rows: int, hq, sh, stream=None) -> int:
@@ -277,6 +286,25 @@ class MoELayer:
         scales = torch.empty((T, H // 128), dtype=torch.float32, device=x.device)
         _check(moe_quantize(self.ctx, x.contiguous(), T, codes, scales, stream), "moe_quantize")
         return codes, scales
+
+    def add_rmsnorm_quantize(self, residual: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor,
+                             eps: float, h_out=None, xn_out=None, stream=None):
+        """Residual add + RMS norm + the normed rows' FP8 groups, one launch.
+        Returns (h, xn, codes, scales); h_out / xn_out may be `residual` or `x`
+        for an in-place update."""
+        for t in (residual, x, gamma):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError("residual, x and gamma must be contiguous bf16 CUDA tensors")
+        T, H = x.shape
+        if residual.shape != x.shape or gamma.shape != (H,):
+            raise ValueError("residual and x must be [rows, H] and gamma [H]")
+        h_out = torch.empty_like(x) if h_out is None else h_out
+        xn_out = torch.empty_like(x) if xn_out is None else xn_out
+        codes = torch.empty((T, H), dtype=torch.uint8, device=x.device)
+        scales = torch.empty((T, H // 128), dtype=torch.float32, device=x.device)
+        _check(moe_add_rmsnorm_quantize(self.ctx, residual, x, gamma, eps, T, h_out, xn_out,
+                                        codes, scales, stream), "moe_add_rmsnorm_quantize")
+        return h_out, xn_out, codes, scales
 
     def expert_activations(self, rows: int, stream=None):
         k, I = self.shape.top_k, self.shape.inter

@@ -14,6 +14,7 @@
 #include <new>
 #include <vector>
 
+#include "addnorm.cuh"
 #include "moe_internal.cuh"
 
 using namespace moe;
@@ -788,6 +789,49 @@ int moe_quantize(moe_ctx* c, const void* x, int rows, uint8_t* codes, float* sca
     cudaGetLastError();
     return MOE_ERR_CUDA;
   }
+  return MOE_OK;
+}
+
+int moe_add_rmsnorm_quantize(moe_ctx* c, const void* residual, const void* x, const void* gamma,
+                             float eps, int rows, void* h_out, void* xn_out, uint8_t* codes,
+                             float* scales, void* stream) {
+  if (!c || rows < 0) return MOE_ERR_INVALID_ARG;
+  if (!(eps >= 0.0f) || !isfinite(eps)) return MOE_ERR_INVALID_ARG;
+  const int H = c->cfg.hidden;
+  if (H > kAddNormMaxHidden) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return MOE_OK;
+  if (!residual || !x || !gamma || !h_out || !xn_out || !codes || !scales)
+    return MOE_ERR_INVALID_ARG;
+  if ((((uintptr_t)residual | (uintptr_t)x | (uintptr_t)gamma | (uintptr_t)h_out |
+        (uintptr_t)xn_out) & 15) || ((uintptr_t)codes & 7) || ((uintptr_t)scales & 3))
+    return MOE_ERR_INVALID_ARG;
+  const size_t nb = (size_t)rows * H * 2, nc = (size_t)rows * H,
+               ns = (size_t)rows * (H / kGroup) * 4, ng = (size_t)H * 2;
+  // each output is either exactly one of the row inputs (in place) or apart
+  // from it; outputs never overlap each other or gamma
+  auto in_place_or_apart = [&](const void* out) {
+    return (out == residual || !overlaps(out, nb, residual, nb)) &&
+           (out == x || !overlaps(out, nb, x, nb));
+  };
+  if (!in_place_or_apart(h_out) || !in_place_or_apart(xn_out) ||
+      overlaps(h_out, nb, xn_out, nb) || overlaps(h_out, nb, gamma, ng) ||
+      overlaps(xn_out, nb, gamma, ng))
+    return MOE_ERR_INVALID_ARG;
+  const void* others[] = {residual, x, h_out, xn_out};
+  for (const void* p : others)
+    if (overlaps(codes, nc, p, nb) || overlaps(scales, ns, p, nb)) return MOE_ERR_INVALID_ARG;
+  if (overlaps(codes, nc, scales, ns) || overlaps(codes, nc, gamma, ng) ||
+      overlaps(scales, ns, gamma, ng))
+    return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  c->last_stream = s;
+  if (launch_add_rmsnorm_quant(static_cast<const bf16*>(residual), static_cast<const bf16*>(x),
+                               static_cast<const bf16*>(gamma), eps, rows, H,
+                               static_cast<bf16*>(h_out), static_cast<bf16*>(xn_out), codes,
+                               scales, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }
 

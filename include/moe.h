@@ -160,6 +160,27 @@ int moe_route_static(const void* x, const float* router, int rows, int hidden, i
 int moe_quantize(moe_ctx* ctx, const void* x, int rows, uint8_t* codes, float* scales,
                  void* stream);
 
+/* Residual add + RMS norm in front of the layer, with the normed rows' FP8
+ * groups, in one launch (PR #925/#927 commit "add-norm fused with the routed
+ * experts' FP8 activation quantization"; PR #939 section "Kernel contract":
+ * plain-gamma RMS norm).  Per row t of H = the context's hidden size:
+ *   h_out[t]  = bf16(residual[t] + x[t])                       (new residual)
+ *   xn_out[t] = bf16(h * (1 / sqrt(sum(h^2) / H + eps)) * gamma) (fp32 math)
+ *   codes[t], scales[t] = the 1 x 128 e4m3 groups of the bf16 row xn_out[t],
+ *     bit for bit what moe_quantize returns for it.
+ * residual, x, h_out, xn_out bf16 [rows][H]; gamma bf16 [H]; codes e4m3
+ * [rows][H]; scales fp32 [rows][H/128]; all device pointers owned by the
+ * caller, the bf16 ones 16-byte aligned, codes 8-byte and scales 4-byte
+ * aligned.  h_out and xn_out may each be exactly `residual` or `x` (in place);
+ * no other overlap is allowed (MOE_ERR_INVALID_ARG).  eps must be finite and
+ * >= 0; a zero row with eps = 0 divides by zero (the output is NaN, as the
+ * formula says).  Needs no loaded weights and no workspace, so rows is not
+ * bounded by max_rows; hidden above 8192 returns MOE_ERR_UNSUPPORTED_SHAPE;
+ * rows == 0 does nothing.  Asynchronous on `stream`. */
+int moe_add_rmsnorm_quantize(moe_ctx* ctx, const void* residual, const void* x,
+                             const void* gamma, float eps, int rows, void* h_out, void* xn_out,
+                             uint8_t* codes, float* scales, void* stream);
+
 /* Expert-side intermediates of the most recent moe_forward, for checking:
  * hq e4m3 [rows][k][I] and sh fp32 [rows][k][I/128] (the re-quantised SwiGLU
  * rows fed to each selected expert's down projection, in rank order), device

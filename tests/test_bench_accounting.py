@@ -49,3 +49,11 @@ def test_stage_bytes_cover_every_timed_stage():
 def test_rows_per_second_is_whole_job():
     assert bench.rows_per_second(1, 100, 11, 0.5) == 100 * 11 / 0.5
     assert bench.rows_per_second(4, 100, 11, 0.5) == 4 * 100 * 11 / 0.5
+
+
+def test_addnorm_bytes():
+    """Per row: residual and x read, new residual and normed row written (bf16),
+    codes (e4m3) and 16 group scales (fp32); gamma once per launch."""
+    H = 2048
+    assert bench.addnorm_bytes(H, 1) == 4 * 2 * H + H + 4 * 16 + 2 * H
+    assert bench.addnorm_bytes(H, 1024) - bench.addnorm_bytes(H, 1023) == 18_496
