@@ -57,3 +57,22 @@ def test_addnorm_bytes():
     H = 2048
     assert bench.addnorm_bytes(H, 1) == 4 * 2 * H + H + 4 * 16 + 2 * H
     assert bench.addnorm_bytes(H, 1024) - bench.addnorm_bytes(H, 1023) == 18_496
+
+
+def test_threaded_oracle_matches_one_thread():
+    """The all-cores oracle leg calls the same C oracle from several threads:
+    its outputs equal the single-threaded ones, row by row."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    import oracle
+    L = W.to_numpy_layer(W.make_layer(W.TINY, 3))
+    xb = W.bf16_bits(W.make_x(W.TINY, 12, 3))
+    one = [oracle.moe_rows(L, xb[r:r + 1]).y_bf16 for r in range(12)]
+    with ThreadPoolExecutor(max_workers=4) as ex:
+        many = list(ex.map(lambda r: oracle.moe_rows(L, xb[r:r + 1]).y_bf16, range(12)))
+    for a, b in zip(one, many):
+        assert np.array_equal(a, b)
+    v, n = bench.cpu_baseline_threads(L, xb, 0.2, 3)
+    assert n >= 3 and v > 0
