@@ -38,6 +38,7 @@ MUT_NORM_EPS_OUTSIDE = 10
 MUT_NORM_NO_RESIDUAL = 11
 MUT_NORM_GAMMA_PLUS_ONE = 12
 MUT_NORM_QUANT_UNROUNDED = 13
+MUT_ROUTER_BF16_IGNORED = 14
 
 
 def build(force: bool = False) -> str:
@@ -60,7 +61,8 @@ class _Layer(ctypes.Structure):
                 ("w13", ctypes.c_void_p), ("s13", ctypes.c_void_p),
                 ("w2", ctypes.c_void_p), ("s2", ctypes.c_void_p),
                 ("wr", ctypes.c_void_p), ("ws13", ctypes.c_void_p),
-                ("ws2", ctypes.c_void_p), ("gate", ctypes.c_void_p)]
+                ("ws2", ctypes.c_void_p), ("gate", ctypes.c_void_p),
+                ("router_bf16", ctypes.c_int)]
 
 
 class _Trace(ctypes.Structure):
@@ -96,6 +98,7 @@ def lib():
         L.orc_router.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                  ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                  ctypes.c_void_p, ctypes.c_void_p]
+        L.orc_router_bf16.argtypes = L.orc_router.argtypes
         L.orc_block_fp8_dot.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
         L.orc_block_fp8_dot.restype = ctypes.c_double
@@ -182,15 +185,17 @@ def add_rmsnorm(residual_bits, x_bits, gamma_bits, eps: float, group: int = 128)
     return h, xn, codes, scales
 
 
-def router_row(x_bf16_bits, wr, k: int):
-    """Router for one row -> (logits f64 [E], idx int32 [k], w f64 [k])."""
+def router_row(x_bf16_bits, wr, k: int, bf16_logits: bool = False):
+    """Router for one row -> (logits f64 [E], idx int32 [k], w f64 [k]).
+    bf16_logits: the variant that routes on bf16-rounded logits."""
     x = _c(x_bf16_bits, np.uint16).ravel()
     wr = _c(wr, np.float32)
     E, H = wr.shape
     logits = np.zeros(E, np.float64)
     idx = np.zeros(k, np.int32)
     w = np.zeros(k, np.float64)
-    lib().orc_router(_p(x), H, _p(wr), E, k, _p(logits), _p(idx), _p(w))
+    fn = lib().orc_router_bf16 if bf16_logits else lib().orc_router
+    fn(_p(x), H, _p(wr), E, k, _p(logits), _p(idx), _p(w))
     return logits, idx, w
 
 
@@ -212,7 +217,7 @@ class OracleResult:
 
 
 def moe_rows(layer: dict, x_bf16_bits, act_quant: bool = True, trace: bool = False,
-             group: int = 128) -> OracleResult:
+             group: int = 128, router_bf16: bool = False) -> OracleResult:
     """Run the layer on T rows.
 
     `layer` holds numpy arrays with the names of the C-ABI weight struct:
@@ -234,7 +239,8 @@ def moe_rows(layer: dict, x_bf16_bits, act_quant: bool = True, trace: bool = Fal
                 ws13=ws13, ws2=_c(layer["ws2"], np.uint16),
                 gate=_c(layer["shared_gate"], np.uint16))
     L = _Layer(H, E, k, I, Is, group, *[_p(arrs[n]) for n in
-                                         ("w13", "s13", "w2", "s2", "wr", "ws13", "ws2", "gate")])
+                                         ("w13", "s13", "w2", "s2", "wr", "ws13", "ws2", "gate")],
+               1 if router_bf16 else 0)
     y = np.zeros((T, H), np.uint16)
     yr = np.zeros((T, H), np.float64)
     tr_arrays = None

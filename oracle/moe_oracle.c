@@ -66,6 +66,7 @@ enum {
   MUT_NORM_NO_RESIDUAL = 11,   /* residual left out of the add */
   MUT_NORM_GAMMA_PLUS_ONE = 12,/* (1 + gamma) offset form instead of plain gamma */
   MUT_NORM_QUANT_UNROUNDED = 13,/* FP8 groups from the normed value before its bf16 rounding */
+  MUT_ROUTER_BF16_IGNORED = 14, /* the bf16-logit router variant leaves the logits in fp32 */
 };
 static int g_mut = 0;
 void orc_set_mutation(int m) { g_mut = m; }
@@ -249,12 +250,13 @@ void orc_add_rmsnorm(const uint16_t* residual, const uint16_t* x, const uint16_t
  * fp32-rounded logit, ties to the lower index, in rank order.  Weights: the
  * softmax of the selected (double) logits, which equals the full softmax
  * renormalised over the selection. */
-void orc_router(const uint16_t* x, int H, const float* wr, int E, int k,
-                double* logits, int32_t* idx, double* w) {
+static void router_impl(const uint16_t* x, int H, const float* wr, int E, int k,
+                        int bf16_logits, double* logits, int32_t* idx, double* w) {
   for (int e = 0; e < E; ++e) {
     double acc = 0.0;
     const float* row = wr + (size_t)e * H;
     for (int i = 0; i < H; ++i) acc += orc_bf16_to_double(x[i]) * (double)row[i];
+    if (bf16_logits && g_mut != MUT_ROUTER_BF16_IGNORED) acc = bf16r((double)(float)acc);
     logits[e] = acc;
   }
   char* taken = (char*)calloc((size_t)E, 1);
@@ -288,6 +290,21 @@ void orc_router(const uint16_t* x, int H, const float* wr, int E, int k,
   double den = 0.0;
   for (int j = 0; j < k; ++j) den += exp(logits[idx[j]] - mx);
   for (int j = 0; j < k; ++j) w[j] = exp(logits[idx[j]] - mx) / den;
+}
+
+void orc_router(const uint16_t* x, int H, const float* wr, int E, int k,
+                double* logits, int32_t* idx, double* w) {
+  router_impl(x, H, wr, E, k, 0, logits, idx, w);
+}
+
+/* Router variant with bf16 logits ([E]: the reference's bf16 PyTorch oracle
+ * routes on bf16 logits, where the 8th and 9th experts can tie exactly): each
+ * logit is the fp32-rounded sum rounded once more to bf16 (nearest, ties to
+ * even); selection (ties to the lower index) and the softmax over the
+ * selection use those bf16 values. */
+void orc_router_bf16(const uint16_t* x, int H, const float* wr, int E, int k,
+                     double* logits, int32_t* idx, double* w) {
+  router_impl(x, H, wr, E, k, 1, logits, idx, w);
 }
 
 /* ---- block-FP8 dot product ---------------------------------------------- */
@@ -343,6 +360,7 @@ typedef struct {
   const uint16_t* ws13;  /* bf16 [2Is][H]; rows 0..Is-1 gate, Is..2Is-1 up */
   const uint16_t* ws2;   /* bf16 [H][Is] */
   const uint16_t* gate;  /* bf16 [H] */
+  int router_bf16;       /* 1: the bf16-logit router variant (orc_router_bf16) */
 } orc_layer;
 
 /* Optional per-row intermediates; any pointer may be NULL. */
@@ -389,7 +407,7 @@ int orc_moe_rows(const orc_layer* L, const uint16_t* x, int T, int act_quant,
   for (int t = 0; t < T; ++t) {
     const uint16_t* xt = x + (size_t)t * H;
     /* router */
-    orc_router(xt, H, L->wr, E, k, logits, idx, w);
+    router_impl(xt, H, L->wr, E, k, L->router_bf16, logits, idx, w);
     if (tr && tr->logits) memcpy(tr->logits + (size_t)t * E, logits, sizeof(double) * E);
     if (tr && tr->idx) memcpy(tr->idx + (size_t)t * k, idx, sizeof(int32_t) * k);
     if (tr && tr->w) memcpy(tr->w + (size_t)t * k, w, sizeof(double) * k);

@@ -58,5 +58,7 @@ def test_refusals_without_a_device(lib):
     assert rc == moe.MOE_ERR_ALLOC_LIMIT and not h.value
     assert moe.moe_create(ok, -1)[0] == moe.MOE_ERR_INVALID_ARG
     assert moe.moe_forward(None, None, None, 1, 0) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_add_rmsnorm_quantize(None, None, None, None, 1e-6, 1, None, None, None,
+                                        None, 0) == moe.MOE_ERR_INVALID_ARG
     moe.moe_destroy(None)
     assert moe.status_string(moe.MOE_ERR_DEVICE_TIMEOUT) == "device-side wait timed out"

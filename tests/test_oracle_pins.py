@@ -355,6 +355,31 @@ def pin_layer_shared_only():
     assert np.array_equal(r.y_ref, 0.5 * ds)
 
 
+def pin_router_bf16_logits():
+    """The bf16-logit router variant: logits from numpy's float64 products,
+    rounded to fp32 and then bf16 by PyTorch's casts; the k largest by a full
+    stable sort of (-logit, expert); weights by scipy's softmax over the
+    selection.  On these rows the variant must meet exact ties among the first
+    k + 1 and pick differently from the fp32 router at least once."""
+    from scipy.special import softmax
+    shape = W.FULL
+    E, k = shape.n_experts, shape.top_k
+    wr = W.make_router(shape, 21).numpy()
+    xb = W.bf16_bits(W.make_x(shape, 24, 21))
+    lg = bits_to_f64(xb) @ wr.astype(np.float64).T
+    lb = torch.from_numpy(lg).float().to(torch.bfloat16).double().numpy()
+    differs = ties = 0
+    for t in range(xb.shape[0]):
+        _, idx, w = oracle.router_row(xb[t], wr, k, bf16_logits=True)
+        order = np.lexsort((np.arange(E), -lb[t]))
+        assert np.array_equal(idx, order[:k])
+        assert np.allclose(w, softmax(lb[t][order[:k]]), rtol=1e-12, atol=0)
+        top = lb[t][order[:k + 1]]
+        ties += int(np.any(top[1:] == top[:-1]))
+        differs += int(not np.array_equal(idx, oracle.router_row(xb[t], wr, k)[1]))
+    assert ties > 0 and differs > 0, (ties, differs)
+
+
 def _addnorm_expected_from_xn(xn_bits):
     """Codes and scales of bf16 rows, through the PyTorch restatement."""
     codes, scales, _ = torch_quant_groups(bits_to_f64(xn_bits).astype(np.float32))
@@ -411,7 +436,8 @@ PINS = [pin_e4m3_table_vs_torch, pin_e4m3_spec_points, pin_e4m3_roundtrip,
         pin_quant_special_cases, pin_quant_vs_torch, pin_router_topk_vs_full_sort,
         pin_router_softmax, pin_block_fp8_dot, pin_layer_brute_force,
         pin_layer_closed_form_all_selected, pin_layer_shared_only,
-        pin_addnorm_constant_rows, pin_addnorm_eps_inside_root, pin_addnorm_vs_library]
+        pin_addnorm_constant_rows, pin_addnorm_eps_inside_root, pin_addnorm_vs_library,
+        pin_router_bf16_logits]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -425,7 +451,8 @@ def test_pin(pin):
                                  oracle.MUT_GATE_SIGN, oracle.MUT_NO_RENORM,
                                  oracle.MUT_ENC_TIE_UP, oracle.MUT_NORM_EPS_OUTSIDE,
                                  oracle.MUT_NORM_NO_RESIDUAL, oracle.MUT_NORM_GAMMA_PLUS_ONE,
-                                 oracle.MUT_NORM_QUANT_UNROUNDED])
+                                 oracle.MUT_NORM_QUANT_UNROUNDED,
+                                 oracle.MUT_ROUTER_BF16_IGNORED])
 def test_planted_mistake_turns_a_pin_red(mut):
     failed = []
     with oracle.mutation(mut):
