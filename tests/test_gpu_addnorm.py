@@ -154,7 +154,6 @@ def test_addnorm_in_place(full_ctx):
 def test_addnorm_degenerate_rows(full_ctx):
     """A zero row, a row whose residual cancels x, a constant row and a row of
     large values; eps > 0 keeps the zero rows finite (xn = 0, scale 1)."""
-    H = W.FULL.hidden
     r, x, g = W.make_addnorm(W.FULL, 4, 9, device="cuda")
     r[0] = 0
     x[0] = 0
@@ -171,7 +170,6 @@ def test_addnorm_degenerate_rows(full_ctx):
         assert torch.all(scales[t] == 1.0)
     # constant row: xn = gamma * 3.5 / sqrt(3.5^2 + eps), within one ulp of gamma
     assert np.all(_ulps_bf16(bits(xn[2:3])[0], bits(g.cpu()[None])[0]) <= 1)
-    assert H % 128 == 0
 
 
 def test_addnorm_zero_rows_and_refusals(full_ctx):
