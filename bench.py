@@ -504,6 +504,36 @@ def cpu_baseline(layer_host, xb, budget_s: float):
     return rows / dt, rows
 
 
+def replay_quantiles(graph, stream, steps_per_replay: int, replays: int,
+                     cap: int = 200) -> dict:
+    """p10 / median / p90 of the time per step (ms), from CUDA events recorded
+    on the launch stream between consecutive replays of the timed graph
+    (after the timed region, so the events do not touch it)."""
+    import torch
+    n = min(cap, replays)
+    if n < 3 or graph is None:
+        return {"unavailable": "fewer than 3 whole-graph replays"}
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(n):
+            graph.replay()
+            ev[i + 1].record(stream)
+    ev[-1].synchronize()
+    per = sorted(ev[i].elapsed_time(ev[i + 1]) / steps_per_replay for i in range(n))
+    return {"p10": per_quantile(per, 0.1), "median": per_quantile(per, 0.5),
+            "p90": per_quantile(per, 0.9), "replays": n,
+            "steps_per_replay": steps_per_replay}
+
+
+def per_quantile(sorted_vals, q: float) -> float:
+    """Linear-interpolated quantile of an ascending list."""
+    pos = q * (len(sorted_vals) - 1)
+    lo = int(pos)
+    hi = min(lo + 1, len(sorted_vals) - 1)
+    return sorted_vals[lo] + (sorted_vals[hi] - sorted_vals[lo]) * (pos - lo)
+
+
 def host_threads() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -644,6 +674,10 @@ def run_ours(args):
         dist.barrier()
     clocks = sampler.finish() if sampler else None
     value = rows_per_second(world, K, T * layers_per_step, ms / 1e3)
+    try:
+        quantiles = replay_quantiles(g_full, stream, per_graph, full)
+    except Exception as e:  # reported, never fatal to the line
+        quantiles = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
 
     # per-kernel device times (events after every launch), same rotation
     stage_ms = {}
@@ -718,6 +752,7 @@ def run_ours(args):
                            "distinct_experts": U,
                            "fp8_tflops": fp8_flops(s, T) / (step_ms * 1e-3) / 1e12},
         "stages_us": {n: round(v * 1e3, 3) for n, v in stage_prof.items()},
+        "step_ms_quantiles": quantiles,
         "gpu_launches": K * launches_per_step * layers_per_step,
         "clocks": clocks,
     }

@@ -76,3 +76,51 @@ def test_threaded_oracle_matches_one_thread():
         assert np.array_equal(a, b)
     v, n = bench.cpu_baseline_threads(L, xb, 0.2, 3)
     assert n >= 3 and v > 0
+
+
+def test_quantiles_interpolate():
+    import numpy as np
+    vals = sorted(np.random.default_rng(0).random(57).tolist())
+    for q in (0.1, 0.5, 0.9):
+        assert abs(bench.per_quantile(vals, q) - float(np.quantile(vals, q))) < 1e-12
+
+
+def test_replay_quantiles_logic(monkeypatch):
+    """The per-replay event bookkeeping, with host stand-ins for CUDA events:
+    replay i takes (i + 1) ms, so per-step times are (i + 1) / steps."""
+    import contextlib
+
+    import torch
+
+    clock = [0.0]
+
+    class FakeEvent:
+        def __init__(self, enable_timing=False):
+            self.t = None
+
+        def record(self, stream=None):
+            self.t = clock[0]
+
+        def elapsed_time(self, other):
+            return other.t - self.t
+
+        def synchronize(self):
+            pass
+
+    class FakeGraph:
+        def __init__(self):
+            self.n = 0
+
+        def replay(self):
+            self.n += 1
+            clock[0] += float(self.n)
+
+    monkeypatch.setattr(torch.cuda, "Event", FakeEvent)
+    monkeypatch.setattr(torch.cuda, "stream", lambda s: contextlib.nullcontext())
+    q = bench.replay_quantiles(FakeGraph(), None, 4, 11)
+    per = [(i + 1) / 4 for i in range(11)]
+    assert q["replays"] == 11 and q["steps_per_replay"] == 4
+    assert abs(q["median"] - per[5]) < 1e-12
+    assert abs(q["p10"] - bench.per_quantile(per, 0.1)) < 1e-12
+    assert "unavailable" in bench.replay_quantiles(FakeGraph(), None, 4, 2)
+    assert "unavailable" in bench.replay_quantiles(None, None, 4, 50)
