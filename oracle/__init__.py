@@ -39,6 +39,7 @@ MUT_NORM_NO_RESIDUAL = 11
 MUT_NORM_GAMMA_PLUS_ONE = 12
 MUT_NORM_QUANT_UNROUNDED = 13
 MUT_ROUTER_BF16_IGNORED = 14
+MUT_PER_ROW_IGNORED = 15
 
 
 def build(force: bool = False) -> str:
@@ -62,7 +63,7 @@ class _Layer(ctypes.Structure):
                 ("w2", ctypes.c_void_p), ("s2", ctypes.c_void_p),
                 ("wr", ctypes.c_void_p), ("ws13", ctypes.c_void_p),
                 ("ws2", ctypes.c_void_p), ("gate", ctypes.c_void_p),
-                ("router_bf16", ctypes.c_int)]
+                ("router_bf16", ctypes.c_int), ("act_per_row", ctypes.c_int)]
 
 
 class _Trace(ctypes.Structure):
@@ -217,13 +218,16 @@ class OracleResult:
 
 
 def moe_rows(layer: dict, x_bf16_bits, act_quant: bool = True, trace: bool = False,
-             group: int = 128, router_bf16: bool = False) -> OracleResult:
+             group: int = 128, router_bf16: bool = False,
+             act_per_row: bool = False) -> OracleResult:
     """Run the layer on T rows.
 
     `layer` holds numpy arrays with the names of the C-ABI weight struct:
     w13 uint8 [E,2I,H], s13 f32 [E,2I/G,H/G], w2 uint8 [E,H,I], s2 f32 [E,H/G,I/G],
     router f32 [E,H], ws13 uint16(bf16) [2Is,H], ws2 uint16 [H,Is],
     shared_gate uint16 [H], and the scalar `top_k`.
+    Variants: router_bf16 routes on bf16-rounded logits; act_per_row gives x
+    and the SwiGLU rows one activation scale per row instead of per 1 x group.
     """
     x = _c(x_bf16_bits, np.uint16)
     T, H = x.shape
@@ -240,7 +244,7 @@ def moe_rows(layer: dict, x_bf16_bits, act_quant: bool = True, trace: bool = Fal
                 gate=_c(layer["shared_gate"], np.uint16))
     L = _Layer(H, E, k, I, Is, group, *[_p(arrs[n]) for n in
                                          ("w13", "s13", "w2", "s2", "wr", "ws13", "ws2", "gate")],
-               1 if router_bf16 else 0)
+               1 if router_bf16 else 0, 1 if act_per_row else 0)
     y = np.zeros((T, H), np.uint16)
     yr = np.zeros((T, H), np.float64)
     tr_arrays = None

@@ -67,6 +67,7 @@ enum {
   MUT_NORM_GAMMA_PLUS_ONE = 12,/* (1 + gamma) offset form instead of plain gamma */
   MUT_NORM_QUANT_UNROUNDED = 13,/* FP8 groups from the normed value before its bf16 rounding */
   MUT_ROUTER_BF16_IGNORED = 14, /* the bf16-logit router variant leaves the logits in fp32 */
+  MUT_PER_ROW_IGNORED = 15,     /* the one-scale-per-row variant keeps 1 x 128 groups */
 };
 static int g_mut = 0;
 void orc_set_mutation(int m) { g_mut = m; }
@@ -245,6 +246,15 @@ void orc_add_rmsnorm(const uint16_t* residual, const uint16_t* x, const uint16_t
   free(xf);
 }
 
+/* One scale for a whole row of n values (the per-row activation variant): the
+ * row quantised as one group, its scale repeated for each of the n / G weight
+ * blocks, so that the block-FP8 dot below reads it per block unchanged. */
+static void quant_row_one_scale(const float* v, int n, int G, uint8_t* codes, float* scales) {
+  float s;
+  orc_quant_row(v, n, n, codes, &s);
+  for (int b = 0; b < n / G; ++b) scales[b] = s;
+}
+
 /* ---- router ([A], [E]) --------------------------------------------------- */
 /* logits[e] = sum_i x_i * Wr[e,i] in double.  Selection: k largest by the
  * fp32-rounded logit, ties to the lower index, in rank order.  Weights: the
@@ -361,6 +371,7 @@ typedef struct {
   const uint16_t* ws2;   /* bf16 [H][Is] */
   const uint16_t* gate;  /* bf16 [H] */
   int router_bf16;       /* 1: the bf16-logit router variant (orc_router_bf16) */
+  int act_per_row;       /* 1: one activation scale per row (x and h) instead of per 1 x G */
 } orc_layer;
 
 /* Optional per-row intermediates; any pointer may be NULL. */
@@ -413,7 +424,10 @@ int orc_moe_rows(const orc_layer* L, const uint16_t* x, int T, int act_quant,
     if (tr && tr->w) memcpy(tr->w + (size_t)t * k, w, sizeof(double) * k);
     /* activation quantisation */
     for (int i = 0; i < H; ++i) xf[i] = (float)orc_bf16_to_double(xt[i]);
-    orc_quant_row(xf, H, G, xq, sx);
+    if (L->act_per_row && g_mut != MUT_PER_ROW_IGNORED)
+      quant_row_one_scale(xf, H, G, xq, sx);
+    else
+      orc_quant_row(xf, H, G, xq, sx);
     if (tr && tr->xq) memcpy(tr->xq + (size_t)t * H, xq, H);
     if (tr && tr->sx) memcpy(tr->sx + (size_t)t * nb_h, sx, sizeof(float) * nb_h);
 
@@ -451,7 +465,12 @@ int orc_moe_rows(const orc_layer* L, const uint16_t* x, int T, int act_quant,
         }
         hf[n] = (float)(silu(g) * u);
       }
-      if (act_quant) orc_quant_row(hf, I, G, hq, sh);
+      if (act_quant) {
+        if (L->act_per_row && g_mut != MUT_PER_ROW_IGNORED)
+          quant_row_one_scale(hf, I, G, hq, sh);
+        else
+          orc_quant_row(hf, I, G, hq, sh);
+      }
       if (tr && tr->hq) memcpy(tr->hq + ((size_t)t * k + j) * I, hq, I);
       if (tr && tr->sh) memcpy(tr->sh + ((size_t)t * k + j) * nb_i, sh, sizeof(float) * nb_i);
       /* down */

@@ -62,9 +62,10 @@ def silu(a):
     return a / (1.0 + np.exp(-a))
 
 
-def brute_force_layer(layer: dict, x_bits: np.ndarray, group=128):
+def brute_force_layer(layer: dict, x_bits: np.ndarray, group=128, act_per_row=False):
     """Dense restatement on tiny shapes: every expert for every row, masked by a
-    top-k found by scanning all k-subsets; quantisation through PyTorch's cast."""
+    top-k found by scanning all k-subsets; quantisation through PyTorch's cast
+    (one scale per row of x and of h when act_per_row)."""
     x = bits_to_f64(x_bits)
     T, H = x.shape
     E, I2, _ = layer["w13"].shape
@@ -80,7 +81,7 @@ def brute_force_layer(layer: dict, x_bits: np.ndarray, group=128):
     ws13 = bits_to_f64(layer["ws13"])
     ws2 = bits_to_f64(layer["ws2"])
     gate = bits_to_f64(layer["shared_gate"])
-    _, _, xd = torch_quant_groups(x.astype(np.float32), group)
+    _, _, xd = torch_quant_groups(x.astype(np.float32), H if act_per_row else group)
     out = np.zeros((T, H))
     sel_all = []
     for t in range(T):
@@ -100,7 +101,7 @@ def brute_force_layer(layer: dict, x_bits: np.ndarray, group=128):
         for j, e in enumerate(order):
             z = np_bf16_round(w13[e] @ xd[t])
             h = (silu(z[:I]) * z[I:]).astype(np.float32)
-            _, _, hd = torch_quant_groups(h[None, :], group)
+            _, _, hd = torch_quant_groups(h[None, :], I if act_per_row else group)
             d = np_bf16_round(w2[e] @ hd[0])
             out[t] += wts[j] * d
         zs = np_bf16_round(ws13 @ x[t])
@@ -314,6 +315,18 @@ def pin_layer_brute_force():
         assert np.allclose(r.y_ref, ref, rtol=1e-9, atol=1e-12 * np.abs(ref).max())
 
 
+def pin_layer_brute_force_per_row_scale():
+    """The one-scale-per-row variant against the dense restatement quantising
+    each row of x and of h as a single group; it must differ from 1 x 128."""
+    L, x = tiny_layer(7, 3)
+    r = oracle.moe_rows(L, x, trace=True, act_per_row=True)
+    ref, sel = brute_force_layer(L, x, act_per_row=True)
+    assert np.array_equal(r.trace["idx"], sel)
+    assert np.allclose(r.y_ref, ref, rtol=1e-9, atol=1e-12 * np.abs(ref).max())
+    assert np.all(r.trace["sx"] == r.trace["sx"][:, :1])
+    assert not np.array_equal(r.y_ref, oracle.moe_rows(L, x).y_ref)
+
+
 def pin_layer_closed_form_all_selected():
     """E = k, zero router -> every weight 1/k; identical experts -> the routed
     sum is one dense block-FP8 SwiGLU; zero shared weights -> gamma * 0."""
@@ -437,7 +450,7 @@ PINS = [pin_e4m3_table_vs_torch, pin_e4m3_spec_points, pin_e4m3_roundtrip,
         pin_router_softmax, pin_block_fp8_dot, pin_layer_brute_force,
         pin_layer_closed_form_all_selected, pin_layer_shared_only,
         pin_addnorm_constant_rows, pin_addnorm_eps_inside_root, pin_addnorm_vs_library,
-        pin_router_bf16_logits]
+        pin_router_bf16_logits, pin_layer_brute_force_per_row_scale]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -452,7 +465,7 @@ def test_pin(pin):
                                  oracle.MUT_ENC_TIE_UP, oracle.MUT_NORM_EPS_OUTSIDE,
                                  oracle.MUT_NORM_NO_RESIDUAL, oracle.MUT_NORM_GAMMA_PLUS_ONE,
                                  oracle.MUT_NORM_QUANT_UNROUNDED,
-                                 oracle.MUT_ROUTER_BF16_IGNORED])
+                                 oracle.MUT_ROUTER_BF16_IGNORED, oracle.MUT_PER_ROW_IGNORED])
 def test_planted_mistake_turns_a_pin_red(mut):
     failed = []
     with oracle.mutation(mut):
