@@ -106,7 +106,8 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out);
 int moe_load_weights(moe_ctx* ctx, const moe_weights* w, int pointers_on_device, void* stream);
 
 /* y = MoE(x).  x: bf16 [rows][H] on the device; y: bf16 [rows][H] on the
- * device; x and y must not overlap.  0 <= rows <= max_rows; rows == 0 does
+ * device; x and y must not overlap and must be 16-byte aligned
+ * (MOE_ERR_INVALID_ARG otherwise).  0 <= rows <= max_rows; rows == 0 does
  * nothing.  Asynchronous on `stream`: no allocation, no host synchronisation,
  * expert counts stay on the device.  Results are bitwise identical from run
  * to run for the same inputs.  Device-side faults of earlier work surface as
