@@ -10,7 +10,9 @@ rows are cut into chunks of at most 16.  The claims: the slots are a
 permutation of the T*k pairs, ordered by (expert, row); the chunks tile every
 expert's rows exactly and their number stays within the workspace bound
 ceil(T*k/16) + E.  This test restates the steps block by block with numpy and
-checks those claims on uniform and skewed routings.
+checks those claims on uniform and skewed routings.  The chained decode
+path (at most 16 rows) schedules with one row mask per expert instead; its
+restatement below is held to the same claims.
 """
 import numpy as np
 import pytest
@@ -83,3 +85,48 @@ def test_schedule_claims(T, E, k, skew):
         covered[first:first + n] += 1
     assert np.all(covered == 1)
     assert n_chunks == len(chunks) <= -(-P // CHUNK) + E
+
+
+def decode_schedule(idx: np.ndarray, E: int):
+    """The chained decode path's schedule (rows <= 16): one row mask per
+    expert, one chunk per selected expert, slots by an exclusive scan of the
+    masks' popcounts and, inside an expert, in row order."""
+    T, k = idx.shape
+    mask = np.zeros(E, np.int64)
+    for p in range(T * k):
+        mask[idx[p // k, p % k]] |= 1 << (p // k)
+    cnt = np.array([bin(int(m)).count("1") for m in mask])
+    slot0 = np.concatenate([[0], np.cumsum(cnt)])[:-1]
+    used = np.concatenate([[0], np.cumsum(cnt > 0)])[:-1]
+    slot_of_pair = np.full(T * k, -1, np.int64)
+    chunks = {}
+    for e in range(E):
+        if cnt[e] == 0:
+            continue
+        chunks[int(used[e])] = (e, int(slot0[e]), int(cnt[e]))
+        for r, t in enumerate(t for t in range(T) if mask[e] >> t & 1):
+            j = int(np.nonzero(idx[t] == e)[0][0])
+            slot_of_pair[t * k + j] = slot0[e] + r
+    return slot_of_pair, chunks, int((cnt > 0).sum())
+
+
+@pytest.mark.parametrize("T", [1, 2, 6, 11, 16])
+@pytest.mark.parametrize("E,k", [(16, 4), (256, 8)])
+def test_decode_schedule_claims(T, E, k):
+    rng = np.random.default_rng(T * 7 + E)
+    for skew in (0.0, 3.0):
+        idx = routing(rng, T, E, k, skew)
+        slot_of_pair, chunks, n_used = decode_schedule(idx, E)
+        P = T * k
+        assert np.array_equal(np.sort(slot_of_pair), np.arange(P))
+        pair_of_slot = np.empty(P, np.int64)
+        pair_of_slot[slot_of_pair] = np.arange(P)
+        key = idx.reshape(-1)[pair_of_slot] * (T + 1) + pair_of_slot // k
+        assert np.all(np.diff(key) > 0)
+        assert sorted(chunks) == list(range(n_used))
+        covered = np.zeros(P, np.int64)
+        for e, first, n in chunks.values():
+            assert 1 <= n <= min(T, CHUNK)
+            assert np.all(idx.reshape(-1)[pair_of_slot[first:first + n]] == e)
+            covered[first:first + n] += 1
+        assert np.all(covered == 1)
