@@ -476,7 +476,8 @@ def run_reference(args):
     value = rows / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": steps, "warmup": 1, "ms_per_step": 1e3 * dt / steps, "higher_is_better": True,
+        "steps": steps, "warmup": 1 if args.warmup else 0, "ms_per_step": 1e3 * dt / steps,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "rows": T, "hidden": s.hidden,
                    "experts": s.n_experts, "top_k": s.top_k, "inter": s.inter,

@@ -124,3 +124,45 @@ def test_replay_quantiles_logic(monkeypatch):
     assert abs(q["p10"] - bench.per_quantile(per, 0.1)) < 1e-12
     assert "unavailable" in bench.replay_quantiles(FakeGraph(), None, 4, 2)
     assert "unavailable" in bench.replay_quantiles(None, None, 4, 50)
+
+
+def _reference_line(*extra, env_extra=None):
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, **(env_extra or {}))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", *extra], cwd=root,
+                       capture_output=True, text=True, timeout=600, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    return [json.loads(ln) for ln in lines]
+
+
+def _check_reference_contract(d):
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_layer():
+    (d,) = _reference_line("--steps", "1", "--warmup", "0")
+    _check_reference_contract(d)
+    assert d["metric"] == bench.METRIC and d["config"]["workload"] == "decode_t1"
+    assert d["warmup"] == 0
+
+
+def test_reference_arm_addnorm():
+    (d,) = _reference_line("--workload", "addnorm_t1", "--steps", "2", "--cpu-seconds", "0.4")
+    _check_reference_contract(d)
+    assert d["metric"] == bench.ADDNORM_METRIC
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    assert _reference_line("--steps", "1", env_extra={"RANK": "1", "WORLD_SIZE": "2"}) == []
