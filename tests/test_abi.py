@@ -62,3 +62,16 @@ def test_refusals_without_a_device(lib):
                                         None, 0) == moe.MOE_ERR_INVALID_ARG
     moe.moe_destroy(None)
     assert moe.status_string(moe.MOE_ERR_DEVICE_TIMEOUT) == "device-side wait timed out"
+
+
+def test_header_constants_match_the_binding():
+    """Every MOE_* enumerator of include/moe.h has the same value in the binding."""
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    found = {}
+    for body in re.findall(r"enum\s*\{(.*?)\}", src, flags=re.S):
+        for name, value in re.findall(r"(MOE_[A-Z_]+)\s*=\s*(-?\d+)", body):
+            found[name] = int(value)
+    assert len(found) >= 9
+    for name, value in found.items():
+        assert getattr(moe, name) == value, name
