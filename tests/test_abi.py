@@ -1,5 +1,6 @@
 """The C-ABI library loads on a host without a GPU and exports every entry
 point include/moe.h declares; shape refusal needs no device."""
+import ctypes
 import os
 import re
 
@@ -75,3 +76,31 @@ def test_header_constants_match_the_binding():
     assert len(found) >= 9
     for name, value in found.items():
         assert getattr(moe, name) == value, name
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """moe_config and moe_weights as ctypes lays them out equal the C layout
+    of include/moe.h (offsets and sizes printed by a program gcc builds)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = {"moe_config": [f for f, _ in moe.moe_config._fields_],
+              "moe_weights": [f for f, _ in moe.moe_weights._fields_]}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "moe.h"', "int main(void) {"]
+    for st, names in fields.items():
+        lines.append(f'  printf("{st} size %zu\\n", sizeof({st}));')
+        for n in names:
+            lines.append(f'  printf("{st} {n} %zu\\n", offsetof({st}, {n}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    c_layout = {tuple(ln.split()[:2]): int(ln.split()[2]) for ln in out if ln.strip()}
+    for st, cls in (("moe_config", moe.moe_config), ("moe_weights", moe.moe_weights)):
+        assert c_layout[(st, "size")] == ctypes.sizeof(cls), st
+        for n in fields[st]:
+            assert c_layout[(st, n)] == getattr(cls, n).offset, (st, n)
