@@ -312,6 +312,10 @@ def run_addnorm(args):
         dist.barrier()
     clocks = sampler.finish() if sampler else None
     value = rows_per_second(world, K, T, ms / 1e3)
+    try:
+        quantiles = replay_quantiles(g_rot, stream, R, full)
+    except Exception as e:  # reported, never fatal to the line
+        quantiles = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
     hbm, _, peak_kind = measured_peaks()
     launch_us = ms / K * 1e3
     ab = addnorm_bytes(H, T)
@@ -333,6 +337,7 @@ def run_addnorm(args):
                      "traffic": traffic_for("add_rmsnorm_quant", args.workload)},
         "gpu_launches": K,
         "clocks": clocks,
+        "step_ms_quantiles": quantiles,
     }
 
     # end to end: residual and x from pinned host memory, all four outputs back
