@@ -49,6 +49,8 @@ def parse():
                          "is quoted at 1, 4, 16, 64, 256 and 1024")
     ap.add_argument("--path", choices=tuple(PATHS), default="auto",
                     help="kernel path (MOE_OPT_PATH): auto picks by row count")
+    ap.add_argument("--no-prompt", action="store_true",
+                    help="leave out the prompt legs of the default one-row line")
     return ap.parse_args()
 
 
@@ -75,33 +77,34 @@ def stage_bytes(s, T: int, U: int) -> dict:
     G, H, I, Is, E, k = s.group, s.hidden, s.inter, s.shared_inter, s.n_experts, s.top_k
     w13 = 2 * I * H + 4 * (2 * I // G) * (H // G)
     w2 = H * I + 4 * (H // G) * (I // G)
-    gateup = U * w13 + 2 * 2 * Is * H + T * H + 2 * T * H + T * k * (I + 4 * (I // G)) + 2 * T * Is
-    down = U * w2 + 2 * H * Is + T * k * (I + 4 * (I // G)) + 2 * T * Is
+    # layer inputs, outputs and weights only: codes, SwiGLU rows, expert
+    # outputs and other workspace traffic are not algorithmic bytes
+    gateup = U * w13 + 2 * 2 * Is * H + 2 * T * H
+    down = U * w2 + 2 * H * Is
     return {
         # decode path: one persistent kernel for the whole layer
         "decode_layer": layer_bytes(s, T, U),
         "decode_row": layer_bytes(s, T, U),
         "decode_rows": layer_bytes(s, T, U),
         # decode path, chained variant (three kernels)
-        "route_decode": 4 * E * H + 2 * T * H + 4 * T * E + T * H + 4 * T * (H // G) + 2 * H
-        + 8 * T * k,
+        "route_decode": 4 * E * H + 2 * T * H + 2 * H,
         "gateup_decode": gateup,
-        "down_combine_decode": down + 8 * T * k + 4 * T + 2 * T * H,
+        "down_combine_decode": down + 2 * T * H,
         # prompt path
-        "router": 4 * E * H + 2 * T * H + 4 * T * E,
-        "quant_gamma": 2 * T * H + 2 * H + T * H + 4 * T * (H // G) + 4 * T,
-        "topk": 4 * T * E + 8 * T * k,
-        "schedule": 4 * T * k * 4,
+        "router": 4 * E * H + 2 * T * H,
+        "quant_gamma": 2 * T * H + 2 * H,
+        "topk": 0,
+        "schedule": 0,
         "gateup": gateup,
-        "down": down + 2 * T * k * H + 2 * T * H,
-        "combine": 2 * T * k * H + 2 * T * H + 2 * T * H + 8 * T * k + 4 * T,
+        "down": down,
+        "combine": 2 * T * H,
         # prompt path on tcgen05
-        "router_tc": 4 * E * H + 2 * T * H + 4 * T * E,
-        "quant_scatter": 2 * T * H + 2 * H + T * k * (H + 4 * (H // G)) + 4 * T + 4 * T * k,
-        "shared_gateup_tc": 2 * 2 * Is * H + 2 * T * H + 2 * T * Is,
-        "gateup_tc": U * w13 + T * k * (H + 4 * (H // G)) + T * k * (I + 4 * (I // G)),
-        "shared_down_tc": 2 * H * Is + 2 * T * Is + 2 * T * H,
-        "down_tc": U * w2 + T * k * (I + 4 * (I // G)) + 2 * T * k * H,
+        "router_tc": 4 * E * H + 2 * T * H,
+        "quant_scatter": 2 * T * H + 2 * H,
+        "shared_gateup_tc": 2 * 2 * Is * H + 2 * T * H,
+        "gateup_tc": U * w13,
+        "shared_down_tc": 2 * H * Is,
+        "down_tc": U * w2,
     }
 
 
@@ -575,30 +578,25 @@ def cpu_baseline_threads(layer_host, xb, budget_s: float, threads: int):
     return sum(counts) / dt, sum(counts)
 
 
-def run_ours(args):
-    import numpy as np
+def warm_gpu(stream):
+    """Keep the GPU busy for ~50 us on `stream` so that the host enqueues the
+    timed region's start event and graphs while the device is still working:
+    the region then starts when its first step starts, not when the host
+    catches up."""
     import torch
-    import torch.distributed as dist
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(100_000)
 
-    import block_fp8_mixture_router_gb300 as moe
-    import workloads as W
 
-    rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    from block_fp8_mixture_router_gb300.build import build
-    build()
-    moe.load_library()
-
-    wl = W.WORKLOADS[args.workload]
+def measure_layer(moe, W, wl, T: int, K: int, Wm: int, L: int, path: str, dev, rank: int,
+                  world: int, e2e_steps: int = 2000) -> dict:
+    """Builds L layer instances (or wl's chained layers), times exactly K
+    steps of T rows in CUDA graphs, and returns the line's measured fields."""
+    import torch
     s = wl.shape
-    T = args.rows if args.rows else wl.rows
+    local = dev.index
     sweep = wl.layers > 1
-    # a single-layer workload rotates over independent layer instances (L2
-    # cold); the sweep passes the rows through its layers in order
-    L = wl.layers if sweep else max(1, args.instances)
+    L = wl.layers if sweep else L
     shape = moe.LayerShape(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, s.group)
     nets, xs, ys, layers = [], [], [], []
     for i in range(L):
@@ -606,7 +604,7 @@ def run_ours(args):
         layer = W.make_layer(s, seed, wl.x_kind, device=dev)
         net = moe.MoELayer(shape, max_rows=max(T, 16), device=local)
         net.load(layer)
-        net.set_option(moe.MOE_OPT_PATH, PATHS[args.path])
+        net.set_option(moe.MOE_OPT_PATH, PATHS[path])
         nets.append(net)
         if not sweep or i == 0:
             xs.append(W.make_x(s, T, seed, wl.x_kind, device=dev))
@@ -617,9 +615,6 @@ def run_ours(args):
     torch.cuda.synchronize()
     stream = torch.cuda.Stream(device=dev)
     layers_per_step = L if sweep else 1
-    K = args.steps if args.steps is not None else max(1, 32000 // (T * layers_per_step))
-    K = max(1, K)
-    Wm = max(3, args.warmup)
 
     def step(i):
         if sweep:
@@ -636,18 +631,20 @@ def run_ours(args):
             step(i)
     stream.synchronize()
 
-    # graphs: one of L steps (one per instance) and one of the remainder
-    def capture(n):
+    def capture(n, first=0):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
+            for i in range(first, first + n):
                 step(i)
         return g
 
-    per_graph = 1 if sweep else L
-    full, rem = divmod(K, per_graph)
-    g_full = capture(per_graph) if full else None
-    g_rem = capture(rem) if rem else None
+    # the K timed steps: whole graphs of up to `chunk` steps (a multiple of
+    # the rotation), then the remainder; K <= chunk is one graph
+    per_rot = 1 if sweep else L
+    chunk = max(per_rot, (max(1, 4096 // (launches_hint(T) * layers_per_step)) // per_rot) * per_rot)
+    full, rem = divmod(K, chunk)
+    g_full = capture(chunk) if full else None
+    g_rem = capture(rem, full * chunk) if rem else None
     with torch.cuda.stream(stream):
         if g_full:
             g_full.replay()
@@ -658,12 +655,14 @@ def run_ours(args):
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     if sampler:
         sampler.mark_start()
+    warm_gpu(stream)
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(full):
@@ -677,11 +676,14 @@ def run_ours(args):
     torch.cuda.synchronize()
     ms = reduce_max(e0.elapsed_time(e1), dev)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     clocks = sampler.finish() if sampler else None
     value = rows_per_second(world, K, T * layers_per_step, ms / 1e3)
+    # spread per step: replays of one rotation's graph after the timed region
     try:
-        quantiles = replay_quantiles(g_full, stream, per_graph, full)
+        g_q = capture(per_rot)
+        quantiles = replay_quantiles(g_q, stream, per_rot, max(3, min(200, 4000 // per_rot)))
     except Exception as e:  # reported, never fatal to the line
         quantiles = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
 
@@ -734,29 +736,21 @@ def run_ours(args):
                          "peak_kind": peak_kind + (" (bf16 x 2 for fp8)" if sf[0] == "fp8" else "")})
     lb = layer_bytes(s, T, U)
     step_ms = ms / K / layers_per_step  # per layer
-
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": Wm, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-        "config": {"workload": wl.name, "rows": T, "hidden": s.hidden, "experts": s.n_experts,
-                   "top_k": s.top_k, "inter": s.inter, "shared_inter": s.shared_inter,
-                   "activations": "bf16", "expert_weights": "e4m3, fp32 128x128 block scales",
-                   "layer_instances": L,
-                   "layers_per_step": layers_per_step,
-                   "l2": (f"{L} chained layers, {L * lb / 2**30:.1f} GiB touched per step"
-                          if sweep else
-                          f"weights rotate over {L} layer instances "
-                          f"({L * lb / 2**30:.1f} GiB touched per rotation)") + " > 129 MB L2",
-                   "timing": "CUDA graphs of whole steps, CUDA events on the launch stream",
-                   "kernel_path": args.path,
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+    out = {
+        "value": value, "ms_per_step": ms / K, "steps": K, "warmup": Wm,
+        "layer_instances": L, "layers_per_step": layers_per_step,
+        "l2": (f"{L} chained layers, {L * lb / 2**30:.1f} GiB touched per step"
+               if sweep else
+               f"weights rotate over {L} layer instances "
+               f"({L * lb / 2**30:.1f} GiB touched per rotation)") + " > 129 MB L2",
         "roofline": roof,
         "layer_roofline": {"bound": "hbm", "algorithmic_bytes_per_step": lb,
                            "achieved": lb / (step_ms * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
                            "frac": lb / (step_ms * 1e-3) / 1e9 / hbm,
                            "distinct_experts": U,
-                           "fp8_tflops": fp8_flops(s, T) / (step_ms * 1e-3) / 1e12},
+                           "fp8_tflops": fp8_flops(s, T) / (step_ms * 1e-3) / 1e12,
+                           "fp8_frac": fp8_flops(s, T) / (step_ms * 1e-3) / 1e12
+                           / (2.0 * bf16_tf)},
         "stages_us": {n: round(v * 1e3, 3) for n, v in stage_prof.items()},
         "step_ms_quantiles": quantiles,
         "gpu_launches": K * launches_per_step * layers_per_step,
@@ -766,7 +760,7 @@ def run_ours(args):
     # end to end through the C ABI with host buffers (copies inside the timed region)
     xh = [x.cpu().pin_memory() for x in xs]
     yh = [torch.empty_like(v).pin_memory() for v in xh]
-    Ke = min(K, 2000)
+    Ke = max(1, min(K, e2e_steps))
 
     def e2e_step(i):
         if sweep:  # one copy in, the layers on the device, one copy out
@@ -788,15 +782,90 @@ def run_ours(args):
     for i in range(Ke):
         e2e_step(i)
     et = reduce_max(time.perf_counter() - t0, dev)
-    line["e2e"] = {"value": rows_per_second(world, Ke, T * layers_per_step, et), "unit": UNIT,
-                   "h2d_bytes_per_step": T * s.hidden * 2, "d2h_bytes_per_step": T * s.hidden * 2,
-                   "steps": Ke,
-                   "api": "moe_forward per layer, host copies per step" if sweep
-                   else "moe_forward_host"}
+    out["e2e"] = {"value": rows_per_second(world, Ke, T * layers_per_step, et), "unit": UNIT,
+                  "h2d_bytes_per_step": T * s.hidden * 2, "d2h_bytes_per_step": T * s.hidden * 2,
+                  "steps": Ke,
+                  "api": "moe_forward per layer, host copies per step" if sweep
+                  else "moe_forward_host"}
+    out["_host"] = (W.to_numpy_layer(layers[0]), W.bf16_bits(xs[0]))
+    for net in nets:
+        net.close()
+    del nets, xs, ys, layers
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def launches_hint(T: int) -> int:
+    """Kernel launches of one forward of T rows (graph size bound only)."""
+    return 1 if T <= 5 else (3 if T <= 16 else 12)
+
+
+# prompt legs reported beside the one-row headline: (workload, steps, instances)
+PROMPT_LEGS = (("prompt_t1024", 50, 2), ("prompt_t16384", 20, 1))
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import block_fp8_mixture_router_gb300 as moe
+    import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from block_fp8_mixture_router_gb300.build import build
+    build()
+    moe.load_library()
+
+    wl = W.WORKLOADS[args.workload]
+    s = wl.shape
+    T = args.rows if args.rows else wl.rows
+    layers_per_step = wl.layers if wl.layers > 1 else 1
+    K = args.steps if args.steps is not None else max(1, 32000 // (T * layers_per_step))
+    K = max(1, K)
+    Wm = max(3, args.warmup)
+    r = measure_layer(moe, W, wl, T, K, Wm, max(1, args.instances), args.path, dev, rank, world)
+    host, xb = r.pop("_host")
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": Wm, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": wl.name, "rows": T, "hidden": s.hidden, "experts": s.n_experts,
+                   "top_k": s.top_k, "inter": s.inter, "shared_inter": s.shared_inter,
+                   "activations": "bf16", "expert_weights": "e4m3, fp32 128x128 block scales",
+                   "layer_instances": r["layer_instances"],
+                   "layers_per_step": r["layers_per_step"], "l2": r["l2"],
+                   "timing": "CUDA graphs of whole steps, CUDA events on the launch stream",
+                   "kernel_path": args.path,
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+    }
+    for key in ("roofline", "layer_roofline", "stages_us", "step_ms_quantiles", "gpu_launches",
+                "clocks", "e2e"):
+        line[key] = r[key]
+
+    # the prompt path beside the one-row headline: its own legs, each with
+    # its own roofline (FP8 tensor roof where the flops bind), stages and e2e
+    if args.workload == "decode_t1" and not args.rows and not args.no_prompt:
+        legs = {}
+        for name, steps, inst in PROMPT_LEGS:
+            pw = W.WORKLOADS[name]
+            try:
+                pr = measure_layer(moe, W, pw, pw.rows, steps, Wm, inst, "auto", dev, rank,
+                                   world, e2e_steps=20)
+                pr.pop("_host")
+                pr["workload"] = name
+                pr["rows"] = pw.rows
+                pr["unit"] = UNIT
+                legs[name] = pr
+            except Exception as e:  # reported, never fatal to the headline
+                legs[name] = {"unavailable": f"{type(e).__name__}: {e}"[:300]}
+        line["prompt"] = legs
 
     if rank == 0 and world == 1:
-        host = W.to_numpy_layer(layers[0])
-        xb = W.bf16_bits(xs[0])
         v, n = cpu_baseline(host, xb, args.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"{n} single-row passes of layer instance 0 "
@@ -815,8 +884,6 @@ def run_ours(args):
                 line["cpu_baseline_all_cores"] = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    for net in nets:
-        net.close()
     if world > 1:
         dist.destroy_process_group()
 

@@ -36,7 +36,8 @@ PATH_DECODE_ROWS = 6  # the role-split multi-row decode kernel for 2..16 rows
 EXPORTED = ("moe_create", "moe_load_weights", "moe_forward", "moe_forward_host", "moe_route",
             "moe_quantize", "moe_expert_activations", "moe_set_option", "moe_required_bytes",
             "moe_last_device_status", "moe_destroy", "moe_status_string",
-            "moe_profile_forward", "moe_route_static", "moe_add_rmsnorm_quantize")
+            "moe_profile_forward", "moe_route_static", "moe_add_rmsnorm_quantize",
+            "moe_forward_codes")
 
 MOE_ROUTE_STATIC_MAX_LOGITS = 262144
 
@@ -82,6 +83,7 @@ def load_library(path: str = LIB_PATH):
                                            vp]
     L.moe_route_static.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
     L.moe_expert_activations.argtypes = [vp, i, vp, vp, vp]
+    L.moe_forward_codes.argtypes = [vp, i, vp, vp, vp]
     L.moe_set_option.argtypes = [vp, i, i]
     L.moe_profile_forward.argtypes = [vp, vp, vp, i, vp, vp, i, ctypes.POINTER(ctypes.c_int), vp]
     L.moe_required_bytes.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(ctypes.c_size_t)]
@@ -164,6 +166,11 @@ def moe_add_rmsnorm_quantize(ctx, residual, x, gamma, eps: float, rows: int, h_o
 
 def moe_expert_activations(ctx, rows: int, hq, sh, stream=None) -> int:
     return load_library().moe_expert_activations(ctx, rows, _ptr(hq), _ptr(sh), _stream(stream))
+
+
+def moe_forward_codes(ctx, rows: int, codes, scales, stream=None) -> int:
+    return load_library().moe_forward_codes(ctx, rows, _ptr(codes), _ptr(scales),
+                                            _stream(stream))
 
 
 def moe_profile_forward(ctx, x, y, rows: int, stream=None, capacity: int = 16):
@@ -313,6 +320,16 @@ class MoELayer:
         sh = torch.empty((rows, k, I // 128), dtype=torch.float32, device=dev)
         _check(moe_expert_activations(self.ctx, rows, hq, sh, stream), "moe_expert_activations")
         return hq, sh
+
+    def forward_codes(self, rows: int, stream=None):
+        """The e4m3 codes and group scales of x that the experts of the most
+        recent forward read: ([rows, k, H] uint8, [rows, k, H/128] fp32)."""
+        k, H = self.shape.top_k, self.shape.hidden
+        dev = torch.device("cuda", self.device)
+        codes = torch.empty((rows, k, H), dtype=torch.uint8, device=dev)
+        scales = torch.empty((rows, k, H // 128), dtype=torch.float32, device=dev)
+        _check(moe_forward_codes(self.ctx, rows, codes, scales, stream), "moe_forward_codes")
+        return codes, scales
 
     def profile(self, x: torch.Tensor, y: torch.Tensor, stream=None):
         rc, stages = moe_profile_forward(self.ctx, x, y, x.shape[0], stream)

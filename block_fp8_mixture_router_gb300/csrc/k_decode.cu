@@ -57,10 +57,12 @@ __device__ void decode_schedule(const KArgs& a) {
   for (int e = threadIdx.x; e < kMaxExperts; e += blockDim.x) s_tok[e] = 0u;
   __threadfence_block();
   __syncthreads();
+  // an index outside [0, E) (possible only after a wait gave up and the
+  // status flag is set) joins no expert's rows
   for (int p = threadIdx.x; p < T * k; p += blockDim.x) {
     const int e = a.w.idx[p];
     s_idx[p] = e;
-    atomicOr(&s_tok[e], 1u << (p / k));
+    if (e >= 0 && e < E) atomicOr(&s_tok[e], 1u << (p / k));
   }
   __syncthreads();
   const int e = threadIdx.x;
@@ -76,7 +78,7 @@ __device__ void decode_schedule(const KArgs& a) {
       const int t = __ffs(m) - 1;
       m &= m - 1;
       int j = 0;
-      while (s_idx[t * k + j] != e) ++j;
+      while (j < k - 1 && s_idx[t * k + j] != e) ++j;
       const int p = t * k + j, slot = slot0 + r;
       a.w.pair_of_slot[slot] = p;
       a.w.slot_of_pair[p] = slot;

@@ -505,4 +505,31 @@ cudaError_t launch_gather_hq(const KArgs& a, uint8_t* hq, float* sh, cudaStream_
   return cudaGetLastError();
 }
 
+// The e4m3 codes and group scales of x that each (row, rank) pair's expert
+// read in the most recent forward: from the row-major workspace copy (decode
+// kernels, warp-MMA prompt kernels) or from the pair's slot of the
+// slot-ordered operand of the tcgen05 gate/up GEMM.
+__global__ void k_gather_codes(KArgs a, const uint8_t* xg, const float* sxg, int slot_order,
+                               uint8_t* codes, float* scales) {
+  const int p = blockIdx.x;  // pair t*k + j
+  const int t = p / a.d.k;
+  const int H = a.d.H, nbh = H / kGroup;
+  const uint8_t* src = a.w.xq + (size_t)t * H;
+  const float* ssrc = a.w.sx + (size_t)t * nbh;
+  if (slot_order) {
+    const int slot = a.w.slot_of_pair[p];
+    src = xg + (size_t)slot * H;
+    ssrc = sxg + (size_t)slot * nbh;
+  }
+  for (int i = threadIdx.x; i < H; i += blockDim.x) codes[(size_t)p * H + i] = src[i];
+  for (int i = threadIdx.x; i < nbh; i += blockDim.x) scales[(size_t)p * nbh + i] = ssrc[i];
+}
+
+cudaError_t launch_gather_codes(const KArgs& a, const uint8_t* xg, const float* sxg,
+                                bool slot_order, uint8_t* codes, float* scales, cudaStream_t s) {
+  if (a.d.T * a.d.k == 0) return cudaSuccess;
+  k_gather_codes<<<a.d.T * a.d.k, 256, 0, s>>>(a, xg, sxg, slot_order ? 1 : 0, codes, scales);
+  return cudaGetLastError();
+}
+
 }  // namespace moe

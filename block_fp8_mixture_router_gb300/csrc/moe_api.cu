@@ -49,6 +49,10 @@ struct moe_ctx {
   // joined back into the caller's stream within each forward
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  // the most recent forward, for moe_forward_codes: its rows (0 = none, or a
+  // later call rewrote the workspace) and where its x codes live
+  int fwd_rows = 0;
+  bool fwd_slot_order = false;
 };
 
 namespace {
@@ -412,6 +416,8 @@ cudaError_t launch_topk_after_router(const KArgs& a, const moe_ctx* c, const TcG
 int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
                 StageRec* rec = nullptr) {
   KArgs a = make_args(c, x, y, T);
+  c->fwd_rows = T;
+  c->fwd_slot_order = use_tc(c, T);
   const int grid = 2 * c->sm_count;
   if (use_decode(c, T) && use_row(c, T)) {
     LAUNCH(launch_decode_row(a, c->sm_count, c->row_smem, c->opt_pdl != 0, s), "decode_row");
@@ -759,6 +765,7 @@ int moe_route(moe_ctx* c, const void* x, int rows, int32_t* idx, float* w, void*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   c->last_stream = s;
   KArgs a = make_args(c, x, nullptr, rows);
+  c->fwd_rows = 0;  // the routing kernels rewrite the workspace's codes
   int rc = run_router_and_quant(c, a, s);
   if (rc) return rc;
   const size_t n = (size_t)rows * c->cfg.top_k;
@@ -781,6 +788,7 @@ int moe_quantize(moe_ctx* c, const void* x, int rows, uint8_t* codes, float* sca
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   c->last_stream = s;
   KArgs a = make_args(c, x, nullptr, rows);
+  c->fwd_rows = 0;  // rewrites the workspace's codes
   if (launch_quant_gamma(a, s) != cudaSuccess) return MOE_ERR_CUDA;
   const size_t H = c->cfg.hidden;
   if (cudaMemcpyAsync(codes, c->w.xq, rows * H, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
@@ -845,6 +853,19 @@ int moe_expert_activations(moe_ctx* c, int rows, uint8_t* hq, float* sh, void* s
   if (!guard.ok) return MOE_ERR_CUDA;
   KArgs a = make_args(c, nullptr, nullptr, rows);
   return check_launch(launch_gather_hq(a, hq, sh, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_forward_codes(moe_ctx* c, int rows, uint8_t* codes, float* scales, void* stream) {
+  if (!c || rows < 0) return MOE_ERR_INVALID_ARG;
+  if (rows > c->cfg.max_rows) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!c->loaded) return MOE_ERR_NOT_LOADED;
+  if (rows == 0) return MOE_OK;
+  if (!codes || !scales || rows != c->fwd_rows) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  KArgs a = make_args(c, nullptr, nullptr, rows);
+  return check_launch(launch_gather_codes(a, c->xg, c->sxg, c->fwd_slot_order, codes, scales,
+                                          static_cast<cudaStream_t>(stream)));
 }
 
 int moe_profile_forward(moe_ctx* c, const void* x, void* y, int rows, float* stage_ms,

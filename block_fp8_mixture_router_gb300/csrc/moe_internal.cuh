@@ -145,6 +145,8 @@ cudaError_t launch_split_router(const float* wr, bf16* out, int E, int Epad, int
 bool make_tc_map(CUtensorMap* m, bool bf16_elems, const void* ptr, uint64_t rows, uint64_t cols,
                  uint32_t box_rows);
 cudaError_t launch_gather_hq(const KArgs& a, uint8_t* hq, float* sh, cudaStream_t s);
+cudaError_t launch_gather_codes(const KArgs& a, const uint8_t* xg, const float* sxg,
+                                bool slot_order, uint8_t* codes, float* scales, cudaStream_t s);
 
 // Decode path (rows <= kDecodeRows): three kernels chained with programmatic
 // dependent launch when `pdl` is set.

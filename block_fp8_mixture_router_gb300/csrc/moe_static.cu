@@ -6,7 +6,9 @@
 // section "What it adds" (the router) and section "Fidelity against the
 // PyTorch oracle" (near-tied 8th/9th experts).  The call is a library
 // convenience; the pages define no such entry point.
-#include <atomic>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "moe_internal.cuh"
 
@@ -17,21 +19,55 @@ namespace {
 static __device__ __align__(256) float g_route_scratch[MOE_ROUTE_STATIC_MAX_LOGITS];
 
 constexpr int kMaxDevices = 64;
-std::atomic<float*> g_scratch_addr[kMaxDevices];
 
-// Address of this device's copy of the scratch, looked up once per device.
+// The scratch's device address per device ordinal, with the context it was
+// looked up in: after a device reset the primary context is new, the library's
+// device code is loaded again (possibly elsewhere), and the address is looked
+// up again.
+struct ScratchAddr {
+  CUcontext ctx = nullptr;
+  float* ptr = nullptr;
+};
+ScratchAddr g_scratch[kMaxDevices];
+std::mutex g_scratch_mu;
+
+PFN_cuCtxGetCurrent_v4000 ctx_getter() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// Address of this device's copy of the scratch, looked up once per device
+// and context.  With no context current on the calling thread yet, the
+// look-up itself makes the device's primary context current.
 int scratch_for(int device, float** out) {
   if (device < 0 || device >= kMaxDevices) return MOE_ERR_UNSUPPORTED_SHAPE;
-  float* p = g_scratch_addr[device].load(std::memory_order_acquire);
-  if (!p) {
+  const PFN_cuCtxGetCurrent_v4000 get_ctx = ctx_getter();
+  CUcontext ctx = nullptr;
+  if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  ScratchAddr& e = g_scratch[device];
+  if (!ctx || e.ctx != ctx || !e.ptr) {
+    float* p = nullptr;
     if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_route_scratch) != cudaSuccess ||
         !p) {
       cudaGetLastError();
       return MOE_ERR_CUDA;
     }
-    g_scratch_addr[device].store(p, std::memory_order_release);
+    if (!ctx && (get_ctx(&ctx) != CUDA_SUCCESS || !ctx)) return MOE_ERR_CUDA;
+    e.ctx = ctx;
+    e.ptr = p;
   }
-  *out = p;
+  *out = e.ptr;
   return MOE_OK;
 }
 

@@ -96,13 +96,23 @@ typedef struct {
  * workspace for cfg->max_rows rows.  Refuses unsupported shapes
  * (MOE_ERR_UNSUPPORTED_SHAPE) and sizes above the cap (MOE_ERR_ALLOC_LIMIT)
  * before allocating anything.  On success *out owns everything; on failure
- * *out is NULL and nothing is left allocated.  Synchronous. */
+ * *out is NULL and nothing is left allocated.  Synchronous.
+ * Defined by: PR #939 "drama3: Fish Audio Drama 3 text to speech on one CUDA
+ * GPU", section "What it adds" (config.zig checks every number the kernels
+ * assume and refuses any other checkpoint shape); PR #925 "drama: load the
+ * checkpoint with direct I/O in file order and build the codec on its own
+ * thread", conversation, the allocation-cap commit (setAllocationLimit: a
+ * refused allocation leaves usage unchanged). */
 int moe_create(const moe_config* cfg, int device, moe_ctx** out);
 
 /* Copy one layer's weights into the context (layout described in
  * moe_weights).  pointers_on_device = 1: device pointers; 0: host pointers
  * (pageable or pinned).  Checks the block scales are finite and positive;
- * returns after the copies have completed (synchronous on `stream`). */
+ * returns after the copies have completed (synchronous on `stream`).
+ * Defined by: PR #925 "drama: load the checkpoint with direct I/O in file
+ * order and build the codec on its own thread", conversation, commit "the
+ * Drama 3 text backbone on CUDA" (weights load as stored; nothing is
+ * requantized). */
 int moe_load_weights(moe_ctx* ctx, const moe_weights* w, int pointers_on_device, void* stream);
 
 /* y = MoE(x).  x: bf16 [rows][H] on the device; y: bf16 [rows][H] on the
@@ -111,16 +121,28 @@ int moe_load_weights(moe_ctx* ctx, const moe_weights* w, int pointers_on_device,
  * nothing.  Asynchronous on `stream`: no allocation, no host synchronisation,
  * expert counts stay on the device.  Results are bitwise identical from run
  * to run for the same inputs.  Device-side faults of earlier work surface as
- * MOE_ERR_CUDA on a later call. */
+ * MOE_ERR_CUDA on a later call.
+ * Defined by: PR #939 "drama3: Fish Audio Drama 3 text to speech on one CUDA
+ * GPU", sections "Precision" (per-row, per-128 e4m3 inputs, amax / 448) and
+ * "What it adds" (the prompt pass and the frame step); the commits "the Drama
+ * 3 text backbone on CUDA" (256-expert top-8 block-FP8 MoE with a gated shared
+ * expert), "one SwiGLU launch for the routed and shared experts" and "MoE
+ * combine on 8-wide vectors". */
 int moe_forward(moe_ctx* ctx, const void* x, void* y, int rows, void* stream);
 
 /* The same layer with x and y in host memory: copies x to the device, runs
  * moe_forward, copies y back and synchronises `stream` before returning.
- * Pinned host buffers give the fastest copies. */
+ * Pinned host buffers give the fastest copies.
+ * Defined by: the layer of moe_forward (PR #939 "drama3: Fish Audio Drama 3
+ * text to speech on one CUDA GPU", section "Precision"). */
 int moe_forward_host(moe_ctx* ctx, const void* x_host, void* y_host, int rows, void* stream);
 
 /* Router only (same kernels as moe_forward): idx int32 [rows][k] in rank
- * order and w fp32 [rows][k], both device pointers.  Asynchronous. */
+ * order and w fp32 [rows][k], both device pointers.  Asynchronous.
+ * Defined by: PR #939 "drama3: Fish Audio Drama 3 text to speech on one CUDA
+ * GPU", section "What it adds" (the router) and section "Fidelity against the
+ * PyTorch oracle" (8th and 9th experts 6e-5 apart or exactly tied: a tie rule
+ * is needed; here the lower expert wins). */
 int moe_route(moe_ctx* ctx, const void* x, int rows, int32_t* idx, float* w, void* stream);
 
 /* Router without a context, for callers that must not allocate device
@@ -142,10 +164,17 @@ int moe_route(moe_ctx* ctx, const void* x, int rows, int32_t* idx, float* w, voi
  * that limit returns MOE_ERR_UNSUPPORTED_SHAPE (256 experts: up to 1024 rows
  * per call) before anything is launched.  Nothing in the scratch has to start
  * at zero: every logit a call reads was written by the same call.
- *   - Nothing is allocated, by this library or by a library it calls.
- *   - The first call on each device looks up the scratch's address once
- *     (cudaGetSymbolAddress); make that first call before any stream capture
- *     starts.
+ *   - The call makes no cudaMalloc or cudaFree call and calls no allocating
+ *     library routine.
+ *   - The first call on each device looks up the scratch's address
+ *     (cudaGetSymbolAddress).  Under CUDA's lazy module loading (the default
+ *     since CUDA 12.2) that look-up, or the first launch, can make the driver
+ *     load this library's device code and the scratch array, which takes
+ *     device memory once.  Make that first call during set-up, before any
+ *     stream capture starts and before the caller's memory pool claims the
+ *     device; later calls allocate nothing.
+ *   - The address is cached per device and per CUDA context: after a device
+ *     reset the next call looks it up again.
  *   - All calls on one device share the scratch: two calls whose work can
  *     overlap on the device (other streams, other host threads) race and give
  *     wrong results.  Order them on one stream, or with events.
@@ -155,9 +184,16 @@ int moe_route(moe_ctx* ctx, const void* x, int rows, int32_t* idx, float* w, voi
 int moe_route_static(const void* x, const float* router, int rows, int hidden, int n_experts,
                      int top_k, int32_t* idx, float* w, void* stream);
 
-/* Activation quantisation only (same kernel as moe_forward): codes e4m3
- * [rows][H] and scales fp32 [rows][H/128], both device pointers.
- * Asynchronous. */
+/* Activation quantisation only: codes e4m3 [rows][H] and scales fp32
+ * [rows][H/128], both device pointers.  Asynchronous.  This launches the
+ * row quantisation kernel of the warp-MMA prompt path; every forward kernel
+ * quantises with the same device routines (group scale, then codes), but the
+ * codes a forward actually fed its experts are read back with
+ * moe_forward_codes.
+ * Defined by: PR #939 "drama3: Fish Audio Drama 3 text to speech on one CUDA
+ * GPU", section "Precision" (e4m3 per row and per 128 inputs, amax / 448);
+ * commit "the Drama 3 text backbone on CUDA" (dynamic 1 x 128 FP8 activation
+ * quantization). */
 int moe_quantize(moe_ctx* ctx, const void* x, int rows, uint8_t* codes, float* scales,
                  void* stream);
 
@@ -177,7 +213,10 @@ int moe_quantize(moe_ctx* ctx, const void* x, int rows, uint8_t* codes, float* s
  * >= 0; a zero row with eps = 0 divides by zero (the output is NaN, as the
  * formula says).  Needs no loaded weights and no workspace, so rows is not
  * bounded by max_rows; hidden above 8192 returns MOE_ERR_UNSUPPORTED_SHAPE;
- * rows == 0 does nothing.  Asynchronous on `stream`. */
+ * rows == 0 does nothing.  Asynchronous on `stream`.
+ * Defined by: PR #925/#927 commit "add-norm fused with the routed experts'
+ * FP8 activation quantization"; PR #939 "drama3: Fish Audio Drama 3 text to
+ * speech on one CUDA GPU", section "Kernel contract" (plain-gamma RMS norm). */
 int moe_add_rmsnorm_quantize(moe_ctx* ctx, const void* residual, const void* x,
                              const void* gamma, float eps, int rows, void* h_out, void* xn_out,
                              uint8_t* codes, float* scales, void* stream);
@@ -185,8 +224,26 @@ int moe_add_rmsnorm_quantize(moe_ctx* ctx, const void* residual, const void* x,
 /* Expert-side intermediates of the most recent moe_forward, for checking:
  * hq e4m3 [rows][k][I] and sh fp32 [rows][k][I/128] (the re-quantised SwiGLU
  * rows fed to each selected expert's down projection, in rank order), device
- * pointers.  Asynchronous; call on the stream of that forward. */
+ * pointers.  Asynchronous; call on the stream of that forward.
+ * Defined by: commit "one SwiGLU launch for the routed and shared experts"
+ * (routed rows stored as their FP8 quantization); PR #939 "drama3: Fish Audio
+ * Drama 3 text to speech on one CUDA GPU", section "Precision". */
 int moe_expert_activations(moe_ctx* ctx, int rows, uint8_t* hq, float* sh, void* stream);
+
+/* The FP8 codes and group scales of x that the experts of the most recent
+ * moe_forward (or moe_forward_host) read: codes e4m3 [rows][k][H] and scales
+ * fp32 [rows][k][H/128], one copy per (row, rank) pair in rank order, device
+ * pointers.  The decode kernels quantise a row once for all its experts; the
+ * tcgen05 prompt kernels give each pair its own slot-ordered copy, and this
+ * call gathers every copy.  rows must equal that forward's rows, and no
+ * moe_route or moe_quantize may have run on the context since
+ * (MOE_ERR_INVALID_ARG otherwise).  Asynchronous; call on the stream of that
+ * forward.
+ * Defined by: PR #939 "drama3: Fish Audio Drama 3 text to speech on one CUDA
+ * GPU", section "Precision" (e4m3 per row and per 128 inputs, amax / 448);
+ * commit "the Drama 3 text backbone on CUDA" (dynamic 1 x 128 FP8 activation
+ * quantization). */
+int moe_forward_codes(moe_ctx* ctx, int rows, uint8_t* codes, float* scales, void* stream);
 
 /* Options.  MOE_OPT_PATH: 0 = automatic (rows <= 16 on the decode kernels:
  * the role-split one-row kernel for 1 row, the role-split multi-row kernel
@@ -202,7 +259,12 @@ int moe_expert_activations(moe_ctx* ctx, int rows, uint8_t* hq, float* sh, void*
  * without them 0, 1 and 6 take the chained kernels.
  * MOE_OPT_PDL: 1 = launch with programmatic dependent launch so a layer's
  * immutable weight reads overlap the previous kernel's tail (default), 0 =
- * plain launches. */
+ * plain launches.
+ * Defined by: PR #927 "drama: the backbone chain launches with programmatic
+ * dependent launch", section "What this changes" (the one-row GEMV prefetches
+ * immutable weights before its wait); PR #939 "drama3: Fish Audio Drama 3 text
+ * to speech on one CUDA GPU", section "What it adds" (the prompt pass and the
+ * frame step: every path computes the same layer). */
 enum { MOE_OPT_PATH = 1, MOE_OPT_PDL = 2 };
 int moe_set_option(moe_ctx* ctx, int option, int value);
 
@@ -210,22 +272,37 @@ int moe_set_option(moe_ctx* ctx, int option, int value);
  * after every launch on `stream` and the call waits for them.  On return
  * stage_ms[i] is the device time of the i-th launch and stage_names[i] a
  * static name, for i < *n_stages (at most `capacity`).  Synchronous; for
- * measurement only (the events add small gaps between launches). */
+ * measurement only (the events add small gaps between launches).
+ * Defined by: PR #920 "drama: Drama 3 (fishaudio/drama-3) text-to-speech on
+ * CUDA", section "Receipt" (per-stage timings of the decode step,
+ * speed-stages.json). */
 int moe_profile_forward(moe_ctx* ctx, const void* x, void* y, int rows, float* stage_ms,
                         const char** stage_names, int capacity, int* n_stages, void* stream);
 
-/* Bytes moe_create would allocate for `cfg` (weights + workspace + staging). */
+/* Bytes moe_create would allocate for `cfg` (weights + workspace + staging).
+ * Defined by: PR #925 "drama: load the checkpoint with direct I/O in file
+ * order and build the codec on its own thread", conversation, the
+ * allocation-cap commit (setAllocationLimit: an engine admits a model against
+ * a memory budget). */
 int moe_required_bytes(const moe_config* cfg, size_t* bytes);
 
 /* Device-side status of the context: MOE_OK, or MOE_ERR_DEVICE_TIMEOUT if a
  * bounded wait in an earlier forward gave up.  Synchronises the context's
- * last stream.  Reading clears the flag. */
+ * last stream.  Reading clears the flag.
+ * Defined by: PR #939 "drama3: Fish Audio Drama 3 text to speech on one CUDA
+ * GPU", conversation, the follow-up fixes (a bad value is refused by name with
+ * an error, not trapped on). */
 int moe_last_device_status(moe_ctx* ctx);
 
-/* Release everything the context owns.  NULL is accepted. */
+/* Release everything the context owns.  NULL is accepted.
+ * Defined by: PR #925 "drama: load the checkpoint with direct I/O in file
+ * order and build the codec on its own thread", conversation (one worker
+ * thread owns the context, stream and modules and releases them). */
 void moe_destroy(moe_ctx* ctx);
 
-/* Static text for a status code. */
+/* Static text for a status code.
+ * Defined by: PR #939 "drama3: Fish Audio Drama 3 text to speech on one CUDA
+ * GPU", conversation, the follow-up fixes (errors refused by name). */
 const char* moe_status_string(int status);
 
 #ifdef __cplusplus

@@ -77,3 +77,81 @@ def check_output(y_gpu_bits: np.ndarray, y_ref: np.ndarray, rows_mask=None):
 def bits(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> uint16 numpy bits (host)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+# ---- the oracle over several host threads ------------------------------------
+
+def oracle_rows(host: dict, xb: np.ndarray, threads: int | None = None, **kw):
+    """oracle.moe_rows on the rows of xb, split over host threads (the oracle
+    is C behind ctypes, which releases the GIL during each call; its only
+    mutable state is a table built before the threads start).  Returns one
+    OracleResult whose arrays are the per-chunk results concatenated in row
+    order, exactly as one call over all rows would give them."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    T = xb.shape[0]
+    if threads is None:
+        try:
+            threads = len(os.sched_getaffinity(0))
+        except (AttributeError, OSError):
+            threads = os.cpu_count() or 1
+    threads = max(1, min(threads, T))
+    if threads == 1:
+        return oracle.moe_rows(host, xb, **kw)
+    oracle.moe_rows(host, xb[:1], **kw)  # builds the e4m3 table before the threads start
+    bounds = np.linspace(0, T, threads + 1).astype(int)
+    parts = [(int(a), int(b)) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+    with ThreadPoolExecutor(max_workers=len(parts)) as ex:
+        res = list(ex.map(lambda ab: oracle.moe_rows(host, xb[ab[0]:ab[1]], **kw), parts))
+    trace = None
+    if res[0].trace is not None:
+        trace = {n: np.concatenate([r.trace[n] for r in res], axis=0) for n in res[0].trace}
+    return oracle.OracleResult(np.concatenate([r.y_bf16 for r in res], axis=0),
+                               np.concatenate([r.y_ref for r in res], axis=0), trace)
+
+
+# ---- FP8 codes read back from the forward ------------------------------------
+
+def check_forward_codes(codes: np.ndarray, scales: np.ndarray, ref_xq: np.ndarray,
+                        ref_sx: np.ndarray):
+    """The codes and group scales every (row, rank) pair's expert read in the
+    forward ([T, k, H] and [T, k, H/128]) equal the oracle's quantisation of
+    the row, bit for bit, for every rank's copy."""
+    T, k, H = codes.shape
+    assert ref_xq.shape == (T, H) and ref_sx.shape == (T, scales.shape[2])
+    for j in range(k):
+        bad = np.nonzero(np.any(codes[:, j] != ref_xq, axis=1))[0]
+        assert bad.size == 0, f"rank {j}: codes differ in rows {bad[:8].tolist()}"
+        bad = np.nonzero(np.any(scales[:, j].view(np.uint32) != ref_sx.view(np.uint32), axis=1))[0]
+        assert bad.size == 0, f"rank {j}: scales differ in rows {bad[:8].tolist()}"
+
+
+def e4m3_steps(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Distance in e4m3 code steps between two code arrays (the codes are
+    sign-magnitude and the magnitude field is monotonic in the value)."""
+    def ordered(c):
+        c = c.astype(np.int32)
+        mag = c & 0x7F
+        return np.where(c & 0x80, -mag, mag)
+    return np.abs(ordered(a) - ordered(b))
+
+
+def hq_agreement(hq: np.ndarray, sh: np.ndarray, ref_hq: np.ndarray, ref_sh: np.ndarray,
+                 rows_mask=None):
+    """Agreement of the re-quantised SwiGLU rows with the oracle's: (fraction of
+    identical codes, largest code-step distance in groups whose scale agrees
+    bit for bit, fraction of groups whose scale agrees).  These codes depend
+    on the fp32 accumulation order of the gate/up sums, so they are reported
+    and held to a bar, not bit-exact."""
+    if rows_mask is not None:
+        hq, sh, ref_hq, ref_sh = hq[rows_mask], sh[rows_mask], ref_hq[rows_mask], ref_sh[rows_mask]
+    if hq.size == 0:
+        return 1.0, 0, 1.0
+    same = float(np.mean(hq == ref_hq))
+    G = hq.shape[-1] // sh.shape[-1]
+    s_ok = sh.view(np.uint32) == ref_sh.view(np.uint32)
+    steps = e4m3_steps(hq, ref_hq).reshape(*sh.shape, G)
+    max_step = int(steps[s_ok].max()) if s_ok.any() else 0
+    return same, max_step, float(np.mean(s_ok))

@@ -104,3 +104,31 @@ def test_struct_layouts_match_the_header(tmp_path):
         assert c_layout[(st, "size")] == ctypes.sizeof(cls), st
         for n in fields[st]:
             assert c_layout[(st, n)] == getattr(cls, n).offset, (st, n)
+
+
+def _declaration_comments():
+    """(function name, the comment block right above its declaration) for
+    every function include/moe.h declares."""
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    out = {}
+    for m in re.finditer(r"/\*((?:(?!\*/).)*)\*/\s*(?:enum\s*\{[^}]*\};\s*)?(?:#define [^\n]*\n\s*)?"
+                         r"(?:int|void|const char\*)\s+(moe_[a-z_]+)\s*\(", src, flags=re.S):
+        out[m.group(2)] = m.group(1)
+    return out
+
+
+def test_every_declaration_cites_its_defining_passage():
+    """Each entry point's comment names the passage of the pages that defines
+    the operation; the allocation-free router says the pages have no
+    counterpart instead."""
+    comments = _declaration_comments()
+    assert set(comments) == set(declared_functions())
+    for name, text in comments.items():
+        flat = " ".join(text.split())
+        if name == "moe_route_static":
+            assert "no counterpart" in flat, name
+            assert "Defined by:" not in flat, name
+            continue
+        assert "Defined by:" in flat, name
+        cited = flat.split("Defined by:", 1)[1]
+        assert re.search(r'(PR #9\d\d|commit ")', cited), (name, cited)

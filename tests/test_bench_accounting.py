@@ -35,15 +35,35 @@ def test_fp8_flops():
 
 
 def test_stage_bytes_cover_every_timed_stage():
-    """Every stage name a forward can report has a byte count."""
+    """Every stage name a forward can report has a byte count; the stages
+    that only read and write workspace (top-k, schedule) have none."""
     s = W.FULL
     sb = bench.stage_bytes(s, 1024, 173.3)
     for name in ("decode_row", "decode_rows", "decode_layer", "route_decode", "gateup_decode",
-                 "down_combine_decode", "router_tc", "topk", "schedule", "quant_scatter",
+                 "down_combine_decode", "router_tc", "quant_scatter",
                  "shared_gateup_tc", "gateup_tc", "shared_down_tc", "down_tc", "combine"):
         assert name in sb and sb[name] > 0, name
+    assert sb["topk"] == 0 and sb["schedule"] == 0
     # the whole-layer kernels move the layer's bytes
     assert sb["decode_row"] == bench.layer_bytes(s, 1024, 173.3)
+
+
+def test_expert_gemm_stages_count_weights_only():
+    """The routed GEMMs' algorithmic bytes are the touched experts' weights and
+    block scales: the gathered codes, the SwiGLU rows and the expert outputs
+    they also move are workspace traffic."""
+    s = W.FULL
+    U = 200
+    sb = bench.stage_bytes(s, 1024, U)
+    assert sb["gateup_tc"] == U * (2 * 512 * 2048 + 4 * 8 * 16)
+    assert sb["down_tc"] == U * (2048 * 512 + 4 * 16 * 4)
+    assert sb["shared_down_tc"] == 2 * 2048 * 512
+    # weights + layer input bytes + layer output bytes over all stages of the
+    # tcgen05 forward = the layer's bytes
+    tc = ("router_tc", "quant_scatter", "shared_gateup_tc", "gateup_tc", "shared_down_tc",
+          "down_tc", "combine")
+    x_reads = 3 * 2 * 1024 * 2048  # router, quantisation and the shared gate/up read x
+    assert sum(sb[n] for n in tc) - x_reads + 2 * 1024 * 2048 == bench.layer_bytes(s, 1024, U)
 
 
 def test_rows_per_second_is_whole_job():
@@ -166,3 +186,20 @@ def test_reference_arm_addnorm():
 
 def test_reference_arm_other_ranks_print_nothing():
     assert _reference_line("--steps", "1", env_extra={"RANK": "1", "WORLD_SIZE": "2"}) == []
+
+
+def test_threaded_oracle_rows_equal_one_call():
+    """The parity tests' multi-threaded oracle helper returns exactly what one
+    call over all rows returns (outputs and every trace array)."""
+    import numpy as np
+
+    import oracle
+    from parity import oracle_rows
+    L = W.to_numpy_layer(W.make_layer(W.TINY, 5))
+    xb = W.bf16_bits(W.make_x(W.TINY, 13, 5))
+    one = oracle.moe_rows(L, xb, trace=True)
+    many = oracle_rows(L, xb, threads=4, trace=True)
+    assert np.array_equal(one.y_bf16, many.y_bf16)
+    assert np.array_equal(one.y_ref, many.y_ref)
+    for n in one.trace:
+        assert np.array_equal(one.trace[n], many.trace[n]), n

@@ -7,7 +7,8 @@ import torch
 
 import oracle
 import workloads as W
-from parity import bits, check_output, check_topk
+from parity import (bits, check_forward_codes, check_output, check_topk, hq_agreement,
+                    oracle_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -49,15 +50,33 @@ class Case:
         return W.make_x(self.shape, rows, self.seed, self.wl.x_kind, device="cuda", tag=tag)
 
 
-def run_and_check(case: Case, x: torch.Tensor, sample_rows=None, path=m.PATH_AUTO):
+# bar for the re-quantised SwiGLU codes (order-dependent, so not bit-exact):
+# at least this fraction identical, and within one e4m3 step wherever the
+# group scale agrees
+HQ_SAME_MIN = 0.98
+HQ_MAX_STEP = 1
+
+
+def run_and_check(case: Case, x: torch.Tensor, sample_rows=None, path=m.PATH_AUTO,
+                  threads=None):
+    """One forward on `path`, then every check against the oracle on the
+    sampled rows (all rows by default): the FP8 codes and scales of x that the
+    forward's experts read (read back from the forward itself, every rank's
+    copy, bit-exact), the routing (bit-exact outside near ties), the routing
+    weights, the re-quantised SwiGLU codes (held to a bar) and y."""
     case.moe.set_option(m.MOE_OPT_PATH, path)
+    T = x.shape[0]
     y = case.moe.forward(x)
+    fcodes, fscales = case.moe.forward_codes(T)
+    hq, sh = case.moe.expert_activations(T)
     idx, w = case.moe.route(x)
     codes, scales = case.moe.quantize(x)
     torch.cuda.synchronize()
-    rows = np.arange(x.shape[0]) if sample_rows is None else np.asarray(sample_rows)
+    rows = np.arange(T) if sample_rows is None else np.asarray(sample_rows)
     xb = bits(x)[rows]
-    ref = oracle.moe_rows(case.host, xb, trace=True)
+    ref = oracle_rows(case.host, xb, threads=threads, trace=True)
+    check_forward_codes(fcodes.cpu().numpy()[rows], fscales.cpu().numpy()[rows],
+                        ref.trace["xq"], ref.trace["sx"])
     near, differ = check_topk(idx.cpu().numpy()[rows], ref.trace["logits"], case.shape.top_k)
     assert differ.sum() <= max(1, 0.02 * rows.size), f"{differ.sum()} rows routed differently"
     exact = ~differ
@@ -65,6 +84,9 @@ def run_and_check(case: Case, x: torch.Tensor, sample_rows=None, path=m.PATH_AUT
     assert np.array_equal(scales.cpu().numpy()[rows], ref.trace["sx"])
     wg = w.cpu().numpy()[rows]
     assert np.allclose(wg[exact], ref.trace["w"][exact], rtol=2e-5, atol=1e-7)
+    same, step, s_ok = hq_agreement(hq.cpu().numpy()[rows], sh.cpu().numpy()[rows],
+                                    ref.trace["hq"], ref.trace["sh"], rows_mask=exact)
+    assert same >= HQ_SAME_MIN and step <= HQ_MAX_STEP, (same, step, s_ok)
     rel, mx = check_output(bits(y)[rows], ref.y_ref, rows_mask=exact)
     return y, ref, rel, mx
 
@@ -75,11 +97,7 @@ def run_and_check(case: Case, x: torch.Tensor, sample_rows=None, path=m.PATH_AUT
 def test_tiny_layer(dev, rows):
     case = Case(W.WORKLOADS["tiny_t4"], 64, dev)
     x = case.x(rows)
-    _, ref, rel, mx = run_and_check(case, x)
-    # intermediates: re-quantised SwiGLU codes mostly identical (not gated by the bar)
-    hq, sh = case.moe.expert_activations(rows)
-    same = np.mean(hq.cpu().numpy() == ref.trace["hq"])
-    assert same > 0.98, same
+    run_and_check(case, x)
 
 
 @pytest.mark.parametrize("path", [m.PATH_AUTO, m.PATH_PROMPT, m.PATH_DECODE_CHAINED])
@@ -294,15 +312,47 @@ def test_prompt_t1024_sampled(dev):
     idx, _ = case.moe.route(x)
     counts = np.bincount(idx.cpu().numpy().ravel(), minlength=256)
     assert counts.max() > 100 and (counts == 0).sum() >= 1, counts
-    sample = sorted(set([0, 1, 511, 1022, 1023] + list(range(7, 1024, 97))))
+    # every one of the 1024 rows against the oracle (over all host cores)
+    run_and_check(case, x)
+    case.moe.close()
+
+
+def _rows_covering_every_expert(idx: np.ndarray, n: int) -> list:
+    """At least one row for every expert some row selected (the first such
+    row), then evenly spaced rows up to n in all."""
+    first = {}
+    for t, row in enumerate(idx):
+        for e in row:
+            first.setdefault(int(e), t)
+    rows = set(first.values())
+    T = idx.shape[0]
+    spread = [int(t) for t in np.linspace(0, T - 1, n).astype(int)]
+    spread += [int(t) for t in np.random.default_rng(0).permutation(T)]
+    for t in spread:
+        if len(rows) >= n:
+            break
+        rows.add(t)
+    return sorted(rows)
+
+
+def test_prompt_t16384_sampled(dev):
+    """The compute-bound prompt shape (16384 rows, about 512 rows per expert):
+    rows covering every selected expert, plus evenly spaced ones, at least 512
+    in all, against the oracle."""
+    wl = W.WORKLOADS["prompt_t16384"]
+    case = Case(wl, 16384, dev)
+    x = case.x(16384)
+    idx, _ = case.moe.route(x)
+    torch.cuda.synchronize()
+    gi = idx.cpu().numpy()
+    counts = np.bincount(gi.ravel(), minlength=256)
+    assert counts.max() > 1000, counts.max()
+    sample = _rows_covering_every_expert(gi, 512)
+    assert len(sample) >= 512
+    covered = set(gi[sample].ravel().tolist())
+    assert covered == set(np.nonzero(counts)[0].tolist())
     run_and_check(case, x, sample_rows=sample)
-    # every row's codes and scales, bit-exact, against the oracle's quantiser
-    codes, scales = case.moe.quantize(x)
-    xb = bits(x)
-    xf = torch.from_numpy(xb.view(np.int16).copy()).view(torch.bfloat16).float().numpy()
-    for r in range(0, 1024, 64):
-        c, s = oracle.quant_row(xf[r])
-        assert np.array_equal(codes[r].cpu().numpy(), c) and np.array_equal(scales[r].cpu().numpy(), s)
+    case.moe.close()
 
 
 def test_repeat_bitwise(full_case):
