@@ -29,8 +29,12 @@ MOE_ERR_DEVICE_TIMEOUT = -6
 
 MOE_OPT_PATH = 1
 MOE_OPT_PDL = 2
+MOE_OPT_POLL_LIMIT = 3
+MOE_OPT_LAUNCH_EPOCH = 4
+MOE_OPT_BATCH_INVARIANT = 5
+MOE_OPT_ROUTER_BF16 = 6
+TAG_WRAP = 0x7FFFFFFF
 PATH_AUTO, PATH_DECODE, PATH_PROMPT, PATH_DECODE_CHAINED, PATH_PROMPT_MMA = 0, 1, 2, 3, 4
-PATH_DECODE_MULTIROW = 5  # the persistent multi-row decode kernel with a grid barrier
 PATH_DECODE_ROWS = 6  # the role-split multi-row decode kernel for 2..16 rows
 
 EXPORTED = ("moe_create", "moe_load_weights", "moe_forward", "moe_forward_host", "moe_route",

@@ -10,6 +10,7 @@ namespace dec {
 
 constexpr long long kSpin = 1ll << 22;  // tries before a wait gives up
 
+
 __device__ __forceinline__ uint32_t sa(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -75,13 +76,24 @@ __device__ __forceinline__ void st_relaxed64(unsigned long long* p, unsigned lon
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
 }
 
-// The value of a tagged word once its tag is current (bounded).
+// Tries before a poll gives up: kSpin unless the context set a limit in
+// status[kPollLimitWord] (copy waits keep kSpin, so a launch never leaves a
+// copy in flight).
+__device__ __forceinline__ long long poll_limit(const int* status) {
+  const int lim = *reinterpret_cast<const volatile int*>(status + kPollLimitWord);
+  return lim > 0 ? (long long)lim : kSpin;
+}
+
+// The value of a tagged word once its tag is current (bounded).  On giving
+// up it sets the status flag and returns whatever value the word holds.
 __device__ __forceinline__ float poll_tagged(const unsigned long long* p, unsigned long long tag,
                                              int* status) {
   unsigned long long v = ld_relaxed64(p);
+  if ((v & 0xFFFFFFFF00000000ull) == tag) return __uint_as_float((uint32_t)v);
+  const long long lim = poll_limit(status);
   long long it = 0;
   while ((v & 0xFFFFFFFF00000000ull) != tag) {
-    if (++it > kSpin) {
+    if (++it > lim) {
       atomicExch(status, 1);
       break;
     }
@@ -146,6 +158,58 @@ __device__ __forceinline__ void poll_gather(int n, unsigned long long tag, int* 
 
 __device__ __forceinline__ void publish(unsigned long long* p, unsigned long long tag, float v) {
   st_relaxed64(p, tag | __float_as_uint(v));
+}
+
+// ---- launch tags ---------------------------------------------------------------
+// A launch's tag is the context's epoch + 1; the last CTA to leave publishes
+// the tag as the new epoch.  A poll accepts a word whose tag equals its
+// launch's, so a tag must never come back while a word written under it
+// could still be read.  On the launch whose tag reaches kTagWrap the last CTA
+// instead clears every exchange word and restarts the epoch at 0: tags then
+// start again at 1 over words that all read 0.  Every CTA of that launch
+// fences its exchange writes before it arrives at the exit counter, so none
+// can land after the clear.
+// Exchange words of the context (tagged logits, then the decode exchange
+// words), as the context allocates them.
+__device__ __forceinline__ void clear_exchange_words(const KArgs& a) {
+  const size_t n_log = (size_t)kDecodeRows * a.d.E;
+  const size_t n_xw = (size_t)kDecodeRows * ((size_t)a.d.k * a.d.I + (size_t)a.d.k * a.d.H +
+                                             a.d.Is + a.d.H);
+  for (size_t i = threadIdx.x; i < n_log; i += blockDim.x) a.w.tlog[i] = 0ull;
+  for (size_t i = threadIdx.x; i < n_xw; i += blockDim.x) a.w.xw[i] = 0ull;
+}
+
+// The exit of a tagged-exchange launch; every thread of the CTA calls it.
+__device__ __forceinline__ void launch_exit(const KArgs& a, int tag) {
+  int* bar_exit = a.w.done + 3;
+  int* epoch = a.w.done + 4;
+  __shared__ int s_last;
+  __syncthreads();
+  if (tag < kTagWrap) {
+    // The next launch reads the epoch, the outputs and the exchange words
+    // only after this grid has completed, and stale words carry older tags.
+    if (threadIdx.x == 0) {
+      const int old = atomicAdd(bar_exit, 1);
+      if (old == (int)gridDim.x - 1) {
+        *bar_exit = 0;
+        *epoch = tag;
+      }
+    }
+    return;
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();  // release: this CTA's exchange writes before its arrival
+    s_last = atomicAdd(bar_exit, 1) == (int)gridDim.x - 1;
+    __threadfence();  // acquire: every other CTA's writes before the clear
+  }
+  __syncthreads();
+  if (!s_last) return;
+  clear_exchange_words(a);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    *bar_exit = 0;
+    *epoch = 0;
+  }
 }
 
 __device__ __forceinline__ uint4 lds16(const void* p) { return *reinterpret_cast<const uint4*>(p); }

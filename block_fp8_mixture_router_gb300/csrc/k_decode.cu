@@ -139,7 +139,8 @@ __global__ void __launch_bounds__(32 * kRtWarps) k_route_decode(KArgs a) {
       }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) s_lg[e] = __ldcg(a.w.logits + (size_t)t * E + e);
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+      s_lg[e] = route_logit(__ldcg(a.w.logits + (size_t)t * E + e), a.d.rbf16);
     __syncthreads();
     // the top-k on the first 8 warps (named barrier), the rest wait below
     if (k <= 8 && E <= 256) {

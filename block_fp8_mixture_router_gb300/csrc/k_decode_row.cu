@@ -220,8 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
   const Roles R = make_roles(G, H, k, I, Is);
   const Lay L = make_lay(smem, R, H, E, I, Is);
   Small* sm = L.sm;
-  int* bar_exit = a.w.done + 3;
-  int* epoch = a.w.done + 4;
+  const int* epoch = a.w.done + 4;
   int* status = a.w.status;
   const Xw X = xw_of(a.w.xw, k, H, I, Is);
   const bool is_routed = b < R.nR;
@@ -361,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     // ---- routed: gather the logits, top-k, then this CTA's expert slice ----
     const int r = b / R.P, p = b % R.P;
     for (int e = threadIdx.x; e < E; e += kThreads)
-      L.lg[e] = poll_tagged(a.w.tlog + e, tag, status);
+      L.lg[e] = route_logit(poll_tagged(a.w.tlog + e, tag, status), a.d.rbf16);
     __syncthreads();
     // the top-k on the first 8 warps (the others wait at the barrier below)
     if (k <= 8 && E <= 256) {
@@ -595,18 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     }
   }
 
-  // ---- exit: the last CTA advances the launch tag ----
-  // No fence is needed: the next launch reads the tag, the outputs and the
-  // exchange words only after this grid has completed (its dependency wait
-  // or stream order), and stale exchange words carry an older tag.
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int old = atomicAdd(bar_exit, 1);
-    if (old == G - 1) {
-      *bar_exit = 0;
-      *epoch = sm->tag;
-    }
-  }
+  // ---- exit: the last CTA advances the launch tag (or clears the words) ----
+  launch_exit(a, sm->tag);
 }
 
 }  // namespace

@@ -206,8 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_rows(KArgs a) {
   const Roles R = rows_roles(G, H, Is);
   const Lay L = rows_lay(smem, H);
   Small* sm = L.sm;
-  int* bar_exit = a.w.done + 3;
-  int* epoch = a.w.done + 4;
+  const int* epoch = a.w.done + 4;
   int* status = a.w.status;
   const Xw X = rows_xw(a.w.xw, k, H, I, Is);
   const bool is_routed = b < R.nR;
@@ -409,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_rows(KArgs a) {
     for (int e = threadIdx.x; e < kMaxExperts; e += kThreads) sm->tok[e] = 0u;
     __syncthreads();
     for (int t = warp; t < T; t += kW)
-      topk_row(lg + (size_t)t * E, E, k, sm->idx + t * k, sm->w + t * k);
+      topk_row(lg + (size_t)t * E, E, k, sm->idx + t * k, sm->w + t * k, a.d.rbf16);
     __syncthreads();
     for (int p = threadIdx.x; p < T * k; p += kThreads)
       atomicOr(&sm->tok[sm->idx[p]], 1u << (p / k));
@@ -847,18 +846,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_rows(KArgs a) {
     }
   }
 
-  // ---- exit: the last CTA advances the launch tag ----
-  // No fence is needed: the next launch reads the tag, the outputs and the
-  // exchange words only after this grid has completed, and stale exchange
-  // words carry an older tag.
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int old = atomicAdd(bar_exit, 1);
-    if (old == G - 1) {
-      *bar_exit = 0;
-      *epoch = sm->tag;
-    }
-  }
+  // ---- exit: the last CTA advances the launch tag (or clears the words) ----
+  launch_exit(a, sm->tag);
 }
 
 }  // namespace

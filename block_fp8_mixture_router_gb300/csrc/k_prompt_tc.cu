@@ -9,23 +9,26 @@
 //
 // Operands are swapped relative to the usual token-by-weight product: a tile
 // is 128 output features (M, the weight rows, always full) by up to 64
-// (block-FP8) or 128 (bf16) tokens (N, rounded up to 16), so experts that see few rows waste no tensor
-// work on padding rows, and one 128-feature tile is exactly one row of weight
+// (block-FP8) or 128 (bf16) tokens (N, rounded up to 16), so experts that see
+// few rows waste no tensor work on padding rows, and one 128-feature tile is
+// exactly one row of weight
 // scale blocks.  For every 128-deep K block the MMAs write a fresh partial
-// into one of two TMEM buffers; the epilogue warps read it back, multiply by
-// (weight block scale x activation scale of each token) and accumulate in
-// registers while the tensor cores fill the other buffer.  The bf16 shared
-// expert needs no per-block scaling and accumulates across K in TMEM.
+// into one of up to four TMEM buffers (Cfg::kNumBuf); the epilogue warps read
+// it back, multiply by (weight block scale x activation scale of each token)
+// and accumulate in registers while the tensor cores fill the next buffers.
+// The bf16 shared expert needs no per-block scaling and accumulates across K
+// in TMEM.
 //
 // A gate tile and its up tile share the token operand and land in the same
 // TMEM lanes, so the thread that owns feature j holds both halves of SwiGLU
 // for it.  The tile's outputs are transposed through shared memory and
 // stored token-major with coalesced 128/256-byte rows.
 //
-// CTA roles (576 threads): warp 0 lane 0 issues TMA, warp 1 owns TMEM and
-// lane 0 issues the MMAs, warps 2-17 are the epilogue (warp w reads TMEM
-// lanes 32*(w%4).. and column quarter (w-2)/4 of the tile's tokens).  Every wait is bounded; a wait that
-// gives up sets the status flag and all roles leave their loops.
+// CTA roles (kTcThreads = 320 threads): warp 0 lane 0 issues TMA, warp 1 owns
+// TMEM and lane 0 issues the MMAs, warps 2-9 are the epilogue (warp w reads
+// TMEM lanes 32*(w%4).. and column half (w-2)/4 of the tile's tokens).  Every
+// wait is bounded; a wait that gives up sets the status flag and all roles
+// leave their loops.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -57,9 +60,8 @@ struct Cfg {
   static constexpr bool kPair = kSwiGLU || kKind == kTcRoutedDown;
   static constexpr bool kRouted = kF8;
   // Tokens per tile (N).  The block-FP8 kinds keep their promoted
-  // accumulators in registers (gate and up: 2 x kN/4 per epilogue thread,
-  // within the ~100 registers a thread has at 18 warps per CTA); the bf16
-  // kinds accumulate in TMEM.
+  // accumulators in registers (gate and up: 2 x kCols per epilogue thread);
+  // the bf16 kinds accumulate in TMEM.
   static constexpr int kN = kF8 ? 64 : 128;
   static constexpr int kCols = kN / (kEpiWarps / 4);  // token columns per epilogue thread
   // TMEM accumulator buffers (gate at +0, up at +kN) and their count

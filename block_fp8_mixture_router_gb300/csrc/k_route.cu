@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(256) k_topk(KArgs a) {
   pdl_wait();
   pdl_trigger();
   topk_row(a.w.logits + (size_t)t * a.d.E, a.d.E, a.d.k, a.w.idx + (size_t)t * a.d.k,
-           a.w.wts + (size_t)t * a.d.k);
+           a.w.wts + (size_t)t * a.d.k, a.d.rbf16);
 }
 
 cudaError_t launch_topk(const KArgs& a, cudaStream_t s, bool pdl) {
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(256) k_topk_splits(KArgs a, const float* __res
     if (e < E) row[e] = acc[i];
   }
   __syncwarp();
-  topk_row(row, E, a.d.k, a.w.idx + (size_t)t * a.d.k, a.w.wts + (size_t)t * a.d.k);
+  topk_row(row, E, a.d.k, a.w.idx + (size_t)t * a.d.k, a.w.wts + (size_t)t * a.d.k, a.d.rbf16);
 }
 
 cudaError_t launch_topk_splits(const KArgs& a, const float* part, int ks, cudaStream_t s,

@@ -26,10 +26,11 @@ struct moe_ctx {
   bool loaded = false;
   int opt_path = 0;
   int opt_pdl = 1;
-  int dec_grid = 0;        // persistent decode kernel: CTAs (one per SM), 0 = unavailable
+  int opt_poll_limit = 0;  // status[kPollLimitWord]; 0 = the kernels' default
+  int opt_invariant = 0;   // batch-invariant rows: the grouped kernels for every T
+  int opt_router_bf16 = 0; // route on logits rounded to bf16
   size_t row_smem = 0;     // one-row decode kernel: shared memory per CTA, 0 = unavailable
   size_t rows_smem = 0;    // 2..16-row decode kernel: shared memory per CTA, 0 = unavailable
-  size_t dec_optin = 0;    // shared memory a CTA may use
   cudaStream_t last_stream = nullptr;
   std::vector<void*> allocs;
   DevLayer L{};
@@ -94,10 +95,17 @@ struct Plan {
   }
 };
 
+// K splits of the tensor-core router in batch-invariant mode, whatever the
+// row count: a row's logits are then the same partial sums added in the same
+// order at every T.
+constexpr int kInvariantSplits = 4;
+
 // Rows (splits x rows) of the router's partial-logit buffer: up to 16 splits
-// while splits x rows stays within 16384.
+// while splits x rows stays within 16384, and always kInvariantSplits splits
+// of max_rows.
 size_t router_part_rows(const moe_config* c) {
-  return std::min<size_t>(16384, 16 * (size_t)c->max_rows);
+  return std::max<size_t>(std::min<size_t>(16384, 16 * (size_t)c->max_rows),
+                          (size_t)kInvariantSplits * c->max_rows);
 }
 
 // K splits of the tensor-core router for T rows: enough items to give every
@@ -174,7 +182,8 @@ int check_launch(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUD
 
 KArgs make_args(moe_ctx* c, const void* x, void* y, int T) {
   KArgs a;
-  a.d = Dims{T, c->cfg.hidden, c->cfg.n_experts, c->cfg.top_k, c->cfg.inter, c->cfg.shared_inter};
+  a.d = Dims{T, c->cfg.hidden, c->cfg.n_experts, c->cfg.top_k, c->cfg.inter, c->cfg.shared_inter,
+             c->opt_router_bf16, c->cfg.act_group == c->cfg.hidden ? 1 : 0};
   a.L = c->L;
   a.w = c->w;
   a.x = static_cast<const bf16*>(x);
@@ -191,12 +200,10 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 bool use_decode(const moe_ctx* c, int T);
 bool use_row(const moe_ctx* c, int T);
 bool use_rows(const moe_ctx* c, int T);
-bool use_fused(const moe_ctx* c, int T);
 bool use_tc(const moe_ctx* c, int T);
 bool router_args(const moe_ctx* c, const void* x, int T, TcGemm* rt, int* grid);
 cudaError_t launch_topk_after_router(const KArgs& a, const moe_ctx* c, const TcGemm& rt,
                                      cudaStream_t s, bool pdl);
-cudaError_t launch_fused(moe_ctx* c, const KArgs& a, cudaStream_t s);
 
 // Routing with the kernels the forward of T rows would use (the persistent
 // decode kernel routes inside the layer: run the layer into the staging
@@ -215,11 +222,6 @@ int run_router_and_quant(moe_ctx* c, const KArgs& a, cudaStream_t s) {
     return launch_decode_rows(b, c->sm_count, c->rows_smem, c->opt_pdl != 0, s) == cudaSuccess
                ? MOE_OK
                : MOE_ERR_CUDA;
-  }
-  if (use_decode(c, a.d.T) && use_fused(c, a.d.T)) {
-    KArgs b = a;
-    b.y = c->stage_y;
-    return launch_fused(c, b, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
   if (use_decode(c, a.d.T))
     return launch_route_decode(a, c->opt_pdl != 0, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -260,20 +262,8 @@ struct StageRec {
 
 // The decode kernels serve rows <= kDecodeRows for hidden sizes up to 4096.
 bool use_decode(const moe_ctx* c, int T) {
-  if (c->opt_path == 2 || c->opt_path == 4) return false;
+  if (c->opt_path == 2 || c->opt_path == 4 || c->opt_invariant) return false;
   return T <= kDecodeRows && c->cfg.hidden <= 4096;
-}
-
-// The persistent decode kernel unless the chained decode kernels are asked for.
-// Stages and shared memory of the persistent decode kernel for T rows: as
-// many stages as the per-CTA opt-in shared memory holds.
-int decode_plan(const moe_ctx* c, int T, size_t* smem) {
-  const int H = c->cfg.hidden, E = c->cfg.n_experts;
-  const int n = decode_layer_stages(T, H, E, c->dec_optin);
-  if (n < 2 || !decode_layer_fits(T, H, E, c->cfg.top_k, c->cfg.inter, c->cfg.shared_inter, n))
-    return 0;
-  *smem = decode_layer_smem(T, H, E, n);
-  return n;
 }
 
 // One row on the role-split one-row kernel unless another decode kernel is
@@ -291,18 +281,6 @@ constexpr int kRowsAuto = 5;
 bool use_rows(const moe_ctx* c, int T) {
   if (T < 2 || T > kDecodeRows || c->rows_smem <= 0) return false;
   return c->opt_path == 6 || ((c->opt_path == 0 || c->opt_path == 1) && T <= kRowsAuto);
-}
-
-// The persistent multi-row kernel only when asked for.
-bool use_fused(const moe_ctx* c, int T) {
-  size_t smem = 0;
-  return c->opt_path == 5 && c->dec_grid > 0 && decode_plan(c, T, &smem) >= 2;
-}
-
-cudaError_t launch_fused(moe_ctx* c, const KArgs& a, cudaStream_t s) {
-  size_t smem = 0;
-  const int n = decode_plan(c, a.d.T, &smem);
-  return launch_decode_layer(a, c->dec_grid, n, smem, c->opt_pdl != 0, s);
 }
 
 // Tensor maps and launch arguments of the four tcgen05 GEMMs.  The weight
@@ -401,7 +379,8 @@ bool router_args(const moe_ctx* c, const void* x, int T, TcGemm* rt, int* grid) 
   *rt = c->tc[kTcRouter];
   if (!make_tc_map(&rt->b, true, x, (uint64_t)T, (uint64_t)c->cfg.hidden, 16)) return false;
   rt->T = T;
-  rt->ksplit = router_splits(c->sm_count, T, rt->n_f, rt->n_k, c->part_rows);
+  rt->ksplit = c->opt_invariant ? std::min(kInvariantSplits, rt->n_k)
+                                : router_splits(c->sm_count, T, rt->n_f, rt->n_k, c->part_rows);
   rt->outf = rt->ksplit > 1 ? c->logits_part : c->w.logits;
   *grid = std::min(c->sm_count, (T + 127) / 128 * rt->n_f * rt->ksplit);
   return true;
@@ -425,10 +404,6 @@ int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
   }
   if (use_decode(c, T) && use_rows(c, T)) {
     LAUNCH(launch_decode_rows(a, c->sm_count, c->rows_smem, c->opt_pdl != 0, s), "decode_rows");
-    return MOE_OK;
-  }
-  if (use_decode(c, T) && use_fused(c, T)) {
-    LAUNCH(launch_fused(c, a, s), "decode_layer");
     return MOE_OK;
   }
   if (use_decode(c, T)) {
@@ -617,22 +592,12 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     delete c;
     return MOE_ERR_CUDA;
   }
-  // persistent decode kernel: one CTA per SM must fit at the largest row count
+  // role-split decode kernels: one CTA per SM, roles fixed by the shape
   {
-    int optin = 0, per_sm = 0;
+    int optin = 0;
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) ==
         cudaSuccess) {
-      const int H = cfg->hidden, E = cfg->n_experts;
-      const int nst = decode_layer_stages(kDecodeRows, H, E, (size_t)optin);
-      const size_t smem = decode_layer_smem(kDecodeRows, H, E, nst);
-      // launches size their shared memory per row count, up to the opt-in limit
-      if (nst >= 2 && setup_decode_layer((size_t)optin) == cudaSuccess &&
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel(), 256, smem) ==
-              cudaSuccess &&
-          per_sm >= 1 && 2 * c->sm_count >= E && cfg->hidden <= 2048) {
-        c->dec_grid = c->sm_count;
-        c->dec_optin = (size_t)optin;
-      }
+      const int E = cfg->n_experts;
       // one-row kernel: every SM one CTA, roles fixed by the shape
       const size_t rs = decode_row_smem(c->sm_count, cfg->hidden, E, cfg->top_k, cfg->inter,
                                         cfg->shared_inter);
@@ -915,13 +880,38 @@ int moe_set_option(moe_ctx* c, int option, int value) {
   if (!c) return MOE_ERR_INVALID_ARG;
   switch (option) {
     case MOE_OPT_PATH:
-      if (value < 0 || value > 6) return MOE_ERR_INVALID_ARG;
+      // 5 named a persistent multi-row decode kernel that no longer exists
+      if (value < 0 || value > 6 || value == 5) return MOE_ERR_INVALID_ARG;
       c->opt_path = value;
       return MOE_OK;
     case MOE_OPT_PDL:
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       c->opt_pdl = value;
       return MOE_OK;
+    case MOE_OPT_ROUTER_BF16:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      c->opt_router_bf16 = value;
+      return MOE_OK;
+    case MOE_OPT_BATCH_INVARIANT:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      c->opt_invariant = value;
+      return MOE_OK;
+    case MOE_OPT_POLL_LIMIT:
+    case MOE_OPT_LAUNCH_EPOCH: {
+      if (value < 0 || (option == MOE_OPT_LAUNCH_EPOCH && value >= kTagWrap))
+        return MOE_ERR_INVALID_ARG;
+      DeviceGuard guard(c->device);
+      if (!guard.ok) return MOE_ERR_CUDA;
+      // the word is read by launches on the context's stream: none may be in flight
+      int* word = option == MOE_OPT_POLL_LIMIT ? c->w.status + kPollLimitWord : c->w.done + 4;
+      if (cudaStreamSynchronize(c->last_stream) != cudaSuccess ||
+          cudaMemcpy(word, &value, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+      }
+      if (option == MOE_OPT_POLL_LIMIT) c->opt_poll_limit = value;
+      return MOE_OK;
+    }
     default:
       return MOE_ERR_INVALID_ARG;
   }
@@ -944,7 +934,10 @@ int moe_last_device_status(moe_ctx* c) {
     if (cudaMemset(c->w.status, 0, plan.sizes[29]) != cudaSuccess ||
         cudaMemset(c->w.gcount, 0, plan.sizes[25]) != cudaSuccess ||
         cudaMemset(c->w.tlog, 0, plan.sizes[32]) != cudaSuccess ||
-        cudaMemset(c->w.xw, 0, plan.sizes[39]) != cudaSuccess) {
+        cudaMemset(c->w.xw, 0, plan.sizes[39]) != cudaSuccess ||
+        (c->opt_poll_limit &&
+         cudaMemcpy(c->w.status + kPollLimitWord, &c->opt_poll_limit, sizeof(int),
+                    cudaMemcpyHostToDevice) != cudaSuccess)) {
       cudaGetLastError();
       return MOE_ERR_CUDA;
     }

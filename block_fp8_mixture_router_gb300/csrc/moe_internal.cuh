@@ -22,8 +22,19 @@ constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 16;
 constexpr int kDecodeRows = 16;   // rows at or below which the decode kernels run
 
+// Context status block (int words): [0] the device status flag, [1..12] the
+// kernels' barrier counters (DevWork::done), [13..14] unused,
+// [kPollLimitWord] tries before a poll of another CTA's exchange word gives
+// up (0 = the kernels' default; a checking option).
+constexpr int kPollLimitWord = 15;
+// The role-split decode kernels' launch tags run from 1 to kTagWrap; the
+// launch that reaches it clears the exchange words and restarts the epoch.
+constexpr int kTagWrap = 0x7FFFFFFF;
+
 struct Dims {
   int T, H, E, k, I, Is;
+  int rbf16;    // 1: route on logits rounded to bf16 (selection and softmax)
+  int per_row;  // 1: one activation scale per row of x and of each SwiGLU row
 };
 
 // Device copies of the weights (context-owned).
@@ -153,15 +164,6 @@ cudaError_t launch_gather_codes(const KArgs& a, const uint8_t* xg, const float* 
 cudaError_t launch_route_decode(const KArgs& a, bool pdl, cudaStream_t s);
 cudaError_t launch_gateup_decode(const KArgs& a, int grid, bool pdl, cudaStream_t s);
 cudaError_t launch_down_combine_decode(const KArgs& a, bool pdl, cudaStream_t s);
-
-// Decode path as one persistent kernel (one CTA per SM, grid barriers).
-size_t decode_layer_smem(int T, int H, int E, int n_stages);
-int decode_layer_stages(int T, int H, int E, size_t budget);
-bool decode_layer_fits(int T, int H, int E, int k, int I, int Is, int n_stages);
-cudaError_t setup_decode_layer(size_t max_smem);
-const void* decode_layer_kernel();
-cudaError_t launch_decode_layer(const KArgs& a, int grid, int n_stages, size_t smem, bool pdl,
-                                cudaStream_t s);
 
 // Launch `kernel` on `s`, allowing it to start before the previous kernel in
 // the stream completes when `pdl` is set (it must call griddepcontrol.wait

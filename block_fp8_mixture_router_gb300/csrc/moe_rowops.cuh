@@ -62,17 +62,24 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// The logit the router selects and weighs by: the fp32 sum, or in the
+// bf16-logit variant that sum rounded to bf16 (nearest, ties to even).
+__device__ __forceinline__ float route_logit(float v, int rbf16) {
+  return rbf16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+}
+
 // kCg: read the logits at L2 (they were written by other CTAs of the same
 // kernel).
+// rbf16: route on the logits rounded to bf16 (route_logit).
 template <bool kCg = false>
 __device__ __forceinline__ void topk_row(const float* logits, int E, int k, int* idx_out,
-                                         float* w_out) {
+                                         float* w_out, int rbf16 = 0) {
   const int lane = threadIdx.x & 31;
   uint32_t key[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
-    key[i] = e < E ? order_key(kCg ? __ldcg(logits + e) : logits[e]) : 0u;
+    key[i] = e < E ? order_key(route_logit(kCg ? __ldcg(logits + e) : logits[e], rbf16)) : 0u;
   }
   uint32_t my_key = 0u, my_e = 0u;
 #pragma unroll 1

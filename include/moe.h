@@ -253,19 +253,55 @@ int moe_forward_codes(moe_ctx* ctx, int rows, uint8_t* codes, float* scales, voi
  * chained decode kernels, 4 = always the grouped prompt kernels with
  * warp-level MMAs instead of tcgen05 (the path every forward takes when a
  * context's shape leaves no room for the tcgen05 kernels: hidden or inter
- * above 4096), 5 = rows <= 16 on the persistent multi-row decode kernel with
- * one grid barrier, 6 = 2..16 rows on the role-split multi-row kernel.  A
+ * above 4096), 6 = 2..16 rows on the role-split multi-row kernel (5 is not
+ * a path and returns MOE_ERR_INVALID_ARG).  A
  * role-split kernel needs the device to have enough SMs for its roles;
  * without them 0, 1 and 6 take the chained kernels.
  * MOE_OPT_PDL: 1 = launch with programmatic dependent launch so a layer's
  * immutable weight reads overlap the previous kernel's tail (default), 0 =
  * plain launches.
- * Defined by: PR #927 "drama: the backbone chain launches with programmatic
+ * MOE_OPT_BATCH_INVARIANT: 1 = a row's y is bit-identical whatever rows
+ * share its forward (any row count, any position): every row count runs on
+ * the grouped kernels (the decode kernels sum in other orders), and the
+ * router's K split is fixed (its partial sums are added in one order at
+ * every row count).  Costs the decode kernels' speed at 16 rows or fewer.
+ * 0 = off (default); MOE_OPT_PATH then chooses.
+ * MOE_OPT_ROUTER_BF16: 1 = route on the fp32 logits rounded to bf16
+ * (nearest, ties to even): the top-k, its tie rule (lower expert first) and
+ * the softmax over the selection all take the rounded values, as a router
+ * with bf16 logits does; exact ties between experts become common.  0 = fp32
+ * logits (default).  moe_route reports the routing of the variant in force.
+ * Checking options (they make the failure and wrap-around paths run; both
+ * wait for the context's last stream and write one device word):
+ * MOE_OPT_POLL_LIMIT: tries before a role-split decode kernel's poll of
+ * another CTA's result gives up and sets the status flag (0 = the built-in
+ * limit).  A small value makes a normal one-row forward give up: its output
+ * is then undefined, moe_last_device_status returns MOE_ERR_DEVICE_TIMEOUT
+ * and restarts the counters, and the next forward is exact again.  Waits for
+ * the kernel's own copies keep the built-in limit.
+ * MOE_OPT_LAUNCH_EPOCH: the launch epoch of the role-split decode kernels
+ * (0 <= value < 2^31 - 1).  Their exchange words carry the launch's tag,
+ * epoch + 1; the launch whose tag reaches 2^31 - 1 clears every word and
+ * restarts the epoch at 0, so a tag never comes back over a stale word.
+ * Defined by: PR #920 "drama: Drama 3 (fishaudio/drama-3) text-to-speech on
+ * CUDA", section "Receipt" (backbone outputs at chunk sizes 1, 7 and 128 are
+ * hash-identical) against PR #939, section "Determinism and request state"
+ * (prompt chunk seams fail) for MOE_OPT_BATCH_INVARIANT; PR #939, section
+ * "Fidelity against the PyTorch oracle" (the 8th and 9th experts tie exactly
+ * on bf16 logits) for MOE_OPT_ROUTER_BF16;
+ * PR #927 "drama: the backbone chain launches with programmatic
  * dependent launch", section "What this changes" (the one-row GEMV prefetches
  * immutable weights before its wait); PR #939 "drama3: Fish Audio Drama 3 text
  * to speech on one CUDA GPU", section "What it adds" (the prompt pass and the
  * frame step: every path computes the same layer). */
-enum { MOE_OPT_PATH = 1, MOE_OPT_PDL = 2 };
+enum {
+  MOE_OPT_PATH = 1,
+  MOE_OPT_PDL = 2,
+  MOE_OPT_POLL_LIMIT = 3,
+  MOE_OPT_LAUNCH_EPOCH = 4,
+  MOE_OPT_BATCH_INVARIANT = 5,
+  MOE_OPT_ROUTER_BF16 = 6
+};
 int moe_set_option(moe_ctx* ctx, int option, int value);
 
 /* One forward like moe_forward, timed per kernel: a CUDA event is recorded

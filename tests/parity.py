@@ -155,3 +155,68 @@ def hq_agreement(hq: np.ndarray, sh: np.ndarray, ref_hq: np.ndarray, ref_sh: np.
     steps = e4m3_steps(hq, ref_hq).reshape(*sh.shape, G)
     max_step = int(steps[s_ok].max()) if s_ok.any() else 0
     return same, max_step, float(np.mean(s_ok))
+
+
+# ---- the bf16-logit router variant ---------------------------------------------
+
+def _bf16_round(v32: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(v32, np.float32)).to(torch.bfloat16) \
+        .float().numpy()
+
+
+def bf16_route_alternatives(logits64: np.ndarray, rel_eps: float = 2.0 ** -14):
+    """The bf16 values the variant routes on, from the oracle's double logits
+    of one row ([E]): (b, alt) where b is the fp32-rounded logit rounded to
+    bf16 and alt[e] is the other bf16 neighbour when the fp32 logit lies
+    within rel_eps (relative) of the bf16 rounding midpoint between them,
+    else NaN.  The GPU sums the fp32 logit in another order, so an expert
+    whose fp32 logit sits that close to a midpoint may round either way."""
+    l32 = logits64.astype(np.float32)
+    b = _bf16_round(l32)
+    # the two bf16 neighbours around l32 and the midpoint between them
+    up = _bf16_round(np.nextafter(b, np.float32(np.inf)) + np.abs(b) * 2.0 ** -8)
+    dn = _bf16_round(np.nextafter(b, np.float32(-np.inf)) - np.abs(b) * 2.0 ** -8)
+    other = np.where(l32 >= b, up, dn)
+    mid = 0.5 * (b.astype(np.float64) + other.astype(np.float64))
+    near = np.abs(l32.astype(np.float64) - mid) <= rel_eps * np.abs(l32.astype(np.float64))
+    alt = np.where(near & (other != b), other, np.nan).astype(np.float32)
+    return b, alt
+
+
+def _order(vals: np.ndarray, k: int):
+    return [int(e) for e in np.lexsort((np.arange(vals.size), -vals.astype(np.float64)))[:k]]
+
+
+def check_topk_bf16(gpu_idx: np.ndarray, logits64: np.ndarray, k: int, max_alts: int = 8):
+    """The bf16-logit variant's ordered top-k, bit-exact (ties to the lower
+    expert) for every row whose decisive experts all round unambiguously to
+    bf16; a row with ambiguous experts must equal the order under one of the
+    roundings those experts allow.  Returns (ambiguous_rows, differing_rows)."""
+    T = gpu_idx.shape[0]
+    amb = np.zeros(T, bool)
+    differ = np.zeros(T, bool)
+    for t in range(T):
+        b, alt = bf16_route_alternatives(logits64[t])
+        ref = _order(b, k)
+        got = [int(v) for v in gpu_idx[t]]
+        # experts that can matter: any whose value, either way, reaches the
+        # (k+1)-th largest value
+        lo = np.sort(np.fmin(b, np.where(np.isnan(alt), b, alt)))[::-1][k]
+        cand = [e for e in np.nonzero(~np.isnan(alt))[0] if max(b[e], alt[e]) >= lo]
+        if not cand:
+            assert got == ref, (t, got, ref)
+            continue
+        amb[t] = True
+        assert len(cand) <= max_alts, (t, len(cand))
+        ok = False
+        for mask in range(1 << len(cand)):
+            v = b.copy()
+            for i, e in enumerate(cand):
+                if mask >> i & 1:
+                    v[e] = alt[e]
+            if _order(v, k) == got:
+                ok = True
+                break
+        assert ok, (t, got, ref, cand)
+        differ[t] = got != ref
+    return amb, differ

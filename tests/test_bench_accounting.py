@@ -39,7 +39,7 @@ def test_stage_bytes_cover_every_timed_stage():
     that only read and write workspace (top-k, schedule) have none."""
     s = W.FULL
     sb = bench.stage_bytes(s, 1024, 173.3)
-    for name in ("decode_row", "decode_rows", "decode_layer", "route_decode", "gateup_decode",
+    for name in ("decode_row", "decode_rows", "route_decode", "gateup_decode",
                  "down_combine_decode", "router_tc", "quant_scatter",
                  "shared_gateup_tc", "gateup_tc", "shared_down_tc", "down_tc", "combine"):
         assert name in sb and sb[name] > 0, name

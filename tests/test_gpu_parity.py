@@ -107,7 +107,7 @@ def test_tiny_layer_every_path(dev, path, rows):
     run_and_check(case, case.x(rows, tag=f"p{rows}"), path=path)
 
 
-@pytest.mark.parametrize("path", [m.PATH_PROMPT, m.PATH_DECODE_CHAINED, m.PATH_DECODE_MULTIROW])
+@pytest.mark.parametrize("path", [m.PATH_PROMPT, m.PATH_DECODE_CHAINED, m.PATH_DECODE_ROWS])
 def test_full_layer_other_paths(full_case, path):
     x = full_case.x(11, tag="paths")
     try:
@@ -171,7 +171,7 @@ def test_decode_t1_many_rows_one_by_one(full_case):
         run_and_check(full_case, x[r:r + 1].contiguous())
 
 
-@pytest.mark.parametrize("path", [m.PATH_DECODE_MULTIROW, m.PATH_DECODE_CHAINED, m.PATH_PROMPT])
+@pytest.mark.parametrize("path", [m.PATH_DECODE_ROWS, m.PATH_DECODE_CHAINED, m.PATH_PROMPT])
 def test_decode_t1_other_kernels(full_case, path):
     """One row on the multi-row decode kernel, the chained decode kernels and
     the prompt kernels (the automatic path takes the one-row kernel)."""
@@ -226,7 +226,7 @@ def tie_layer(dev):
     return layer, net, W.to_numpy_layer(layer)
 
 
-@pytest.mark.parametrize("rows,path", [(1, m.PATH_AUTO), (1, m.PATH_DECODE_MULTIROW),
+@pytest.mark.parametrize("rows,path", [(1, m.PATH_AUTO), (1, m.PATH_DECODE_ROWS),
                                        (1, m.PATH_DECODE_CHAINED), (3, m.PATH_AUTO),
                                        (8, m.PATH_AUTO), (8, m.PATH_DECODE_ROWS),
                                        (40, m.PATH_AUTO), (40, m.PATH_PROMPT_MMA)])
@@ -275,11 +275,11 @@ def t11_case(dev):
     return Case(W.WORKLOADS["decode_t11"], 64, dev)
 
 
-@pytest.mark.parametrize("path", [m.PATH_AUTO, m.PATH_DECODE_ROWS, m.PATH_DECODE_MULTIROW])
+@pytest.mark.parametrize("path", [m.PATH_AUTO, m.PATH_DECODE_ROWS, m.PATH_PROMPT])
 def test_decode_t11(t11_case, path):
     """Eleven rows with overlapping expert sets on the automatic path (the
-    chained decode kernels), the role-split multi-row kernel and the
-    persistent multi-row kernel."""
+    chained decode kernels), the role-split multi-row kernel and the grouped
+    tcgen05 kernels."""
     x = t11_case.x(11)
     try:
         run_and_check(t11_case, x, path=path)
@@ -294,6 +294,7 @@ def test_path_option_range(t11_case):
     assert t11_case.moe.ctx is not None
     assert m.moe_set_option(t11_case.moe.ctx, m.MOE_OPT_PATH, 7) == m.MOE_ERR_INVALID_ARG
     assert m.moe_set_option(t11_case.moe.ctx, m.MOE_OPT_PATH, -1) == m.MOE_ERR_INVALID_ARG
+    assert m.moe_set_option(t11_case.moe.ctx, m.MOE_OPT_PATH, 5) == m.MOE_ERR_INVALID_ARG
     assert m.moe_set_option(t11_case.moe.ctx, m.MOE_OPT_PATH, m.PATH_DECODE_ROWS) == m.MOE_OK
     assert m.moe_set_option(t11_case.moe.ctx, m.MOE_OPT_PATH, m.PATH_AUTO) == m.MOE_OK
 
