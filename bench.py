@@ -420,6 +420,135 @@ def reference_addnorm(args):
     print(json.dumps(line), flush=True)
 
 
+# ---- the layer taking the residual stream: fused add-norm vs two calls -------
+
+ADDNORM_LAYER_ROWS = {"addnorm_layer_t1": 1, "addnorm_layer_t11": 11,
+                      "addnorm_layer_t1024": 1024}
+
+
+def run_addnorm_layer(args):
+    """moe_forward_addnorm (the add-norm inside the layer's launches) against
+    moe_add_rmsnorm_quantize followed by moe_forward, on the same rotation of
+    layer instances; the line's value is the fused call's rows/s."""
+    import torch
+    import torch.distributed as dist
+
+    import block_fp8_mixture_router_gb300 as moe
+    import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from block_fp8_mixture_router_gb300.build import build
+    build()
+    moe.load_library()
+    s = W.FULL
+    H = s.hidden
+    T = args.rows if args.rows else ADDNORM_LAYER_ROWS[args.workload]
+    L = max(1, args.instances if T < 64 else 2)
+    shape = moe.LayerShape(s.hidden, s.n_experts, s.top_k, s.inter, s.shared_inter, s.group)
+    nets, ins, outs = [], [], []
+    for i in range(L):
+        seed = replica_seed(1 + 7919 * i, rank)
+        net = moe.MoELayer(shape, max_rows=max(T, 16), device=local)
+        net.load(W.make_layer(s, seed, device=dev))
+        nets.append(net)
+        r, x, g = (t.to(dev) for t in W.make_addnorm(s, T, replica_seed(5000 + i, rank)))
+        ins.append((r, x, g))
+        outs.append(tuple(torch.empty_like(x) for _ in range(3)) +
+                    (torch.empty((T, H), dtype=torch.uint8, device=dev),
+                     torch.empty((T, H // 128), dtype=torch.float32, device=dev)))
+    stream = torch.cuda.Stream(device=dev)
+
+    def fused(i):
+        j = i % L
+        r, x, g = ins[j]
+        h, xn, y, _, _ = outs[j]
+        rc = moe.moe_forward_addnorm(nets[j].ctx, r, x, g, W.NORM_EPS, T, h, None, y, stream)
+        if rc != moe.MOE_OK:
+            raise moe.MoEError(rc, "moe_forward_addnorm")
+
+    def separate(i):
+        j = i % L
+        r, x, g = ins[j]
+        h, xn, y, c, sc = outs[j]
+        rc = moe.moe_add_rmsnorm_quantize(nets[j].ctx, r, x, g, W.NORM_EPS, T, h, xn, c, sc,
+                                          stream)
+        if rc == moe.MOE_OK:
+            rc = moe.moe_forward(nets[j].ctx, xn, y, T, stream)
+        if rc != moe.MOE_OK:
+            raise moe.MoEError(rc, "add-norm then forward")
+
+    K = args.steps if args.steps is not None else max(L, 32000 // T)
+    Wm = max(3, args.warmup)
+    res = {}
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if sampler:
+        sampler.mark_start()
+    for name, fn in (("fused", fused), ("separate", separate)):
+        with torch.cuda.stream(stream):
+            for i in range(Wm):
+                fn(i)
+        stream.synchronize()
+        g_k = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_k, stream=stream):
+            for i in range(K):
+                fn(i)
+        g_warm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_warm, stream=stream):
+            for i in range(L):
+                fn(i)
+        with torch.cuda.stream(stream):
+            g_k.replay()
+        stream.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        warm_gpu(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, int(30e-3 / max(1e-6, 15e-6 * L * max(1, T // 16))))):
+                g_warm.replay()
+            e0.record(stream)
+            g_k.replay()
+            e1.record(stream)
+        e1.synchronize()
+        ms = reduce_max(e0.elapsed_time(e1), dev)
+        res[name] = {"value": rows_per_second(world, K, T, ms / 1e3), "ms_per_step": ms / K}
+    if sampler:
+        sampler.mark_end()
+    clocks = sampler.finish() if sampler else None
+    f, sp = res["fused"], res["separate"]
+    line = {
+        "metric": "MoE-layer rows/s (residual add + RMS norm + layer)", "value": f["value"],
+        "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": f["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "rows": T, "hidden": H, "eps": W.NORM_EPS,
+                   "layer_instances": L,
+                   "l2": f"weights rotate over {L} layer instances > 129 MB L2",
+                   "timing": "CUDA graphs of K steps, CUDA events on the launch stream",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "separate": {"value": sp["value"], "ms_per_step": sp["ms_per_step"],
+                     "api": "moe_add_rmsnorm_quantize then moe_forward"},
+        "saved_us_per_step": (sp["ms_per_step"] - f["ms_per_step"]) * 1e3,
+        "saved_bytes_per_step": T * H * 2 * 2,  # the normed rows written and read again
+        # one launch per fused step at one row; more rows launch the add-norm
+        # kernel and the forward's kernels (not counted here)
+        "gpu_launches": K if T == 1 else None,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for net in nets:
+        net.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
 # ---- replicas ---------------------------------------------------------------
 
 def reduce_max(value: float, dev=None) -> float:
@@ -900,6 +1029,13 @@ def main():
     args = parse()
     if args.workload in ADDNORM_ROWS:
         (reference_addnorm if args.impl == "reference" else run_addnorm)(args)
+    elif args.workload in ADDNORM_LAYER_ROWS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the add-norm layer leg has no oracle timing; see the layer and "
+                              "add-norm workloads"}), flush=True)
+        else:
+            run_addnorm_layer(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -41,7 +41,7 @@ EXPORTED = ("moe_create", "moe_load_weights", "moe_forward", "moe_forward_host",
             "moe_quantize", "moe_expert_activations", "moe_set_option", "moe_required_bytes",
             "moe_last_device_status", "moe_destroy", "moe_status_string",
             "moe_profile_forward", "moe_route_static", "moe_add_rmsnorm_quantize",
-            "moe_forward_codes")
+            "moe_forward_codes", "moe_forward_addnorm")
 
 MOE_ROUTE_STATIC_MAX_LOGITS = 262144
 
@@ -88,6 +88,7 @@ def load_library(path: str = LIB_PATH):
     L.moe_route_static.argtypes = [vp, vp, i, i, i, i, vp, vp, vp]
     L.moe_expert_activations.argtypes = [vp, i, vp, vp, vp]
     L.moe_forward_codes.argtypes = [vp, i, vp, vp, vp]
+    L.moe_forward_addnorm.argtypes = [vp, vp, vp, vp, ctypes.c_float, i, vp, vp, vp, vp]
     L.moe_set_option.argtypes = [vp, i, i]
     L.moe_profile_forward.argtypes = [vp, vp, vp, i, vp, vp, i, ctypes.POINTER(ctypes.c_int), vp]
     L.moe_required_bytes.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(ctypes.c_size_t)]
@@ -170,6 +171,13 @@ def moe_add_rmsnorm_quantize(ctx, residual, x, gamma, eps: float, rows: int, h_o
 
 def moe_expert_activations(ctx, rows: int, hq, sh, stream=None) -> int:
     return load_library().moe_expert_activations(ctx, rows, _ptr(hq), _ptr(sh), _stream(stream))
+
+
+def moe_forward_addnorm(ctx, residual, x, gamma, eps: float, rows: int, h_out, xn_out, y,
+                        stream=None) -> int:
+    return load_library().moe_forward_addnorm(ctx, _ptr(residual), _ptr(x), _ptr(gamma),
+                                              float(eps), rows, _ptr(h_out), _ptr(xn_out),
+                                              _ptr(y), _stream(stream))
 
 
 def moe_forward_codes(ctx, rows: int, codes, scales, stream=None) -> int:
@@ -275,6 +283,20 @@ class MoELayer:
             y = torch.empty_like(x)
         _check(moe_forward(self.ctx, x, y, x.shape[0], stream), "moe_forward")
         return y
+
+    def forward_addnorm(self, residual: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor,
+                        eps: float, keep_xn: bool = False, stream=None):
+        """Residual add + RMS norm + the layer: returns (h, xn or None, y)."""
+        for t in (residual, x, gamma):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError("residual, x and gamma must be contiguous bf16 CUDA tensors")
+        T, H = x.shape
+        h = torch.empty_like(x)
+        xn = torch.empty_like(x) if keep_xn else None
+        y = torch.empty_like(x)
+        _check(moe_forward_addnorm(self.ctx, residual, x, gamma, eps, T, h, xn, y, stream),
+               "moe_forward_addnorm")
+        return h, xn, y
 
     def forward_host(self, x: torch.Tensor, y: torch.Tensor | None = None, stream=None):
         if x.dtype != torch.bfloat16 or x.is_cuda:

@@ -96,6 +96,8 @@ struct Small {
   uint32_t cand_key[2 * kW * kMaxTopK];
   uint32_t cand_id[2 * kW * kMaxTopK];
   float gred[kW];
+  float gmax[kW];  // one scale per row: each warp's amax
+  float gss[kW];   // add-norm: each warp's sum of squares
   float gamma;
   int tag;
   float comb[kMaxTopK + 1][16];  // down outputs gathered for the combine
@@ -279,12 +281,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
   for (int i = 0; i < kMaxV; ++i)
     gw[i] = i < nv ? __ldg(reinterpret_cast<const uint2*>(a.L.gate + k0 + 128 * i + 4 * lane))
                    : make_uint2(0u, 0u);
+  // the add-norm's gamma (immutable) before the wait as well
+  const bool addnorm = a.an.residual != nullptr;
+  uint2 gn[kMaxV];
+#pragma unroll
+  for (int i = 0; i < kMaxV; ++i)
+    gn[i] = (addnorm && i < nv)
+                ? __ldg(reinterpret_cast<const uint2*>(a.an.gamma + k0 + 128 * i + 4 * lane))
+                : make_uint2(0u, 0u);
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x == 0) sm->tag = ld_acquire(epoch) + 1;
 
   // ---- router logits, x quantisation (1 x 128 groups) and the shared gate ----
-  float acc2[2] = {0.0f, 0.0f}, gacc = 0.0f;
+  float acc2[2] = {0.0f, 0.0f}, gacc = 0.0f, gmx = 0.0f;
   // both slices' x loads in flight together (the stores below could alias
   // x as far as the compiler knows, so it would not hoist the second)
   uint2 xr[kMaxV];
@@ -292,6 +302,65 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
   for (int i = 0; i < kMaxV; ++i)
     xr[i] = i < nv ? __ldcg(reinterpret_cast<const uint2*>(a.x + k0 + 128 * i + 4 * lane))
                    : make_uint2(0u, 0u);
+  if (addnorm) {
+    // residual add and RMS norm in this pass (every CTA the whole row): h =
+    // bf16(residual + x), r = 1 / sqrt(sum(h^2) / H + eps) in fp32 over a
+    // fixed order (lanes, then warps 0..kW-1), xn = bf16(h * r * gamma); xn
+    // then stands for x below.  CTA 0 writes h (and xn if asked).
+    uint2 rr[kMaxV];
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i)
+      rr[i] = i < nv ? __ldcg(reinterpret_cast<const uint2*>(a.an.residual + k0 + 128 * i +
+                                                             4 * lane))
+                     : make_uint2(0u, 0u);
+    float hv[kMaxV][4];
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i) {
+      if (i >= nv) continue;
+      const __nv_bfloat162 r0 = *reinterpret_cast<const __nv_bfloat162*>(&rr[i].x);
+      const __nv_bfloat162 r1 = *reinterpret_cast<const __nv_bfloat162*>(&rr[i].y);
+      const __nv_bfloat162 x0 = *reinterpret_cast<const __nv_bfloat162*>(&xr[i].x);
+      const __nv_bfloat162 x1 = *reinterpret_cast<const __nv_bfloat162*>(&xr[i].y);
+      const __nv_bfloat162 h0 = __floats2bfloat162_rn(__low2float(r0) + __low2float(x0),
+                                                      __high2float(r0) + __high2float(x0));
+      const __nv_bfloat162 h1 = __floats2bfloat162_rn(__low2float(r1) + __low2float(x1),
+                                                      __high2float(r1) + __high2float(x1));
+      hv[i][0] = __low2float(h0);
+      hv[i][1] = __high2float(h0);
+      hv[i][2] = __low2float(h1);
+      hv[i][3] = __high2float(h1);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ss = fmaf(hv[i][c], hv[i][c], ss);
+      if (b == 0) {
+        uint2 hp;
+        hp.x = *reinterpret_cast<const uint32_t*>(&h0);
+        hp.y = *reinterpret_cast<const uint32_t*>(&h1);
+        *reinterpret_cast<uint2*>(a.an.h_out + k0 + 128 * i + 4 * lane) = hp;
+      }
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) sm->gss[warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) tot += sm->gss[w];
+    const float rn = __frsqrt_rn(__fdiv_rn(tot, (float)H) + a.an.eps);
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i) {
+      if (i >= nv) continue;
+      const __nv_bfloat162 g0 = *reinterpret_cast<const __nv_bfloat162*>(&gn[i].x);
+      const __nv_bfloat162 g1 = *reinterpret_cast<const __nv_bfloat162*>(&gn[i].y);
+      const __nv_bfloat162 n0 = __floats2bfloat162_rn(hv[i][0] * rn * __low2float(g0),
+                                                      hv[i][1] * rn * __high2float(g0));
+      const __nv_bfloat162 n1 = __floats2bfloat162_rn(hv[i][2] * rn * __low2float(g1),
+                                                      hv[i][3] * rn * __high2float(g1));
+      xr[i].x = *reinterpret_cast<const uint32_t*>(&n0);
+      xr[i].y = *reinterpret_cast<const uint32_t*>(&n1);
+      if (b == 0 && a.an.xn_out)
+        *reinterpret_cast<uint2*>(a.an.xn_out + k0 + 128 * i + 4 * lane) = xr[i];
+    }
+  }
 #pragma unroll
   for (int i = 0; i < kMaxV; ++i) {
     if (i >= nv) continue;
@@ -312,14 +381,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     }
     float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
     m = warp_max(m);
-    const float sc = group_scale(m);
-    const uint32_t packed = quant4(x0, x1, x2, x3, sc);
-    *reinterpret_cast<uint32_t*>(L.xq + kk) = packed;
     *reinterpret_cast<uint2*>(L.xs + kk) = raw;
-    if (lane == 0) L.sx[kk / kGroup] = sc;
-    if (b == 0) {
-      *reinterpret_cast<uint32_t*>(a.w.xq + kk) = packed;
-      if (lane == 0) a.w.sx[kk / kGroup] = sc;
+    if (a.d.per_row) {
+      gmx = fmaxf(gmx, m);  // quantised below, once the row's amax is known
+    } else {
+      const float sc = group_scale(m);
+      const uint32_t packed = quant4(x0, x1, x2, x3, sc);
+      *reinterpret_cast<uint32_t*>(L.xq + kk) = packed;
+      if (lane == 0) L.sx[kk / kGroup] = sc;
+      if (b == 0) {
+        *reinterpret_cast<uint32_t*>(a.w.xq + kk) = packed;
+        if (lane == 0) a.w.sx[kk / kGroup] = sc;
+      }
     }
     const __nv_bfloat162 g0 = *reinterpret_cast<const __nv_bfloat162*>(&gw[i].x);
     const __nv_bfloat162 g1 = *reinterpret_cast<const __nv_bfloat162*>(&gw[i].y);
@@ -334,9 +407,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
       L.red[warp] = v0;
       L.red[kW + warp] = v1;
       sm->gred[warp] = vg;
+      sm->gmax[warp] = gmx;
     }
   }
   __syncthreads();
+  if (a.d.per_row) {
+    // one scale per row: every group takes the row's amax / 448
+    float rm = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) rm = fmaxf(rm, sm->gmax[w]);
+    const float sc = group_scale(rm);
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i) {
+      if (i >= nv) continue;
+      const int kk = k0 + 128 * i + 4 * lane;
+      const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&xr[i].x);
+      const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&xr[i].y);
+      const uint32_t packed =
+          quant4(__low2float(p0), __high2float(p0), __low2float(p1), __high2float(p1), sc);
+      *reinterpret_cast<uint32_t*>(L.xq + kk) = packed;
+      if (lane == 0) L.sx[kk / kGroup] = sc;
+      if (b == 0) {
+        *reinterpret_cast<uint32_t*>(a.w.xq + kk) = packed;
+        if (lane == 0) a.w.sx[kk / kGroup] = sc;
+      }
+    }
+  }
   const unsigned long long tag = (unsigned long long)(unsigned)sm->tag << 32;
   if (threadIdx.x < 2) {
     const int ee = b + G * threadIdx.x;
@@ -454,11 +550,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     for (int i = threadIdx.x; i < I; i += kThreads)
       L.hall[i] = poll_tagged(X.h + (size_t)r * I + i, tag, status);
     __syncthreads();
+    float hrs = 0.0f;  // one scale per row: the SwiGLU row's amax / 448
+    if (a.d.per_row) {
+      float m = 0.0f;
+      for (int i = threadIdx.x; i < I / 4; i += kThreads) {
+        const float4 v = *reinterpret_cast<const float4*>(L.hall + 4 * i);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+      }
+      m = warp_max(m);
+      if (lane == 0) sm->gmax[warp] = m;
+      __syncthreads();
+#pragma unroll
+      for (int w = 0; w < kW; ++w) hrs = fmaxf(hrs, sm->gmax[w]);
+      hrs = group_scale(hrs);
+    }
     for (int grp = warp; grp < nbi; grp += kW) {
       const float4 v = *reinterpret_cast<const float4*>(L.hall + grp * kGroup + 4 * lane);
       float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
       m = warp_max(m);
-      const float s = group_scale(m);
+      const float s = a.d.per_row ? hrs : group_scale(m);
       const uint32_t packed = quant4(v.x, v.y, v.z, v.w, s);
       *reinterpret_cast<uint32_t*>(L.hq + grp * kGroup + 4 * lane) = packed;
       if (lane == 0) L.sh[grp] = s;

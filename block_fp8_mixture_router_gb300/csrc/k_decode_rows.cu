@@ -71,6 +71,8 @@ struct Small {
   float gred[kW * kR];
   float gamma[kR];
   int tag;
+  float gmx[2][kW * 4];  // one scale per row: each warp's amax of a row group (two buffers)
+  float hmx[kR * 8];     // one scale per row: group amaxes of an expert's SwiGLU rows
 };
 
 // Row strides in shared memory (padding keeps the 8 rows an MMA reads at once
@@ -310,6 +312,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_rows(KArgs a) {
 #pragma unroll
         for (int j = 0; j < kGR; ++j)
           gm[i][j] = fmaxf(gm[i][j], __shfl_xor_sync(0xffffffffu, gm[i][j], o));
+    if (a.d.per_row) {
+      // one scale per row: every group of a row takes the row's amax, over
+      // all warps (alternate buffers, so one barrier per row group suffices)
+      static_assert(kGR == 4, "gmx holds four rows per warp");
+      float* gmx = sm->gmx[(t0 / kGR) & 1];
+      if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < kGR; ++j) {
+          float v = 0.0f;
+#pragma unroll
+          for (int i = 0; i < kMaxV; ++i) v = fmaxf(v, gm[i][j]);
+          gmx[warp * kGR + j] = v;
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < kGR; ++j) {
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kW; ++w) v = fmaxf(v, gmx[w * kGR + j]);
+#pragma unroll
+        for (int i = 0; i < kMaxV; ++i) gm[i][j] = v;
+      }
+    }
     // router dot products (experts b, b + G) and the shared gate
     float acc[3][kGR];
 #pragma unroll
@@ -631,12 +657,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_rows(KArgs a) {
             },
             [&](int i2, float val) { hstage[i2] = val; });
         __syncthreads();
+        if (a.d.per_row) {
+          // one scale per row: the group amaxes first, then each row's
+          for (int it = warp; it < nt * nbi; it += kW) {
+            const int col = it / nbi, grp = it % nbi;
+            const float4 hv = *reinterpret_cast<const float4*>(hstage + (size_t)col * I +
+                                                               grp * kGroup + 4 * lane);
+            const float m =
+                warp_max(fmaxf(fmaxf(fabsf(hv.x), fabsf(hv.y)), fmaxf(fabsf(hv.z), fabsf(hv.w))));
+            if (lane == 0) sm->hmx[it] = m;
+          }
+          __syncthreads();
+        }
         for (int it = warp; it < nt * nbi; it += kW) {
           const int col = it / nbi, grp = it % nbi;
           const float4 hv =
               *reinterpret_cast<const float4*>(hstage + (size_t)col * I + grp * kGroup + 4 * lane);
           float m = fmaxf(fmaxf(fabsf(hv.x), fabsf(hv.y)), fmaxf(fabsf(hv.z), fabsf(hv.w)));
           m = warp_max(m);
+          if (a.d.per_row) {
+            m = 0.0f;
+            for (int g2 = 0; g2 < nbi; ++g2) m = fmaxf(m, sm->hmx[col * nbi + g2]);
+          }
           const float sq = group_scale(m);
           const uint32_t packed = quant4(hv.x, hv.y, hv.z, hv.w, sq);
           *reinterpret_cast<uint32_t*>(A.hq + (size_t)col * hq_stride(I) + grp * kGroup +

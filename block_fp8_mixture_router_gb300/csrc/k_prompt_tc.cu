@@ -445,6 +445,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
                               : make_float4(0.f, 0.f, 0.f, 0.f);
           }
           if constexpr (kKind == kTcRoutedGateUp) {
+            if (g.hf) {
+              // one scale per row: the fp32 SwiGLU rows, quantised per row
+              // once every feature tile of the row is done (k_quant_h_rows)
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int col = c0s + kEpiWarps * u;
+                if (col < it.n)
+                  *reinterpret_cast<float4*>(g.hf + (size_t)(it.row0 + col) * g.ldo + fcol +
+                                             4 * lane) = v[u];
+              }
+              continue;
+            }
             float m[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
@@ -536,6 +548,8 @@ __global__ void __launch_bounds__(256) k_quant_scatter(KArgs a, uint8_t* xg, flo
   __syncthreads();
   const bf16* xr = a.x + (size_t)t * H;
   const int ngroups = H / kGroup;
+  const bool pre_q = a.an.pre_q != 0;  // the add-norm already wrote the row's codes
+  const float rs = (a.d.per_row && !pre_q) ? row_scale(xr, H, red) : 0.0f;
   // the shared gate's dot product from the same registers as the codes
   float acc = 0.0f;
   for (int gi = warp; gi < ngroups; gi += 8) {
@@ -552,10 +566,17 @@ __global__ void __launch_bounds__(256) k_quant_scatter(KArgs a, uint8_t* xg, flo
     acc = fmaf(v1, __high2float(g0), acc);
     acc = fmaf(v2, __low2float(g1), acc);
     acc = fmaf(v3, __high2float(g1), acc);
-    float m = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
-    m = warp_max(m);
-    const float s = group_scale(m);
-    const uint32_t packed = quant4(v0, v1, v2, v3, s);
+    uint32_t packed;
+    float s;
+    if (pre_q) {
+      packed = *reinterpret_cast<const uint32_t*>(a.w.xq + (size_t)t * H + base);
+      s = a.w.sx[(size_t)t * ngroups + gi];
+    } else {
+      float m = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+      m = warp_max(m);
+      s = a.d.per_row ? rs : group_scale(m);
+      packed = quant4(v0, v1, v2, v3, s);
+    }
     for (int j = 0; j < k; ++j) {
       *reinterpret_cast<uint32_t*>(xg + (size_t)slots[j] * H + base) = packed;
       if (lane == 0) sxg[(size_t)slots[j] * ngroups + gi] = s;
@@ -569,6 +590,31 @@ __global__ void __launch_bounds__(256) k_quant_scatter(KArgs a, uint8_t* xg, flo
     for (int w = 0; w < 8; ++w) v += red[w];
     a.w.gamma[t] = sigmoid_f32(v);
   }
+}
+
+// ---- SwiGLU rows with one scale per row ---------------------------------------
+// One warp per slot: the row's amax over its I fp32 values, one scale, and the
+// e4m3 codes of every value (rows of hf [slots][I] -> hq [slots][I], and the
+// row's scale in each of its I/128 entries of sh).
+__global__ void __launch_bounds__(256) k_quant_h_rows(const float* __restrict__ hf,
+                                                      uint8_t* __restrict__ hq,
+                                                      float* __restrict__ sh, int n_rows, int I) {
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
+  if (r >= n_rows) return;
+  const float* row = hf + (size_t)r * I;
+  float m = 0.0f;
+  for (int c = 4 * lane; c < I; c += 128) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(row + c));
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  const float s = group_scale(warp_max(m));
+  for (int c = 4 * lane; c < I; c += 128) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(row + c));
+    *reinterpret_cast<uint32_t*>(hq + (size_t)r * I + c) = quant4(v.x, v.y, v.z, v.w, s);
+  }
+  for (int g = lane; g < I / kGroup; g += 32) sh[(size_t)r * (I / kGroup) + g] = s;
 }
 
 // Router weights as three bf16 parts, w = hi + mid + lo exactly (each part
@@ -633,6 +679,13 @@ cudaError_t launch_tc_gemm(int kind, const TcGemm& g, int grid, size_t smem, cud
   cfg.numAttrs = pdl ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelExC(&cfg, kernel_of(kind), args);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_quant_h_rows(const float* hf, uint8_t* hq, float* sh, int n_rows, int I,
+                                cudaStream_t s, bool pdl) {
+  if (n_rows < 1) return cudaSuccess;
+  return launch_pdl(k_quant_h_rows, dim3((n_rows + 7) / 8), dim3(256), 0, s, pdl, hf, hq, sh,
+                    n_rows, I);
 }
 
 cudaError_t launch_quant_scatter(const KArgs& a, uint8_t* xg, float* sxg, cudaStream_t s,

@@ -76,11 +76,15 @@ bool config_supported(const moe_config* c) {
   if (c->shared_inter <= 0 || c->shared_inter % kGroup) return false;
   if (c->top_k < 1 || c->top_k > kMaxTopK) return false;
   if (c->n_experts < c->top_k || c->n_experts > kMaxExperts) return false;
-  if (c->act_group != kGroup) return false;
+  if (c->act_group != kGroup && c->act_group != c->hidden) return false;
   if (c->max_rows < 1 || c->max_rows > 65536) return false;
   if (c->hidden > 65536 || c->inter > 65536 || c->shared_inter > 65536) return false;
   return true;
 }
+
+// One activation scale per row of x and of each SwiGLU row (act_group ==
+// hidden) instead of one per 1 x 128 group.
+bool per_row_scales(const moe_config& c) { return c.act_group == c.hidden && c.hidden > kGroup; }
 
 // Byte layout of everything a context allocates, in allocation order.
 struct Plan {
@@ -181,9 +185,9 @@ void free_all(moe_ctx* c) {
 int check_launch(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 KArgs make_args(moe_ctx* c, const void* x, void* y, int T) {
-  KArgs a;
+  KArgs a = {};  // a.an zero: no add-norm in front of the layer
   a.d = Dims{T, c->cfg.hidden, c->cfg.n_experts, c->cfg.top_k, c->cfg.inter, c->cfg.shared_inter,
-             c->opt_router_bf16, c->cfg.act_group == c->cfg.hidden ? 1 : 0};
+             c->opt_router_bf16, per_row_scales(c->cfg) ? 1 : 0};
   a.L = c->L;
   a.w = c->w;
   a.x = static_cast<const bf16*>(x);
@@ -263,7 +267,10 @@ struct StageRec {
 // The decode kernels serve rows <= kDecodeRows for hidden sizes up to 4096.
 bool use_decode(const moe_ctx* c, int T) {
   if (c->opt_path == 2 || c->opt_path == 4 || c->opt_invariant) return false;
-  return T <= kDecodeRows && c->cfg.hidden <= 4096;
+  if (T > kDecodeRows || c->cfg.hidden > 4096) return false;
+  // one scale per row: only the role-split decode kernels quantise whole rows
+  if (per_row_scales(c->cfg)) return use_row(c, T) || use_rows(c, T);
+  return true;
 }
 
 // One row on the role-split one-row kernel unless another decode kernel is
@@ -280,7 +287,8 @@ constexpr int kRowsAuto = 5;
 
 bool use_rows(const moe_ctx* c, int T) {
   if (T < 2 || T > kDecodeRows || c->rows_smem <= 0) return false;
-  return c->opt_path == 6 || ((c->opt_path == 0 || c->opt_path == 1) && T <= kRowsAuto);
+  return c->opt_path == 6 ||
+         ((c->opt_path == 0 || c->opt_path == 1) && (T <= kRowsAuto || per_row_scales(c->cfg)));
 }
 
 // Tensor maps and launch arguments of the four tcgen05 GEMMs.  The weight
@@ -321,6 +329,7 @@ void setup_tc(moe_ctx* c) {
   g[kTcRoutedGateUp].sb = c->sxg;
   g[kTcRoutedGateUp].hq = c->w.hq;
   g[kTcRoutedGateUp].sh = c->w.sh;
+  g[kTcRoutedGateUp].hf = per_row_scales(f) ? c->w.hbuf : nullptr;
   // routed down: W2 [E*H][I] x hq [slots][I]
   ok &= make_tc_map(&g[kTcRoutedDown].a, false, c->L.w2, E * H, I, 128);
   ok &= make_tc_map(&g[kTcRoutedDown].b, false, c->w.hq, R, I, 16);
@@ -392,9 +401,12 @@ cudaError_t launch_topk_after_router(const KArgs& a, const moe_ctx* c, const TcG
                        : launch_topk(a, s, pdl);
 }
 
+// pre_q: w.xq / w.sx already hold x's codes (written by the add-norm kernel
+// of moe_forward_addnorm); the grouped path then scatters them as they are.
 int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
-                StageRec* rec = nullptr) {
+                StageRec* rec = nullptr, bool pre_q = false) {
   KArgs a = make_args(c, x, y, T);
+  a.an.pre_q = pre_q ? 1 : 0;
   c->fwd_rows = T;
   c->fwd_slot_order = use_tc(c, T);
   const int grid = 2 * c->sm_count;
@@ -457,6 +469,10 @@ int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
     LAUNCH(launch_tc_gemm(kTcRoutedGateUp, c->tc[kTcRoutedGateUp], c->sm_count,
                           c->tc_smem[kTcRoutedGateUp], s, pdl),
            "gateup_tc");
+    if (per_row_scales(c->cfg))
+      LAUNCH(launch_quant_h_rows(c->w.hbuf, c->w.hq, c->w.sh, T * c->cfg.top_k, c->cfg.inter, s,
+                                 pdl),
+             "quant_h_rows");
     LAUNCH(launch_tc_gemm(kTcRoutedDown, c->tc[kTcRoutedDown], c->sm_count,
                           c->tc_smem[kTcRoutedDown], s, pdl),
            "down_tc");
@@ -620,6 +636,13 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     return MOE_ERR_CUDA;
   }
   setup_tc(c);
+  // one scale per row needs the tcgen05 kernels above 16 rows (the warp-MMA
+  // and chained decode kernels quantise 1 x 128 groups only)
+  if (per_row_scales(*cfg) && !c->tc_ok) {
+    free_all(c);
+    delete c;
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  }
   *out = c;
   return MOE_OK;
 }
@@ -771,7 +794,7 @@ int moe_add_rmsnorm_quantize(moe_ctx* c, const void* residual, const void* x, co
   if (!c || rows < 0) return MOE_ERR_INVALID_ARG;
   if (!(eps >= 0.0f) || !isfinite(eps)) return MOE_ERR_INVALID_ARG;
   const int H = c->cfg.hidden;
-  if (H > kAddNormMaxHidden) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (H > kAddNormMaxHidden || per_row_scales(c->cfg)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (rows == 0) return MOE_OK;
   if (!residual || !x || !gamma || !h_out || !xn_out || !codes || !scales)
     return MOE_ERR_INVALID_ARG;
@@ -806,6 +829,54 @@ int moe_add_rmsnorm_quantize(moe_ctx* c, const void* residual, const void* x, co
                                scales, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+int moe_forward_addnorm(moe_ctx* c, const void* residual, const void* x, const void* gamma,
+                        float eps, int rows, void* h_out, void* xn_out, void* y, void* stream) {
+  if (!c || rows < 0) return MOE_ERR_INVALID_ARG;
+  if (rows > c->cfg.max_rows) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!c->loaded) return MOE_ERR_NOT_LOADED;
+  if (!(eps >= 0.0f) || !isfinite(eps)) return MOE_ERR_INVALID_ARG;
+  const int H = c->cfg.hidden;
+  if (H > kAddNormMaxHidden || per_row_scales(c->cfg)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return MOE_OK;
+  if (!residual || !x || !gamma || !h_out || !y) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)residual | (uintptr_t)x | (uintptr_t)gamma | (uintptr_t)h_out |
+       (uintptr_t)xn_out | (uintptr_t)y) & 15)
+    return MOE_ERR_INVALID_ARG;
+  // outputs apart from every input and from each other (the one-row kernel
+  // reads the inputs in every CTA while one of them writes the outputs)
+  const size_t nb = (size_t)rows * H * 2, ng = (size_t)H * 2;
+  const void* outs[] = {h_out, xn_out, y};
+  for (int i = 0; i < 3; ++i) {
+    if (!outs[i]) continue;
+    if (overlaps(outs[i], nb, residual, nb) || overlaps(outs[i], nb, x, nb) ||
+        overlaps(outs[i], nb, gamma, ng))
+      return MOE_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 3; ++j)
+      if (outs[j] && overlaps(outs[i], nb, outs[j], nb)) return MOE_ERR_INVALID_ARG;
+  }
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  c->last_stream = s;
+  if (use_decode(c, rows) && use_row(c, rows)) {
+    // one row: the add-norm runs inside the layer's one kernel
+    KArgs a = make_args(c, x, y, rows);
+    a.an = AddNorm{static_cast<const bf16*>(residual), static_cast<const bf16*>(gamma),
+                   static_cast<bf16*>(h_out), static_cast<bf16*>(xn_out), eps, 0};
+    c->fwd_rows = rows;
+    c->fwd_slot_order = false;
+    return check_launch(launch_decode_row(a, c->sm_count, c->row_smem, c->opt_pdl != 0, s));
+  }
+  // more rows: the add-norm kernel writes h, the normed rows and their codes,
+  // and the grouped path scatters those codes without quantising again
+  bf16* xn = xn_out ? static_cast<bf16*>(xn_out) : c->stage_x;
+  if (launch_add_rmsnorm_quant(static_cast<const bf16*>(residual), static_cast<const bf16*>(x),
+                               static_cast<const bf16*>(gamma), eps, rows, H,
+                               static_cast<bf16*>(h_out), xn, c->w.xq, c->w.sx, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return run_forward(c, xn, y, rows, s, nullptr, true);
 }
 
 int moe_expert_activations(moe_ctx* c, int rows, uint8_t* hq, float* sh, void* stream) {
@@ -882,6 +953,7 @@ int moe_set_option(moe_ctx* c, int option, int value) {
     case MOE_OPT_PATH:
       // 5 named a persistent multi-row decode kernel that no longer exists
       if (value < 0 || value > 6 || value == 5) return MOE_ERR_INVALID_ARG;
+      if (per_row_scales(c->cfg) && (value == 3 || value == 4)) return MOE_ERR_UNSUPPORTED_SHAPE;
       c->opt_path = value;
       return MOE_OK;
     case MOE_OPT_PDL:

@@ -80,12 +80,25 @@ struct DevWork {
   int* sched_blk;       // [ceil(T/256)][E] rows per expert in each 256-row block
 };
 
+// The residual add + RMS norm in front of the layer, when a forward takes
+// (residual, x) instead of x (moe_forward_addnorm); residual == nullptr for
+// a plain forward.
+struct AddNorm {
+  const bf16* residual;  // [T][H]
+  const bf16* gamma;     // [H]
+  bf16* h_out;           // [T][H] the new residual stream, bf16(residual + x)
+  bf16* xn_out;          // [T][H] the normed rows, or nullptr
+  float eps;
+  int pre_q;             // 1: w.xq / w.sx already hold the normed rows' codes
+};
+
 struct KArgs {
   Dims d;
   DevLayer L;
   DevWork w;
-  const bf16* x;
+  const bf16* x;  // the layer's input; with an add-norm, the block output added to residual
   bf16* y;
+  AddNorm an;
 };
 
 // Upper bound of sum_e ceil(count_e / kChunk) over experts with sum_e count_e = T*k.
@@ -140,6 +153,8 @@ struct TcGemm {
   const float* sa;     // weight block scales (routed)
   const float* sb;     // activation scales [slot][n_k] (routed)
   uint8_t* hq;         // routed gate/up: e4m3 SwiGLU rows [slot][ldo]
+  float* hf;           // routed gate/up with one scale per row: fp32 SwiGLU rows
+                       // [slot][ldo] instead of hq (quantised by k_quant_h_rows)
   float* sh;           // routed gate/up: their scales [slot][ldo/128]
   bf16* out;           // expert kinds: bf16 [row][ldo]
   float* outf;         // router: fp32 logits [ksplit][row][ldo] (partials when ksplit > 1)
@@ -152,6 +167,8 @@ cudaError_t launch_tc_gemm(int kind, const TcGemm& g, int grid, size_t smem, cud
                            bool pdl = false);
 cudaError_t launch_quant_scatter(const KArgs& a, uint8_t* xg, float* sxg, cudaStream_t s,
                                  bool pdl = false);
+cudaError_t launch_quant_h_rows(const float* hf, uint8_t* hq, float* sh, int n_rows, int I,
+                                cudaStream_t s, bool pdl = false);
 cudaError_t launch_split_router(const float* wr, bf16* out, int E, int Epad, int H, cudaStream_t s);
 bool make_tc_map(CUtensorMap* m, bool bf16_elems, const void* ptr, uint64_t rows, uint64_t cols,
                  uint32_t box_rows);

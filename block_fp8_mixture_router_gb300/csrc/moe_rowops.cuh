@@ -11,14 +11,41 @@ namespace moe {
 // ---- activation quantisation (1 x 128 groups) and the shared gate ----------
 // One CTA per row (any multiple of 32 threads up to 1024).  Warp w quantises
 // groups w, w + nw, ...; each lane holds 4 consecutive values of the group.
+// With one scale per row (a.d.per_row) every group takes the row's scale.
 // The gate dot product x . g is reduced in a fixed order (per-thread strided
 // sums, then warps 0..nw-1).
+// Largest |value| of four bf16 values packed in a uint2.
+__device__ __forceinline__ float amax4(const uint2& raw) {
+  const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+  const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+  return fmaxf(fmaxf(fabsf(__low2float(p0)), fabsf(__high2float(p0))),
+               fmaxf(fabsf(__low2float(p1)), fabsf(__high2float(p1))));
+}
+
+// Scale of a whole row (one scale per row): amax over the row's H values,
+// reduced over the CTA's warps (every thread calls it; it synchronises the
+// CTA twice).  red: at least nw floats of shared memory.
+__device__ __forceinline__ float row_scale(const bf16* xr, int H, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  float m = 0.0f;
+  for (int base = 4 * threadIdx.x; base < H; base += 4 * blockDim.x)
+    m = fmaxf(m, amax4(*reinterpret_cast<const uint2*>(xr + base)));
+  m = warp_max(m);
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  float r = 0.0f;
+  for (int w = 0; w < nw; ++w) r = fmaxf(r, red[w]);
+  __syncthreads();  // red is free again
+  return group_scale(r);
+}
+
 __device__ __forceinline__ void quant_row_and_gate(const KArgs& a, int t) {
   __shared__ float red[32];
   const int H = a.d.H;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const bf16* xr = a.x + (size_t)t * H;
   const int ngroups = H / kGroup;
+  const float rs = a.d.per_row ? row_scale(xr, H, red) : 0.0f;
   for (int gi = warp; gi < ngroups; gi += nw) {
     const int base = gi * kGroup + 4 * lane;
     uint2 raw = *reinterpret_cast<const uint2*>(xr + base);
@@ -27,7 +54,7 @@ __device__ __forceinline__ void quant_row_and_gate(const KArgs& a, int t) {
     float v[4] = {__low2float(p0), __high2float(p0), __low2float(p1), __high2float(p1)};
     float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
     m = warp_max(m);
-    const float s = group_scale(m);
+    const float s = a.d.per_row ? rs : group_scale(m);
     const uint32_t packed = quant4(v[0], v[1], v[2], v[3], s);
     *reinterpret_cast<uint32_t*>(a.w.xq + (size_t)t * H + base) = packed;
     if (lane == 0) a.w.sx[(size_t)t * ngroups + gi] = s;

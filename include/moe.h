@@ -57,15 +57,25 @@ typedef struct moe_ctx moe_ctx; /* opaque: owns the device weights and workspace
 
 /* Layer shape.  Supported: hidden % 128 == 0, inter % 128 == 0,
  * shared_inter % 128 == 0, 1 <= top_k <= 16, top_k <= n_experts <= 256,
- * act_group == 128, 1 <= max_rows <= 65536.  The Drama 3 layer is
- * hidden 2048, 256 experts, top-8, inter 512, shared_inter 512. */
+ * act_group == 128 or act_group == hidden, 1 <= max_rows <= 65536.  The
+ * Drama 3 layer is hidden 2048, 256 experts, top-8, inter 512,
+ * shared_inter 512.
+ * act_group: 128 quantises the experts' inputs per row and per 128 values
+ * (PR #939 "drama3: Fish Audio Drama 3 text to speech on one CUDA GPU",
+ * section "Precision"); hidden gives each row of x, and each routed SwiGLU
+ * row, one scale (row amax / 448), the other reading of "dynamic per-row"
+ * activations.  Weight scales stay per 128 x 128 block either way.  With one
+ * scale per row, 16 rows or fewer run on the role-split decode kernels and
+ * more on the tcgen05 kernels (MOE_OPT_PATH 3 and 4, and
+ * moe_add_rmsnorm_quantize, return MOE_ERR_UNSUPPORTED_SHAPE), and a device
+ * without the tcgen05 kernels for the shape refuses the context. */
 typedef struct {
   int hidden;          /* H */
   int n_experts;       /* E */
   int top_k;           /* k */
   int inter;           /* I: routed SwiGLU width */
   int shared_inter;    /* Is: shared SwiGLU width */
-  int act_group;       /* activation quantisation group = weight block edge (128) */
+  int act_group;       /* activation quantisation group: 128, or hidden (one scale per row) */
   int max_rows;        /* largest T one forward accepts; sizes the workspace */
   size_t workspace_cap_bytes; /* 0 = no cap; else weights + workspace must fit */
 } moe_config;
@@ -220,6 +230,33 @@ int moe_quantize(moe_ctx* ctx, const void* x, int rows, uint8_t* codes, float* s
 int moe_add_rmsnorm_quantize(moe_ctx* ctx, const void* residual, const void* x,
                              const void* gamma, float eps, int rows, void* h_out, void* xn_out,
                              uint8_t* codes, float* scales, void* stream);
+
+/* The residual add + RMS norm and the layer in one call: the layer's input
+ * is the normed sum, and the add-norm feeds the experts the FP8 groups it
+ * quantises itself (PR #925/#927 commit "add-norm fused with the routed
+ * experts' FP8 activation quantization").  Per row t of H values:
+ *   h_out[t] = bf16(residual[t] + x[t])                          (new residual)
+ *   xn[t]    = bf16(h * (1 / sqrt(sum(h^2) / H + eps)) * gamma)   (fp32 math)
+ *   y[t]     = the layer of moe_forward on xn[t]
+ * One row runs as one kernel: every CTA of the one-row kernel takes the
+ * add-norm of the row in its first pass.  More rows run the add-norm kernel
+ * of moe_add_rmsnorm_quantize, whose codes and scales the grouped path
+ * scatters to the experts as they are.  The sum of squares is reduced in a
+ * different order in the two cases, so a normed value within about 1e-6
+ * relative of a bf16 rounding midpoint may round the other way between them.
+ * residual, x, h_out, xn_out, y bf16 [rows][H]; gamma bf16 [H]; device
+ * pointers, 16-byte aligned.  xn_out may be NULL (the normed rows are then
+ * not kept); h_out, xn_out and y must not overlap any input or each other
+ * (MOE_ERR_INVALID_ARG).  eps finite and >= 0.  Contexts with one scale per
+ * row, or hidden above 8192, return MOE_ERR_UNSUPPORTED_SHAPE.
+ * Asynchronous on `stream`; moe_forward_codes afterwards returns the codes
+ * the experts read.
+ * Defined by: PR #925/#927 commit "add-norm fused with the routed experts'
+ * FP8 activation quantization"; PR #939 "drama3: Fish Audio Drama 3 text to
+ * speech on one CUDA GPU", section "Kernel contract" (plain-gamma RMS norm)
+ * and section "Precision" (bf16 residual stream). */
+int moe_forward_addnorm(moe_ctx* ctx, const void* residual, const void* x, const void* gamma,
+                        float eps, int rows, void* h_out, void* xn_out, void* y, void* stream);
 
 /* Expert-side intermediates of the most recent moe_forward, for checking:
  * hq e4m3 [rows][k][I] and sh fp32 [rows][k][I/128] (the re-quantised SwiGLU

@@ -47,13 +47,17 @@ def test_refusals_without_a_device(lib):
            moe.moe_config(2048, 4, 8, 512, 512, 128, 16, 0),
            moe.moe_config(2048, 256, 0, 512, 512, 128, 16, 0),
            moe.moe_config(2048, 256, 17, 512, 512, 128, 16, 0),
-           moe.moe_config(2048, 256, 8, 512, 512, 2048, 16, 0),
+           moe.moe_config(2048, 256, 8, 512, 512, 256, 16, 0),
+           moe.moe_config(2048, 256, 8, 512, 512, 1024, 16, 0),
            moe.moe_config(2048, 256, 8, 512, 512, 128, 0, 0),
            moe.moe_config(2048, 256, 8, 512, 512, 128, 65537, 0)]
     for cfg in bad:
         rc, h = moe.moe_create(cfg, 0)
         assert rc == moe.MOE_ERR_UNSUPPORTED_SHAPE and not h.value
         assert moe.moe_required_bytes(cfg)[0] == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    # one activation scale per row (act_group == hidden) is a supported shape
+    assert moe.moe_required_bytes(moe.moe_config(2048, 256, 8, 512, 512, 2048, 16, 0))[0] == \
+        moe.MOE_OK
     capped = moe.moe_config(2048, 256, 8, 512, 512, 128, 1024, 1 << 20)
     rc, h = moe.moe_create(capped, 0)
     assert rc == moe.MOE_ERR_ALLOC_LIMIT and not h.value

@@ -30,12 +30,16 @@ def dev():
 class Case:
     """A layer built on the GPU, loaded into a context, plus its host copy."""
 
-    def __init__(self, wl: W.Workload, max_rows: int, dev, layer_idx: int = 0):
+    def __init__(self, wl: W.Workload, max_rows: int, dev, layer_idx: int = 0,
+                 act_group: int | None = None):
         self.wl = wl
         self.shape = wl.shape
         seed = W.layer_seed(wl, layer_idx)
         self.layer = W.make_layer(wl.shape, seed, wl.x_kind, device=dev)
-        self.moe = m.MoELayer(_shape(wl.shape), max_rows=max_rows)
+        shape = _shape(wl.shape)
+        if act_group is not None:
+            shape.act_group = act_group
+        self.moe = m.MoELayer(shape, max_rows=max_rows)
         self.moe.load(self.layer)
         self._host = None
         self.seed = seed
@@ -58,7 +62,7 @@ HQ_MAX_STEP = 1
 
 
 def run_and_check(case: Case, x: torch.Tensor, sample_rows=None, path=m.PATH_AUTO,
-                  threads=None):
+                  threads=None, oracle_kw=None):
     """One forward on `path`, then every check against the oracle on the
     sampled rows (all rows by default): the FP8 codes and scales of x that the
     forward's experts read (read back from the forward itself, every rank's
@@ -74,7 +78,7 @@ def run_and_check(case: Case, x: torch.Tensor, sample_rows=None, path=m.PATH_AUT
     torch.cuda.synchronize()
     rows = np.arange(T) if sample_rows is None else np.asarray(sample_rows)
     xb = bits(x)[rows]
-    ref = oracle_rows(case.host, xb, threads=threads, trace=True)
+    ref = oracle_rows(case.host, xb, threads=threads, trace=True, **(oracle_kw or {}))
     check_forward_codes(fcodes.cpu().numpy()[rows], fscales.cpu().numpy()[rows],
                         ref.trace["xq"], ref.trace["sx"])
     near, differ = check_topk(idx.cpu().numpy()[rows], ref.trace["logits"], case.shape.top_k)
