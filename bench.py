@@ -833,13 +833,14 @@ def measure_layer(moe, W, wl, T: int, K: int, Wm: int, L: int, path: str, dev, r
             stage_ms.setdefault(name, []).append(t)
     stage_avg = {n: sum(v) / len(v) for n, v in stage_ms.items()}
     stage_prof = dict(stage_avg)
-    launches_per_step = len(stage_avg)
+    launches_per_step = sum(STAGE_LAUNCHES.get(n, 1) for n in stage_avg)
     duration_source = "per-kernel CUDA events of a profiled forward (moe_profile_forward)"
-    if launches_per_step == 1:
-        # one kernel per layer forward: its launches are the timed region's
+    if len(stage_avg) == 1:
+        # one stage per layer forward: its launches are the timed region's
         # launches, so their average duration is the timed region's
         stage_avg = {n: ms / K / layers_per_step for n in stage_avg}
-        duration_source = "CUDA events over the timed region (one launch per layer forward)"
+        duration_source = ("CUDA events over the timed region (the layer forward's "
+                           f"{launches_per_step} launch(es), chained)")
 
     # touched experts per layer instance; in the sweep each layer's input is
     # the previous layer's output (ys[j - 1] after the timed steps)
@@ -931,6 +932,11 @@ def measure_layer(moe, W, wl, T: int, K: int, Wm: int, L: int, path: str, dev, r
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return out
+
+
+# stages that time more than one launch (none today: moe_profile_forward
+# records one event after every launch)
+STAGE_LAUNCHES = {}
 
 
 def launches_hint(T: int) -> int:

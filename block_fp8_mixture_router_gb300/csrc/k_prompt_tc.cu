@@ -24,11 +24,11 @@
 // for it.  The tile's outputs are transposed through shared memory and
 // stored token-major with coalesced 128/256-byte rows.
 //
-// CTA roles (kTcThreads = 320 threads): warp 0 lane 0 issues TMA, warp 1 owns
-// TMEM and lane 0 issues the MMAs, warps 2-9 are the epilogue (warp w reads
-// TMEM lanes 32*(w%4).. and column half (w-2)/4 of the tile's tokens).  Every
-// wait is bounded; a wait that gives up sets the status flag and all roles
-// leave their loops.
+// CTA roles (kTcThreads = 576 threads): warp 0 lane 0 issues TMA, warp 1 owns
+// TMEM and lane 0 issues the MMAs, warps 2-17 are the epilogue (warp w reads
+// TMEM lanes 32*(w%4).. and column quarter (w-2)/4 of the tile's tokens).
+// Every wait is bounded; a wait that gives up sets the status flag and all
+// roles leave their loops.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -39,10 +39,13 @@ namespace moe {
 
 namespace {
 
-// Epilogue warps, 2 per TMEM lane quarter: with the TMA and MMA warps that is
-// 10 warps, at most 3 on one SM sub-partition, so each thread may hold up to
-// 168 registers (the block-FP8 epilogue keeps 2 x 32 promoted accumulators)
-constexpr int kEpiWarps = 8;
+// Epilogue warps, 4 per TMEM lane quarter: the per-K-block promotion is a
+// chain of dependent loads and FMAs, so four warps per SM sub-partition hide
+// its latency (two left the epilogue issue-bound at 40 % of the issue slots).
+// With the TMA and MMA warps that is 18 warps, so a thread may hold up to 96
+// registers; the block-FP8 epilogue keeps 2 x 16 promoted accumulators and
+// reads one tile's partials from TMEM at a time.
+constexpr int kEpiWarps = 16;
 constexpr int kTcThreads = 64 + 32 * kEpiWarps;  // + the TMA and MMA warps
 constexpr int kTile = 128;        // output features per tile (M)
 constexpr int kKBytes = 128;      // bytes of K per stage (one 128B swizzle row)
@@ -152,6 +155,8 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// 18 warps: an SM sub-partition holds up to 5 of them, so a thread may use
+// at most 96 registers (5 x 32 x 96 <= 16384 per sub-partition)
 template <int kKind>
 __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant__ TcGemm g) {
   using C = Cfg<kKind>;
@@ -167,7 +172,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
   const uint32_t span_a = (uint32_t)((kN * g.n_k * 4 + 32 + 15) & ~15);
   const uint32_t span_w = (uint32_t)((g.n_k * 4 + 32 + 15) & ~15);
   const uint32_t sbs_slot = kF8 ? span_a + 2 * span_w : 0u;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sbs + 2 * sbs_slot);
+  // block-FP8: the current item's scale products [2 tiles][n_k][kN] (weight
+  // block scale x token scale), formed once per item
+  float* pbuf = reinterpret_cast<float*>(sbs + 2 * sbs_slot);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pbuf + (kF8 ? 2 * g.n_k * kN : 0));
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* tfull = bars + 2 * S;
@@ -362,6 +370,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
         sc_tok = reinterpret_cast<const float*>(slot + sc.s[0].lead);
         s_wg = reinterpret_cast<const float*>(slot + span_a + sc.s[1].lead);
         s_wu = reinterpret_cast<const float*>(slot + span_a + span_w + sc.s[2].lead);
+        // (weight block scale x token scale) for every (tile, K block, token);
+        // padding tokens get 0.  The previous item's K loop, the last reader of
+        // pbuf, ended before that item's store phase and its barriers.
+        for (int i = 32 * ew + lane; i < n_k * kN; i += 32 * kEpiWarps) {
+          const int kb = i / kN, t = i - kb * kN;
+          const float st = t < it.n ? sc_tok[t * n_k + kb] : 0.0f;
+          pbuf[i] = s_wg[kb] * st;
+          pbuf[n_k * kN + i] = s_wu[kb] * st;
+        }
+        epi_sync();
       }
       float acc0[kCols], acc1[kCols];
 #pragma unroll
@@ -373,19 +391,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
         const uint32_t ta0 = tmem + tl + tb * kAcc + c0;
         if constexpr (kF8) {
           // block-FP8: partial x (weight block scale x token scale), 16
-          // columns of both tiles under one TMEM wait at a time
+          // columns of both tiles under one TMEM wait at a time; the products
+          // come from pbuf as broadcast vectors
           static_assert(kCols % 16 == 0, "x16 loads per tile");
-          const float wg = s_wg[kb], wu = s_wu[kb];
 #pragma unroll
           for (int c4 = 0; c4 < kCols / 16; ++c4) {
             if (c0 + 16 * c4 < n16) {
-              uint32_t va[16], vb[16];
-              tc::tmem_ld16x2(ta0 + 16 * c4, ta0 + kN + 16 * c4, va, vb);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float s = sc_tok[(c0 + 16 * c4 + i) * n_k + kb];
-                acc0[16 * c4 + i] = fmaf(__uint_as_float(va[i]), wg * s, acc0[16 * c4 + i]);
-                acc1[16 * c4 + i] = fmaf(__uint_as_float(vb[i]), wu * s, acc1[16 * c4 + i]);
+              for (int tile = 0; tile < 2; ++tile) {
+                uint32_t va[16];
+                tc::tmem_ld16(ta0 + tile * kN + 16 * c4, va);
+                const float4* ps = reinterpret_cast<const float4*>(
+                    pbuf + (tile * n_k + kb) * kN + c0 + 16 * c4);
+                float* acc = tile == 0 ? acc0 : acc1;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  const float4 s4 = ps[q4];
+                  const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    const int c = 16 * c4 + 4 * q4 + i;
+                    acc[c] = fmaf(__uint_as_float(va[4 * q4 + i]), ss[i], acc[c]);
+                  }
+                }
               }
             }
           }
@@ -520,8 +548,9 @@ size_t smem_bytes(int n_k) {
   const size_t slot = C::kF8 ? (((size_t)C::kN * n_k * 4 + 32 + 15) & ~(size_t)15) +
                                    2 * (((size_t)n_k * 4 + 32 + 15) & ~(size_t)15)
                              : 0;
+  const size_t prod = C::kF8 ? (size_t)2 * n_k * C::kN * 4 : 0;
   return 1024 + (size_t)C::kStages * C::kStageBytes + (size_t)C::kN * kTile * 4 + 2 * slot +
-         (2 * C::kStages + 2 * C::kNumBuf + 4) * 8 + 16 + (3 * kMaxExperts + 1) * 4;
+         prod + (2 * C::kStages + 2 * C::kNumBuf + 4) * 8 + 16 + (3 * kMaxExperts + 1) * 4;
 }
 
 const void* kernel_of(int kind) {
