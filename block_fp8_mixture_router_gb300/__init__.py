@@ -34,6 +34,7 @@ MOE_OPT_LAUNCH_EPOCH = 4
 MOE_OPT_BATCH_INVARIANT = 5
 MOE_OPT_ROUTER_BF16 = 6
 TAG_WRAP = 0x7FFFFFFF
+TAG_CLEAR = TAG_WRAP - 4096  # tags of the role-split decode kernels stay below TAG_WRAP
 PATH_AUTO, PATH_DECODE, PATH_PROMPT, PATH_DECODE_CHAINED, PATH_PROMPT_MMA = 0, 1, 2, 3, 4
 PATH_DECODE_ROWS = 6  # the role-split multi-row decode kernel for 2..16 rows
 
@@ -41,7 +42,8 @@ EXPORTED = ("moe_create", "moe_load_weights", "moe_forward", "moe_forward_host",
             "moe_quantize", "moe_expert_activations", "moe_set_option", "moe_required_bytes",
             "moe_last_device_status", "moe_destroy", "moe_status_string",
             "moe_profile_forward", "moe_route_static", "moe_add_rmsnorm_quantize",
-            "moe_forward_codes", "moe_forward_addnorm")
+            "moe_forward_codes", "moe_forward_addnorm", "moe_chain_create",
+            "moe_chain_forward", "moe_chain_destroy")
 
 MOE_ROUTE_STATIC_MAX_LOGITS = 262144
 
@@ -89,6 +91,10 @@ def load_library(path: str = LIB_PATH):
     L.moe_expert_activations.argtypes = [vp, i, vp, vp, vp]
     L.moe_forward_codes.argtypes = [vp, i, vp, vp, vp]
     L.moe_forward_addnorm.argtypes = [vp, vp, vp, vp, ctypes.c_float, i, vp, vp, vp, vp]
+    L.moe_chain_create.argtypes = [ctypes.POINTER(ctypes.c_void_p), i, ip]
+    L.moe_chain_forward.argtypes = [vp, vp, vp, i, vp]
+    L.moe_chain_destroy.argtypes = [vp]
+    L.moe_chain_destroy.restype = None
     L.moe_set_option.argtypes = [vp, i, i]
     L.moe_profile_forward.argtypes = [vp, vp, vp, i, vp, vp, i, ctypes.POINTER(ctypes.c_int), vp]
     L.moe_required_bytes.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(ctypes.c_size_t)]
@@ -98,7 +104,7 @@ def load_library(path: str = LIB_PATH):
     L.moe_status_string.argtypes = [i]
     L.moe_status_string.restype = ctypes.c_char_p
     for n in EXPORTED:
-        if n not in ("moe_destroy", "moe_status_string"):
+        if n not in ("moe_destroy", "moe_status_string", "moe_chain_destroy"):
             getattr(L, n).restype = ctypes.c_int
     _lib = L
     return L
@@ -178,6 +184,22 @@ def moe_forward_addnorm(ctx, residual, x, gamma, eps: float, rows: int, h_out, x
     return load_library().moe_forward_addnorm(ctx, _ptr(residual), _ptr(x), _ptr(gamma),
                                               float(eps), rows, _ptr(h_out), _ptr(xn_out),
                                               _ptr(y), _stream(stream))
+
+
+def moe_chain_create(ctxs):
+    arr = (ctypes.c_void_p * len(ctxs))(*[c.value if isinstance(c, ctypes.c_void_p) else c
+                                          for c in ctxs])
+    h = ctypes.c_void_p()
+    rc = load_library().moe_chain_create(arr, len(ctxs), ctypes.byref(h))
+    return rc, h
+
+
+def moe_chain_forward(chain, x, y_all, rows: int, stream=None) -> int:
+    return load_library().moe_chain_forward(chain, _ptr(x), _ptr(y_all), rows, _stream(stream))
+
+
+def moe_chain_destroy(chain) -> None:
+    load_library().moe_chain_destroy(chain)
 
 
 def moe_forward_codes(ctx, rows: int, codes, scales, stream=None) -> int:
@@ -364,3 +386,36 @@ class MoELayer:
 
     def device_status(self) -> int:
         return moe_last_device_status(self.ctx)
+
+
+class MoEChain:
+    """Layers in sequence (each a MoELayer that must outlive the chain): the
+    output of layer l is the input of layer l + 1."""
+
+    def __init__(self, layers):
+        self.layers = list(layers)
+        rc, h = moe_chain_create([net.ctx for net in self.layers])
+        _check(rc, "moe_chain_create")
+        self.chain = h
+
+    def close(self):
+        if getattr(self, "chain", None):
+            moe_chain_destroy(self.chain)
+            self.chain = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def forward(self, x: torch.Tensor, y_all: torch.Tensor | None = None, stream=None):
+        """x [rows, H] bf16 -> every layer's output [n_layers, rows, H]."""
+        if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2:
+            raise ValueError("x must be a 2-D bf16 CUDA tensor")
+        x = x.contiguous()
+        if y_all is None:
+            y_all = torch.empty((len(self.layers),) + tuple(x.shape), dtype=x.dtype,
+                                device=x.device)
+        _check(moe_chain_forward(self.chain, x, y_all, x.shape[0], stream), "moe_chain_forward")
+        return y_all

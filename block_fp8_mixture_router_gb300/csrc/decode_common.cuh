@@ -164,11 +164,12 @@ __device__ __forceinline__ void publish(unsigned long long* p, unsigned long lon
 // A launch's tag is the context's epoch + 1; the last CTA to leave publishes
 // the tag as the new epoch.  A poll accepts a word whose tag equals its
 // launch's, so a tag must never come back while a word written under it
-// could still be read.  On the launch whose tag reaches kTagWrap the last CTA
-// instead clears every exchange word and restarts the epoch at 0: tags then
-// start again at 1 over words that all read 0.  Every CTA of that launch
-// fences its exchange writes before it arrives at the exit counter, so none
-// can land after the clear.
+// could still be read.  On the launch whose last tag reaches kTagClear the
+// last CTA instead clears every exchange word and restarts the epoch at 0:
+// tags then start again at 1 over words that all read 0.  (A chain launch
+// uses one tag per layer, at most kMaxChain, so tags stay below kTagWrap.)
+// Every CTA of that launch fences its exchange writes before it arrives at
+// the exit counter, so none can land after the clear.
 // Exchange words of the context (tagged logits, then the decode exchange
 // words), as the context allocates them.
 __device__ __forceinline__ void clear_exchange_words(const KArgs& a) {
@@ -177,15 +178,18 @@ __device__ __forceinline__ void clear_exchange_words(const KArgs& a) {
                                              a.d.Is + a.d.H);
   for (size_t i = threadIdx.x; i < n_log; i += blockDim.x) a.w.tlog[i] = 0ull;
   for (size_t i = threadIdx.x; i < n_xw; i += blockDim.x) a.w.xw[i] = 0ull;
+  if (a.chain.yw)
+    for (int i = threadIdx.x; i < a.d.H; i += blockDim.x) a.chain.yw[i] = 0ull;
 }
 
 // The exit of a tagged-exchange launch; every thread of the CTA calls it.
+// tag: the launch's last tag.
 __device__ __forceinline__ void launch_exit(const KArgs& a, int tag) {
   int* bar_exit = a.w.done + 3;
   int* epoch = a.w.done + 4;
   __shared__ int s_last;
   __syncthreads();
-  if (tag < kTagWrap) {
+  if (tag < kTagClear) {
     // The next launch reads the epoch, the outputs and the exchange words
     // only after this grid has completed, and stale words carry older tags.
     if (threadIdx.x == 0) {

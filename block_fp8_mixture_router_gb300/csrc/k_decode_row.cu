@@ -211,7 +211,18 @@ __device__ __forceinline__ void shared_part(const uint8_t* rows, int H, const bf
   }
 }
 
-template <int kDummy>
+// kChain = 0: one layer.  kChain = 1: the layers of a.chain in order, one row
+// passed through them (layer l's x is layer l-1's y, read as the tagged words
+// the combine publishes); every CTA keeps its role for every layer, and the
+// shared CTAs start streaming layer l+1's weights as soon as they finish
+// layer l.
+// Order this thread's earlier shared-memory accesses before bulk copies
+// that reuse the same bytes.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+template <int kChain>
 __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int G = gridDim.x, b = blockIdx.x;
@@ -236,26 +247,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
   }
   __syncthreads();
 
-  // ---- before the wait: the shared expert's weights and the router rows ----
   const uint32_t sgu_unit = 16u * (uint32_t)H * 2u;  // [8 gate; 8 up] bf16 rows
   const uint32_t sdn_unit = (uint32_t)kSdnUnit * (uint32_t)Is * 2u;
   const int sdn_m0 = is_sdn ? s2 * R.R2 : 0;
   const int sdn_rows = is_sdn ? max(0, min(R.R2, H - sdn_m0)) : 0;
   const int n_sdn_units = sdn_rows / kSdnUnit;
   const int n_sgu_units = R.Fs / 8;
+  const int n_layers = kChain ? a.chain.n : 1;
+  int base_tag = 0;     // thread 0: the first layer's launch tag
+  int layer_tag = 0;    // every thread: the tag of the layer last computed
+  for (int l = 0; l < n_layers; ++l) {
+  // this layer's weights; the routed CTA's barriers complete once per layer
+  const DevLayer LW = kChain ? a.chain.layers[l] : a.L;
+  const uint32_t lp = (uint32_t)(l & 1);
+
+  // ---- before the wait: the shared expert's weights and the router rows ----
+  // (later layers: right after the previous layer, whose ring reads are done)
   if (threadIdx.x == 0) {
+    if (l > 0) fence_proxy_async();
     if (is_sgu) {
       for (int u = 0; u < n_sgu_units && u < kSguSlots; ++u) {
         uint8_t* dst = L.data + (size_t)u * sgu_unit;
         const int n0 = s1 * R.Fs + 8 * u;
         mbar_expect(&L.bar[u], sgu_unit);
-        bulk_copy(dst, a.L.ws13 + (size_t)n0 * H, sgu_unit / 2, &L.bar[u]);
-        bulk_copy(dst + sgu_unit / 2, a.L.ws13 + (size_t)(Is + n0) * H, sgu_unit / 2, &L.bar[u]);
+        bulk_copy(dst, LW.ws13 + (size_t)n0 * H, sgu_unit / 2, &L.bar[u]);
+        bulk_copy(dst + sgu_unit / 2, LW.ws13 + (size_t)(Is + n0) * H, sgu_unit / 2, &L.bar[u]);
       }
     } else if (is_sdn) {
       for (int u = 0; u < n_sdn_units && u < kSdnSlots; ++u) {
         mbar_expect(&L.bar[u], sdn_unit);
-        bulk_copy(L.data + (size_t)u * sdn_unit, a.L.ws2 + (size_t)(sdn_m0 + kSdnUnit * u) * Is,
+        bulk_copy(L.data + (size_t)u * sdn_unit, LW.ws2 + (size_t)(sdn_m0 + kSdnUnit * u) * Is,
                   sdn_unit, &L.bar[u]);
       }
     }
@@ -273,13 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
 #pragma unroll
     for (int i = 0; i < kMaxV; ++i)
       wv[h][i] = (er < E && i < nv)
-                     ? __ldg(reinterpret_cast<const float4*>(a.L.wr + (size_t)er * H + k0 +
+                     ? __ldg(reinterpret_cast<const float4*>(LW.wr + (size_t)er * H + k0 +
                                                              128 * i + 4 * lane))
                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   }
 #pragma unroll
   for (int i = 0; i < kMaxV; ++i)
-    gw[i] = i < nv ? __ldg(reinterpret_cast<const uint2*>(a.L.gate + k0 + 128 * i + 4 * lane))
+    gw[i] = i < nv ? __ldg(reinterpret_cast<const uint2*>(LW.gate + k0 + 128 * i + 4 * lane))
                    : make_uint2(0u, 0u);
   // the add-norm's gamma (immutable) before the wait as well
   const bool addnorm = a.an.residual != nullptr;
@@ -289,19 +310,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     gn[i] = (addnorm && i < nv)
                 ? __ldg(reinterpret_cast<const uint2*>(a.an.gamma + k0 + 128 * i + 4 * lane))
                 : make_uint2(0u, 0u);
-  pdl_wait();
-  pdl_trigger();
-  if (threadIdx.x == 0) sm->tag = ld_acquire(epoch) + 1;
+  if (l == 0) {
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x == 0) base_tag = ld_acquire(epoch) + 1;
+  }
+  if (threadIdx.x == 0) sm->tag = base_tag + l;
 
   // ---- router logits, x quantisation (1 x 128 groups) and the shared gate ----
   float acc2[2] = {0.0f, 0.0f}, gacc = 0.0f, gmx = 0.0f;
   // both slices' x loads in flight together (the stores below could alias
   // x as far as the compiler knows, so it would not hoist the second)
   uint2 xr[kMaxV];
+  if (kChain && l > 0) {
+    // x = the previous layer's y: four tagged words per lane (bf16 values)
+    const unsigned long long ptag = (unsigned long long)(unsigned)layer_tag << 32;
 #pragma unroll
-  for (int i = 0; i < kMaxV; ++i)
-    xr[i] = i < nv ? __ldcg(reinterpret_cast<const uint2*>(a.x + k0 + 128 * i + 4 * lane))
-                   : make_uint2(0u, 0u);
+    for (int i = 0; i < kMaxV; ++i) {
+      if (i >= nv) {
+        xr[i] = make_uint2(0u, 0u);
+        continue;
+      }
+      const unsigned long long* src = a.chain.yw + k0 + 128 * i + 4 * lane;
+      float v[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) v[c] = poll_tagged(src + c, ptag, status);
+      const __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
+      const __nv_bfloat162 p1 = __floats2bfloat162_rn(v[2], v[3]);
+      xr[i].x = *reinterpret_cast<const uint32_t*>(&p0);
+      xr[i].y = *reinterpret_cast<const uint32_t*>(&p1);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i)
+      xr[i] = i < nv ? __ldcg(reinterpret_cast<const uint2*>(a.x + k0 + 128 * i + 4 * lane))
+                     : make_uint2(0u, 0u);
+  }
   if (addnorm) {
     // residual add and RMS norm in this pass (every CTA the whole row): h =
     // bf16(residual + x), r = 1 / sqrt(sum(h^2) / H + eps) in fp32 over a
@@ -433,7 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
       }
     }
   }
-  const unsigned long long tag = (unsigned long long)(unsigned)sm->tag << 32;
+  layer_tag = sm->tag;
+  const unsigned long long tag = (unsigned long long)(unsigned)layer_tag << 32;
   if (threadIdx.x < 2) {
     const int ee = b + G * threadIdx.x;
     if (ee < E) {
@@ -472,14 +517,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     const int ldu = H + kRowPad;                        // row stride in shared memory
     const size_t ubytes = (size_t)16 * ldu;             // one [8 gate; 8 up] unit
     const int ldd = I + kRowPad;
-    const uint8_t* W13 = a.L.w13 + (size_t)e * 2 * I * H;
-    const float* S13 = a.L.s13 + (size_t)e * (2 * I / kGroup) * nbh;
+    const uint8_t* W13 = LW.w13 + (size_t)e * 2 * I * H;
+    const float* S13 = LW.s13 + (size_t)e * (2 * I / kGroup) * nbh;
     uint8_t* w2s = L.data + (size_t)nu * ubytes;  // [128][ldd]
     const float *lg_, *lu_, *ld_;
     int dg, du, dd;
     const uint32_t bg = span16(S13 + (size_t)(n0 / kGroup) * nbh, nbh, &lg_, &dg);
     const uint32_t bu = span16(S13 + (size_t)((I + n0) / kGroup) * nbh, nbh, &lu_, &du);
-    const uint32_t bd = span16(a.L.s2 + ((size_t)e * nbh + p) * nbi, nbi, &ld_, &dd);
+    const uint32_t bd = span16(LW.s2 + ((size_t)e * nbh + p) * nbi, nbi, &ld_, &dd);
     const size_t wslot = al16((size_t)(nbh + 8) * 4);
     float* sgp = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(L.wsc)) + dg;
     float* sup = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(L.wsc) + wslot) + du;
@@ -487,6 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     // copies, one row each, issued in parallel: warp 0 the gate/up rows of
     // the units (bar u), warp 1 the down rows (bar 6), warp 2 the scales
     // (bar 7); each barrier's byte count is set before its copies
+    // (a later layer's copies land where the previous layer's rows were read)
+    if (kChain && l > 0 && warp < 3) fence_proxy_async();
     if (warp == 0) {
       if (lane < nu) mbar_expect(&L.bar[lane], 2 * uhalf);
       __syncwarp();
@@ -499,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     } else if (warp == 1) {
       if (lane == 0) mbar_expect(&L.bar[6], (uint32_t)kGroup * I);
       __syncwarp();
-      const uint8_t* W2 = a.L.w2 + ((size_t)e * H + (size_t)kGroup * p) * I;
+      const uint8_t* W2 = LW.w2 + ((size_t)e * H + (size_t)kGroup * p) * I;
       for (int m = lane; m < kGroup; m += 32)
         bulk_copy(w2s + (size_t)m * ldd, W2 + (size_t)m * I, (uint32_t)I, &L.bar[6]);
     } else if (warp == 2 && lane == 0) {
@@ -527,8 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     const int wpu = kW / nu;
     const int u = warp % nu, part = warp / nu;
     const int nsl = H / 64, per = nsl / wpu;
-    copy_wait(&L.bar[7], 0, status);
-    copy_wait(&L.bar[u], 0, status);
+    copy_wait(&L.bar[7], lp, status);
+    copy_wait(&L.bar[u], lp, status);
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     routed_part(L.data + (size_t)u * ubytes, ldu, sgp, sup, L.xq, L.sx, part * per,
                 part * per + per, acc);
@@ -580,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     }
     __syncthreads();
     // down rows [128p + 16w, +16) of expert e over the full I
-    copy_wait(&L.bar[6], 0, status);
+    copy_wait(&L.bar[6], lp, status);
     {
       // 128 rows = 8 m-tiles: warp w takes m-tile w % 8 over K half w / 8;
       // the second half's sums are added through shared memory
@@ -630,14 +677,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
       float y = 0.0f;
       for (int j = 0; j < k; ++j) y = fmaf(sm->w[j], sm->comb[j][threadIdx.x], y);
       y = fmaf(sm->gamma, sm->comb[k][threadIdx.x], y);
-      a.y[m0 + threadIdx.x] = __float2bfloat16_rn(y);
+      const bf16 yb = __float2bfloat16_rn(y);
+      a.y[(kChain ? (size_t)l * H : 0) + m0 + threadIdx.x] = yb;
+      if (kChain) publish(a.chain.yw + m0 + threadIdx.x, tag, __bfloat162float(yb));
     }
   } else if (is_sgu) {
     // ---- shared gate/up: units of [8 gate; 8 up] rows, all warps split K ----
     const int nsl = H / 32, per = nsl / kW;
     for (int uu = 0; uu < n_sgu_units; ++uu) {
       const int slot = uu % kSguSlots;
-      copy_wait(&L.bar[slot], (uint32_t)((uu / kSguSlots) & 1), status);
+      // the slot's completions so far: its uses in earlier layers, then here
+      const int uses = (n_sgu_units - slot + kSguSlots - 1) / kSguSlots;
+      copy_wait(&L.bar[slot], (uint32_t)((l * uses + uu / kSguSlots) & 1), status);
       float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       shared_part(L.data + (size_t)slot * sgu_unit, H, L.xs, warp * per, warp * per + per, acc);
       float* red = L.red;
@@ -650,8 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
         uint8_t* dst = L.data + (size_t)slot * sgu_unit;
         const int n0 = s1 * R.Fs + 8 * un;
         mbar_expect(&L.bar[slot], sgu_unit);
-        bulk_copy(dst, a.L.ws13 + (size_t)n0 * H, sgu_unit / 2, &L.bar[slot]);
-        bulk_copy(dst + sgu_unit / 2, a.L.ws13 + (size_t)(Is + n0) * H, sgu_unit / 2,
+        bulk_copy(dst, LW.ws13 + (size_t)n0 * H, sgu_unit / 2, &L.bar[slot]);
+        bulk_copy(dst + sgu_unit / 2, LW.ws13 + (size_t)(Is + n0) * H, sgu_unit / 2,
                   &L.bar[slot]);
       }
       if (warp == 0 && q == 0) {
@@ -674,7 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
     __syncthreads();
     for (int uu = warp; uu < n_sdn_units; uu += kW) {
       const int slot = uu % kSdnSlots;
-      copy_wait(&L.bar[slot], (uint32_t)((uu / kSdnSlots) & 1), status);
+      const int uses = (n_sdn_units - slot + kSdnSlots - 1) / kSdnSlots;
+      copy_wait(&L.bar[slot], (uint32_t)((l * uses + uu / kSdnSlots) & 1), status);
       const uint8_t* rows = L.data + (size_t)slot * sdn_unit;
       for (int tile = 0; tile < kSdnUnit / 16; ++tile) {
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -699,10 +751,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
       if (lane == 0 && un < n_sdn_units) {
         mbar_expect(&L.bar[slot], sdn_unit);
         bulk_copy(L.data + (size_t)slot * sdn_unit,
-                  a.L.ws2 + (size_t)(sdn_m0 + kSdnUnit * un) * Is, sdn_unit, &L.bar[slot]);
+                  LW.ws2 + (size_t)(sdn_m0 + kSdnUnit * un) * Is, sdn_unit, &L.bar[slot]);
       }
     }
   }
+
+  // every thread is done with this layer's shared scratch (sm->tag, the
+  // top-k, the exchange staging) before the next layer writes it
+  __syncthreads();
+  }  // layers
 
   // ---- exit: the last CTA advances the launch tag (or clears the words) ----
   launch_exit(a, sm->tag);
@@ -732,12 +789,19 @@ bool decode_row_fits(int G, int H, int E, int k, int I, int Is, size_t budget) {
 }
 
 cudaError_t setup_decode_row(size_t max_smem) {
-  return cudaFuncSetAttribute(k_decode_row<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const cudaError_t e = cudaFuncSetAttribute(
+      k_decode_row<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_decode_row<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)max_smem);
 }
 
 cudaError_t launch_decode_row(const KArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s) {
   return launch_pdl(k_decode_row<0>, dim3(grid), dim3(kThreads), smem, s, pdl, a);
+}
+
+cudaError_t launch_decode_chain(const KArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s) {
+  return launch_pdl(k_decode_row<1>, dim3(grid), dim3(kThreads), smem, s, pdl, a);
 }
 
 }  // namespace moe

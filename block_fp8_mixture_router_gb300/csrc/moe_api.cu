@@ -970,7 +970,7 @@ int moe_set_option(moe_ctx* c, int option, int value) {
       return MOE_OK;
     case MOE_OPT_POLL_LIMIT:
     case MOE_OPT_LAUNCH_EPOCH: {
-      if (value < 0 || (option == MOE_OPT_LAUNCH_EPOCH && value >= kTagWrap))
+      if (value < 0 || (option == MOE_OPT_LAUNCH_EPOCH && value >= kTagClear))
         return MOE_ERR_INVALID_ARG;
       DeviceGuard guard(c->device);
       if (!guard.ok) return MOE_ERR_CUDA;
@@ -1015,6 +1015,101 @@ int moe_last_device_status(moe_ctx* c) {
     }
   }
   return flag ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+}
+
+// ---- layers in sequence ------------------------------------------------------
+
+struct moe_chain {
+  int n = 0;
+  std::vector<moe_ctx*> ctx;
+  DevLayer* table = nullptr;          // [n] on the device
+  unsigned long long* yw = nullptr;   // [H] tagged y words (one-row chain kernel)
+};
+
+int moe_chain_create(moe_ctx* const* layers, int n_layers, moe_chain** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!layers || n_layers < 1) return MOE_ERR_INVALID_ARG;
+  if (n_layers > kMaxChain) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const moe_ctx* c0 = layers[0];
+  if (!c0) return MOE_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    const moe_ctx* c = layers[l];
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (!c->loaded) return MOE_ERR_NOT_LOADED;
+    if (c->device != c0->device || c->cfg.hidden != c0->cfg.hidden ||
+        c->cfg.n_experts != c0->cfg.n_experts || c->cfg.top_k != c0->cfg.top_k ||
+        c->cfg.inter != c0->cfg.inter || c->cfg.shared_inter != c0->cfg.shared_inter ||
+        c->cfg.act_group != c0->cfg.act_group)
+      return MOE_ERR_UNSUPPORTED_SHAPE;
+  }
+  DeviceGuard guard(c0->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  moe_chain* ch = new (std::nothrow) moe_chain();
+  if (!ch) return MOE_ERR_CUDA;
+  ch->n = n_layers;
+  ch->ctx.assign(layers, layers + n_layers);
+  std::vector<DevLayer> host(n_layers);
+  for (int l = 0; l < n_layers; ++l) host[l] = layers[l]->L;
+  const size_t nt = sizeof(DevLayer) * n_layers, ny = sizeof(unsigned long long) * c0->cfg.hidden;
+  if (cudaMalloc(&ch->table, nt) != cudaSuccess || cudaMalloc(&ch->yw, ny) != cudaSuccess ||
+      cudaMemcpy(ch->table, host.data(), nt, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(ch->yw, 0, ny) != cudaSuccess) {
+    cudaGetLastError();
+    if (ch->table) cudaFree(ch->table);
+    if (ch->yw) cudaFree(ch->yw);
+    delete ch;
+    return MOE_ERR_CUDA;
+  }
+  *out = ch;
+  return MOE_OK;
+}
+
+int moe_chain_forward(moe_chain* ch, const void* x, void* y_all, int rows, void* stream) {
+  if (!ch || rows < 0) return MOE_ERR_INVALID_ARG;
+  moe_ctx* c0 = ch->ctx[0];
+  for (moe_ctx* c : ch->ctx)
+    if (rows > c->cfg.max_rows) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0) return MOE_OK;
+  if (!x || !y_all) return MOE_ERR_INVALID_ARG;
+  const size_t H = c0->cfg.hidden, nb = (size_t)rows * H * 2;
+  if (overlaps(x, nb, y_all, nb * ch->n)) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)x | (uintptr_t)y_all) & 15) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(c0->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (rows == 1 && use_decode(c0, 1) && use_row(c0, 1)) {
+    // one launch over every layer; the first context's workspace and launch
+    // tags serve the whole chain
+    c0->last_stream = s;
+    c0->fwd_rows = 0;  // its checking buffers now hold the last layer's values
+    KArgs a = make_args(c0, x, y_all, 1);
+    a.chain = Chain{ch->table, ch->n, ch->yw};
+    return check_launch(launch_decode_chain(a, c0->sm_count, c0->row_smem, c0->opt_pdl != 0, s));
+  }
+  // otherwise each layer's forward, y of layer l the input of layer l + 1
+  const char* src = static_cast<const char*>(x);
+  char* dst = static_cast<char*>(y_all);
+  for (int l = 0; l < ch->n; ++l) {
+    moe_ctx* c = ch->ctx[l];
+    c->last_stream = s;
+    const int rc = run_forward(c, src, dst, rows, s);
+    if (rc != MOE_OK) return rc;
+    src = dst;
+    dst += nb;
+  }
+  return MOE_OK;
+}
+
+void moe_chain_destroy(moe_chain* ch) {
+  if (!ch) return;
+  {
+    DeviceGuard guard(ch->ctx[0]->device);
+    cudaDeviceSynchronize();
+    cudaFree(ch->table);
+    cudaFree(ch->yw);
+  }
+  delete ch;
 }
 
 void moe_destroy(moe_ctx* c) {

@@ -27,9 +27,12 @@ constexpr int kDecodeRows = 16;   // rows at or below which the decode kernels r
 // [kPollLimitWord] tries before a poll of another CTA's exchange word gives
 // up (0 = the kernels' default; a checking option).
 constexpr int kPollLimitWord = 15;
-// The role-split decode kernels' launch tags run from 1 to kTagWrap; the
-// launch that reaches it clears the exchange words and restarts the epoch.
+// The role-split decode kernels' launch tags stay below kTagWrap: the launch
+// whose last tag reaches kTagClear clears the exchange words and restarts the
+// epoch, and one launch uses at most kMaxChain tags (one per layer).
 constexpr int kTagWrap = 0x7FFFFFFF;
+constexpr int kMaxChain = 4096;
+constexpr int kTagClear = kTagWrap - kMaxChain;
 
 struct Dims {
   int T, H, E, k, I, Is;
@@ -92,13 +95,22 @@ struct AddNorm {
   int pre_q;             // 1: w.xq / w.sx already hold the normed rows' codes
 };
 
+// Layers passed through in one launch (the one-row chain kernel): n layers'
+// weights, and the words through which layer l's y becomes layer l+1's x.
+struct Chain {
+  const DevLayer* layers;      // [n] device array
+  int n;
+  unsigned long long* yw;      // [H] tagged y words
+};
+
 struct KArgs {
   Dims d;
   DevLayer L;
   DevWork w;
   const bf16* x;  // the layer's input; with an add-norm, the block output added to residual
-  bf16* y;
+  bf16* y;        // the layer's output; in a chain, [n][H] (every layer's y)
   AddNorm an;
+  Chain chain;    // n == 0: one layer
 };
 
 // Upper bound of sum_e ceil(count_e / kChunk) over experts with sum_e count_e = T*k.
@@ -123,6 +135,8 @@ size_t decode_row_smem(int G, int H, int E, int k, int I, int Is);
 bool decode_row_fits(int G, int H, int E, int k, int I, int Is, size_t budget);
 cudaError_t setup_decode_row(size_t max_smem);
 cudaError_t launch_decode_row(const KArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s);
+// The one-row kernel over the layers of a.chain in one launch.
+cudaError_t launch_decode_chain(const KArgs& a, int grid, size_t smem, bool pdl, cudaStream_t s);
 
 // ---- 2..16-row decode kernel (k_decode_rows.cu) ---------------------------------
 size_t decode_rows_smem(int H);

@@ -317,9 +317,10 @@ int moe_forward_codes(moe_ctx* ctx, int rows, uint8_t* codes, float* scales, voi
  * and restarts the counters, and the next forward is exact again.  Waits for
  * the kernel's own copies keep the built-in limit.
  * MOE_OPT_LAUNCH_EPOCH: the launch epoch of the role-split decode kernels
- * (0 <= value < 2^31 - 1).  Their exchange words carry the launch's tag,
- * epoch + 1; the launch whose tag reaches 2^31 - 1 clears every word and
- * restarts the epoch at 0, so a tag never comes back over a stale word.
+ * (0 <= value < 2^31 - 1 - 4096).  Their exchange words carry the launch's
+ * tag, epoch + 1 (a chain launch uses one tag per layer); the launch whose
+ * last tag reaches 2^31 - 1 - 4096 clears every word and restarts the epoch
+ * at 0, so a tag never comes back over a stale word.
  * Defined by: PR #920 "drama: Drama 3 (fishaudio/drama-3) text-to-speech on
  * CUDA", section "Receipt" (backbone outputs at chunk sizes 1, 7 and 128 are
  * hash-identical) against PR #939, section "Determinism and request state"
@@ -366,6 +367,40 @@ int moe_required_bytes(const moe_config* cfg, size_t* bytes);
  * GPU", conversation, the follow-up fixes (a bad value is refused by name with
  * an error, not trapped on). */
 int moe_last_device_status(moe_ctx* ctx);
+
+/* Layers in sequence: the backbone's MoE layers, the output of layer l the
+ * input of layer l + 1 (nothing in between), as one object over contexts that
+ * stay owned by the caller and must outlive it.  All contexts loaded, on one
+ * device, with one shape; at most 4096 layers (MOE_ERR_UNSUPPORTED_SHAPE
+ * otherwise).  Allocates a small device table; synchronous.
+ * Defined by: PR #939 "drama3: Fish Audio Drama 3 text to speech on one CUDA
+ * GPU", section "What it adds" (the frame step runs the next backbone row as
+ * one CUDA graph); PR #927 "drama: the backbone chain launches with
+ * programmatic dependent launch", section "What this changes". */
+typedef struct moe_chain moe_chain;
+int moe_chain_create(moe_ctx* const* layers, int n_layers, moe_chain** out);
+
+/* x bf16 [rows][H] through every layer: y_all bf16 [n_layers][rows][H] holds
+ * each layer's output (device pointers, 16-byte aligned, x apart from
+ * y_all).  One row on a shape the one-row kernel serves runs as ONE launch
+ * over all layers: every CTA keeps its role from layer to layer, a layer's
+ * input is read from the words the previous layer's combine publishes, and
+ * the CTAs that finish a layer early start streaming the next layer's shared
+ * expert at once.  That launch uses the first context's workspace and launch
+ * tags (a forward on that context in between is fine when stream-ordered);
+ * moe_forward_codes on it is refused afterwards.  More rows run each layer's
+ * moe_forward in order.  rows <= every context's max_rows.  Asynchronous on
+ * `stream`.
+ * Defined by: PR #939 "drama3: Fish Audio Drama 3 text to speech on one CUDA
+ * GPU", section "What it adds" (the frame step runs the next backbone row as
+ * one CUDA graph) and section "Precision" (the layer of moe_forward). */
+int moe_chain_forward(moe_chain* chain, const void* x, void* y_all, int rows, void* stream);
+
+/* Release the chain's table.  NULL is accepted; the contexts stay.
+ * Defined by: PR #925 "drama: load the checkpoint with direct I/O in file
+ * order and build the codec on its own thread", conversation (the worker
+ * thread that owns the modules releases them). */
+void moe_chain_destroy(moe_chain* chain);
 
 /* Release everything the context owns.  NULL is accepted.
  * Defined by: PR #925 "drama: load the checkpoint with direct I/O in file

@@ -115,7 +115,7 @@ def _declaration_comments():
     every function include/moe.h declares."""
     src = open(os.path.join(ROOT, "include", "moe.h")).read()
     out = {}
-    for m in re.finditer(r"/\*((?:(?!\*/).)*)\*/\s*(?:enum\s*\{[^}]*\};\s*)?(?:#define [^\n]*\n\s*)?"
+    for m in re.finditer(r"/\*((?:(?!\*/).)*)\*/\s*(?:enum\s*\{[^}]*\};\s*)?(?:#define [^\n]*\n\s*)?(?:typedef struct \w+ \w+;\s*)?"
                          r"(?:int|void|const char\*)\s+(moe_[a-z_]+)\s*\(", src, flags=re.S):
         out[m.group(2)] = m.group(1)
     return out

@@ -47,7 +47,7 @@ def test_poll_limit_option_range(case):
     ctx = case.moe.ctx
     assert m.moe_set_option(ctx, m.MOE_OPT_POLL_LIMIT, -1) == m.MOE_ERR_INVALID_ARG
     assert m.moe_set_option(ctx, m.MOE_OPT_LAUNCH_EPOCH, -1) == m.MOE_ERR_INVALID_ARG
-    assert m.moe_set_option(ctx, m.MOE_OPT_LAUNCH_EPOCH, m.TAG_WRAP) == m.MOE_ERR_INVALID_ARG
+    assert m.moe_set_option(ctx, m.MOE_OPT_LAUNCH_EPOCH, m.TAG_CLEAR) == m.MOE_ERR_INVALID_ARG
     assert m.moe_set_option(ctx, m.MOE_OPT_POLL_LIMIT, 0) == m.MOE_OK
 
 
@@ -71,8 +71,8 @@ def test_launch_tags_across_the_wrap(case):
     xs = {1: case.x(1, tag="wrap1"), 3: case.x(3, tag="wrap3"), 4: case.x(4, tag="wrap4")}
     ref = {T: case.moe.forward(x).clone() for T, x in xs.items()}
     torch.cuda.synchronize()
-    case.moe.set_option(m.MOE_OPT_LAUNCH_EPOCH, m.TAG_WRAP - 3)
-    # tags W-2, W-1, W (clears the words; epoch back to 0), then 1, 2, 3, ...
+    case.moe.set_option(m.MOE_OPT_LAUNCH_EPOCH, m.TAG_CLEAR - 3)
+    # tags C-2, C-1, C (clears the words; epoch back to 0), then 1, 2, 3, ...
     order = [1, 3, 4, 3, 1, 4, 1, 3]
     outs = [(T, case.moe.forward(xs[T]).clone()) for T in order]
     torch.cuda.synchronize()
