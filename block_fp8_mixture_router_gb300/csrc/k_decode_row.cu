@@ -7,8 +7,9 @@
 //   shared gate/up CTA s < P: shared SwiGLU features [s*Fs, s*Fs + Fs);
 //   shared down CTA (the rest): a block of the shared expert's output rows.
 //
-// All CTAs compute router logits (experts b and b + G) while quantising x
-// and taking the shared gate's dot product from the same registers.  Results
+// Every CTA quantises x and takes the shared gate's dot product in one
+// register pass; the routed CTAs also compute the router logits (experts 2b
+// and 2b + 1) in it.  Results
 // move between CTAs as 64-bit {launch tag, value} words in global memory,
 // each written once per launch and polled until its tag is current:
 //   logits            every CTA computes the same top-k;
@@ -281,7 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
       }
     }
   }
-  // router rows: experts b and b + G; each warp covers a 1/kW share of K of both
+  // router rows: the routed CTAs compute every logit, experts 2b and 2b + 1
+  // (the shared CTAs' own work would delay theirs); each warp covers a 1/kW
+  // share of K of both
   const int keighth = H / kW;
   const int k0 = warp * keighth;
   constexpr int kMaxV = kMaxRowH / kW / 128 > 0 ? kMaxRowH / kW / 128 : 1;
@@ -290,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
   uint2 gw[kMaxV];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int er = b + G * h;
+    const int er = is_routed ? 2 * b + h : E;
 #pragma unroll
     for (int i = 0; i < kMaxV; ++i)
       wv[h][i] = (er < E && i < nv)
@@ -332,9 +335,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
         continue;
       }
       const unsigned long long* src = a.chain.yw + k0 + 128 * i + 4 * lane;
+      // the four words' loads in flight together; only stale ones polled again
+      unsigned long long w4[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) w4[c] = ld_relaxed64(src + c);
       float v[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) v[c] = poll_tagged(src + c, ptag, status);
+      for (int c = 0; c < 4; ++c)
+        v[c] = (w4[c] & 0xFFFFFFFF00000000ull) == ptag ? __uint_as_float((uint32_t)w4[c])
+                                                        : poll_tagged(src + c, ptag, status);
       const __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
       const __nv_bfloat162 p1 = __floats2bfloat162_rn(v[2], v[3]);
       xr[i].x = *reinterpret_cast<const uint32_t*>(&p0);
@@ -479,8 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
   }
   layer_tag = sm->tag;
   const unsigned long long tag = (unsigned long long)(unsigned)layer_tag << 32;
-  if (threadIdx.x < 2) {
-    const int ee = b + G * threadIdx.x;
+  if (threadIdx.x < 2 && is_routed) {
+    const int ee = 2 * b + threadIdx.x;
     if (ee < E) {
       float v = 0.0f;
 #pragma unroll
@@ -776,8 +785,9 @@ size_t decode_row_smem(int G, int H, int E, int k, int I, int Is) {
 // bytes of shared memory per CTA.
 bool decode_row_fits(int G, int H, int E, int k, int I, int Is, size_t budget) {
   if (H % (kW * 128) != 0 || H > kMaxRowH) return false;
-  if (E > 2 * G || E > 32 * kW || k > kMaxTopK || kGroup % k != 0 || kGroup / k > 16) return false;
+  if (E > 32 * kW || k > kMaxTopK || kGroup % k != 0 || kGroup / k > 16) return false;
   const Roles R = make_roles(G, H, k, I, Is);
+  if (E > 2 * R.nR) return false;  // the routed CTAs compute two logits each
   if (R.nS2 < 1 || I % R.P != 0 || Is % R.P != 0) return false;
   if (R.F < 8 || R.F % 8 != 0 || kGroup % R.F != 0 || kW % (R.F / 8) != 0) return false;
   if (kW % (kGroup / 16) != 0 || (I / 64) % (kW / (kGroup / 16)) != 0) return false;
