@@ -178,8 +178,6 @@ __device__ __forceinline__ void clear_exchange_words(const KArgs& a) {
                                              a.d.Is + a.d.H);
   for (size_t i = threadIdx.x; i < n_log; i += blockDim.x) a.w.tlog[i] = 0ull;
   for (size_t i = threadIdx.x; i < n_xw; i += blockDim.x) a.w.xw[i] = 0ull;
-  if (a.chain.yw)
-    for (int i = threadIdx.x; i < a.d.H; i += blockDim.x) a.chain.yw[i] = 0ull;
 }
 
 // The exit of a tagged-exchange launch; every thread of the CTA calls it.
@@ -196,6 +194,7 @@ __device__ __forceinline__ void launch_exit(const KArgs& a, int tag) {
       const int old = atomicAdd(bar_exit, 1);
       if (old == (int)gridDim.x - 1) {
         *bar_exit = 0;
+        if (a.chain.n) a.w.done[6] = 0;  // the chain's combine counter
         *epoch = tag;
       }
     }
@@ -212,6 +211,7 @@ __device__ __forceinline__ void launch_exit(const KArgs& a, int tag) {
   __syncthreads();
   if (threadIdx.x == 0) {
     *bar_exit = 0;
+    if (a.chain.n) a.w.done[6] = 0;
     *epoch = 0;
   }
 }

@@ -213,10 +213,10 @@ __device__ __forceinline__ void shared_part(const uint8_t* rows, int H, const bf
 }
 
 // kChain = 0: one layer.  kChain = 1: the layers of a.chain in order, one row
-// passed through them (layer l's x is layer l-1's y, read as the tagged words
-// the combine publishes); every CTA keeps its role for every layer, and the
-// shared CTAs start streaming layer l+1's weights as soon as they finish
-// layer l.
+// passed through them (layer l's x is layer l-1's y, read once a counter of
+// the routed CTAs' finished combines says it is complete); every CTA keeps
+// its role for every layer, and the shared CTAs start streaming layer l+1's
+// weights as soon as they finish layer l.
 // Order this thread's earlier shared-memory accesses before bulk copies
 // that reuse the same bytes.
 __device__ __forceinline__ void fence_proxy_async() {
@@ -236,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
   Small* sm = L.sm;
   const int* epoch = a.w.done + 4;
   int* status = a.w.status;
+  int* ycount = a.w.done + 6;  // chain: routed combines done in this launch
   const Xw X = xw_of(a.w.xw, k, H, I, Is);
   const bool is_routed = b < R.nR;
   const bool is_sgu = !is_routed && b < R.nR + R.nS1;
@@ -326,29 +327,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
   // x as far as the compiler knows, so it would not hoist the second)
   uint2 xr[kMaxV];
   if (kChain && l > 0) {
-    // x = the previous layer's y: four tagged words per lane (bf16 values)
-    const unsigned long long ptag = (unsigned long long)(unsigned)layer_tag << 32;
-#pragma unroll
-    for (int i = 0; i < kMaxV; ++i) {
-      if (i >= nv) {
-        xr[i] = make_uint2(0u, 0u);
-        continue;
+    // x = the previous layer's y: once every routed CTA has counted its
+    // combine done (a release after its y stores), read it at L2
+    if (threadIdx.x == 0) {
+      const int want = R.nR * l;
+      long long it = 0;
+      while (ld_acquire(ycount) < want) {
+        if (++it > kSpin) {
+          atomicExch(status, 1);
+          break;
+        }
+        if (it > 16) __nanosleep(32);
       }
-      const unsigned long long* src = a.chain.yw + k0 + 128 * i + 4 * lane;
-      // the four words' loads in flight together; only stale ones polled again
-      unsigned long long w4[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) w4[c] = ld_relaxed64(src + c);
-      float v[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        v[c] = (w4[c] & 0xFFFFFFFF00000000ull) == ptag ? __uint_as_float((uint32_t)w4[c])
-                                                        : poll_tagged(src + c, ptag, status);
-      const __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]);
-      const __nv_bfloat162 p1 = __floats2bfloat162_rn(v[2], v[3]);
-      xr[i].x = *reinterpret_cast<const uint32_t*>(&p0);
-      xr[i].y = *reinterpret_cast<const uint32_t*>(&p1);
     }
+    __syncthreads();
+    const bf16* yp = a.y + (size_t)(l - 1) * H;
+#pragma unroll
+    for (int i = 0; i < kMaxV; ++i)
+      xr[i] = i < nv ? __ldcg(reinterpret_cast<const uint2*>(yp + k0 + 128 * i + 4 * lane))
+                     : make_uint2(0u, 0u);
   } else {
 #pragma unroll
     for (int i = 0; i < kMaxV; ++i)
@@ -686,9 +683,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_row(KArgs a) {
       float y = 0.0f;
       for (int j = 0; j < k; ++j) y = fmaf(sm->w[j], sm->comb[j][threadIdx.x], y);
       y = fmaf(sm->gamma, sm->comb[k][threadIdx.x], y);
-      const bf16 yb = __float2bfloat16_rn(y);
-      a.y[(kChain ? (size_t)l * H : 0) + m0 + threadIdx.x] = yb;
-      if (kChain) publish(a.chain.yw + m0 + threadIdx.x, tag, __bfloat162float(yb));
+      a.y[(kChain ? (size_t)l * H : 0) + m0 + threadIdx.x] = __float2bfloat16_rn(y);
+    }
+    if (kChain) {
+      // the next layer reads this y once every routed CTA has counted itself
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(ycount, 1);
+      }
     }
   } else if (is_sgu) {
     // ---- shared gate/up: units of [8 gate; 8 up] rows, all warps split K ----

@@ -1023,7 +1023,6 @@ struct moe_chain {
   int n = 0;
   std::vector<moe_ctx*> ctx;
   DevLayer* table = nullptr;          // [n] on the device
-  unsigned long long* yw = nullptr;   // [H] tagged y words (one-row chain kernel)
 };
 
 int moe_chain_create(moe_ctx* const* layers, int n_layers, moe_chain** out) {
@@ -1051,13 +1050,11 @@ int moe_chain_create(moe_ctx* const* layers, int n_layers, moe_chain** out) {
   ch->ctx.assign(layers, layers + n_layers);
   std::vector<DevLayer> host(n_layers);
   for (int l = 0; l < n_layers; ++l) host[l] = layers[l]->L;
-  const size_t nt = sizeof(DevLayer) * n_layers, ny = sizeof(unsigned long long) * c0->cfg.hidden;
-  if (cudaMalloc(&ch->table, nt) != cudaSuccess || cudaMalloc(&ch->yw, ny) != cudaSuccess ||
-      cudaMemcpy(ch->table, host.data(), nt, cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemset(ch->yw, 0, ny) != cudaSuccess) {
+  const size_t nt = sizeof(DevLayer) * n_layers;
+  if (cudaMalloc(&ch->table, nt) != cudaSuccess ||
+      cudaMemcpy(ch->table, host.data(), nt, cudaMemcpyHostToDevice) != cudaSuccess) {
     cudaGetLastError();
     if (ch->table) cudaFree(ch->table);
-    if (ch->yw) cudaFree(ch->yw);
     delete ch;
     return MOE_ERR_CUDA;
   }
@@ -1084,7 +1081,7 @@ int moe_chain_forward(moe_chain* ch, const void* x, void* y_all, int rows, void*
     c0->last_stream = s;
     c0->fwd_rows = 0;  // its checking buffers now hold the last layer's values
     KArgs a = make_args(c0, x, y_all, 1);
-    a.chain = Chain{ch->table, ch->n, ch->yw};
+    a.chain = Chain{ch->table, ch->n};
     return check_launch(launch_decode_chain(a, c0->sm_count, c0->row_smem, c0->opt_pdl != 0, s));
   }
   // otherwise each layer's forward, y of layer l the input of layer l + 1
@@ -1107,7 +1104,6 @@ void moe_chain_destroy(moe_chain* ch) {
     DeviceGuard guard(ch->ctx[0]->device);
     cudaDeviceSynchronize();
     cudaFree(ch->table);
-    cudaFree(ch->yw);
   }
   delete ch;
 }

@@ -23,7 +23,8 @@ constexpr int kMaxTopK = 16;
 constexpr int kDecodeRows = 16;   // rows at or below which the decode kernels run
 
 // Context status block (int words): [0] the device status flag, [1..12] the
-// kernels' barrier counters (DevWork::done), [13..14] unused,
+// kernels' barrier counters (DevWork::done; done[6] counts the one-row chain
+// kernel's finished combines), [13..14] unused,
 // [kPollLimitWord] tries before a poll of another CTA's exchange word gives
 // up (0 = the kernels' default; a checking option).
 constexpr int kPollLimitWord = 15;
@@ -96,11 +97,10 @@ struct AddNorm {
 };
 
 // Layers passed through in one launch (the one-row chain kernel): n layers'
-// weights, and the words through which layer l's y becomes layer l+1's x.
+// weights (layer l's y, in the output, is layer l+1's x).
 struct Chain {
   const DevLayer* layers;      // [n] device array
   int n;
-  unsigned long long* yw;      // [H] tagged y words
 };
 
 struct KArgs {
