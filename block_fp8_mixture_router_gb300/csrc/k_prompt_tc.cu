@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
     tc::fence_barrier_init();
     tc::tma_prefetch_map(&g.a);
     tc::tma_prefetch_map(&g.b);
+    tc::tma_prefetch_map(&g.bt);
   }
   if (warp == 1) {
     __syncwarp();
@@ -282,8 +283,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
                         sc.s[2].bytes, &sfull[sl]);
         }
         const int arow = it.e * g.a_rows_e + it.f * g.f_rows;
-        const int nb = (it.n + kBBox - 1) / kBBox;
-        const uint32_t bytes = (kPair ? 2 : 1) * kATileBytes + nb * kBBoxBytes;
+        // a tile of more than half the token rows takes one box of kN rows
+        // (rows past the tile belong to the next expert or lie beyond the
+        // operand, which reads zeros; the MMA does not use them), a smaller
+        // one its 16-row boxes: fewer copies for the one issuing thread
+        const bool whole = 2 * it.n > kN;
+        const int nb = whole ? 1 : (it.n + kBBox - 1) / kBBox;
+        const uint32_t bytes =
+            (kPair ? 2 : 1) * kATileBytes + (whole ? kN * kKBytes : nb * kBBoxBytes);
         for (int kb = it.kb0; kb < it.kb1; ++kb) {
           if (!tc::wait_bounded(&empty[st], ph ^ 1u, s_abort, g.status)) { ok = false; break; }
           uint8_t* sp = stages + st * C::kStageBytes;
@@ -292,8 +299,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
           tc::tma_load_2d(sp, &g.a, kb * kx, arow, &full[st]);
           if constexpr (kPair) tc::tma_load_2d(sp + kATileBytes, &g.a, kb * kx, arow + g.up_rows, &full[st]);
           uint8_t* bp = sp + (kPair ? 2 : 1) * kATileBytes;
-          for (int i = 0; i < nb; ++i)
-            tc::tma_load_2d(bp + i * kBBoxBytes, &g.b, bx, it.row0 + kBBox * i, &full[st]);
+          if (whole) {
+            tc::tma_load_2d(bp, &g.bt, bx, it.row0, &full[st]);
+          } else {
+            for (int i = 0; i < nb; ++i)
+              tc::tma_load_2d(bp + i * kBBoxBytes, &g.b, bx, it.row0 + kBBox * i, &full[st]);
+          }
           ++n_issued;
           if (++st == (uint32_t)S) { st = 0; ph ^= 1u; }
         }
@@ -675,6 +686,16 @@ cudaError_t launch_split_router(const float* wr, bf16* out, int E, int Epad, int
                                 cudaStream_t s) {
   k_split_router<<<1024, 256, 0, s>>>(wr, out, E, Epad, H);
   return cudaGetLastError();
+}
+
+int tc_gemm_tile_rows(int kind) {
+  switch (kind) {
+    case kTcRoutedGateUp: return Cfg<kTcRoutedGateUp>::kN;
+    case kTcRoutedDown: return Cfg<kTcRoutedDown>::kN;
+    case kTcSharedGateUp: return Cfg<kTcSharedGateUp>::kN;
+    case kTcSharedDown: return Cfg<kTcSharedDown>::kN;
+    default: return Cfg<kTcRouter>::kN;
+  }
 }
 
 size_t tc_gemm_smem(int kind, int n_k) {

@@ -320,6 +320,8 @@ void setup_tc(moe_ctx* c) {
   // routed gate/up: W13 [E*2I][H] x xg [slots][H]
   ok &= make_tc_map(&g[kTcRoutedGateUp].a, false, c->L.w13, E * 2 * I, H, 128);
   ok &= make_tc_map(&g[kTcRoutedGateUp].b, false, c->xg, R, H, 16);
+  ok &= make_tc_map(&g[kTcRoutedGateUp].bt, false, c->xg, R, H,
+                    (uint32_t)tc_gemm_tile_rows(kTcRoutedGateUp));
   g[kTcRoutedGateUp].n_k = (int)(H / kGroup);
   g[kTcRoutedGateUp].n_f = (int)(I / kGroup);
   g[kTcRoutedGateUp].a_rows_e = (int)(2 * I);
@@ -333,6 +335,8 @@ void setup_tc(moe_ctx* c) {
   // routed down: W2 [E*H][I] x hq [slots][I]
   ok &= make_tc_map(&g[kTcRoutedDown].a, false, c->L.w2, E * H, I, 128);
   ok &= make_tc_map(&g[kTcRoutedDown].b, false, c->w.hq, R, I, 16);
+  ok &= make_tc_map(&g[kTcRoutedDown].bt, false, c->w.hq, R, I,
+                    (uint32_t)tc_gemm_tile_rows(kTcRoutedDown));
   g[kTcRoutedDown].n_k = (int)(I / kGroup);
   g[kTcRoutedDown].n_f = (int)(H / (2 * kGroup));  // two adjacent output tiles per item
   g[kTcRoutedDown].f_rows = 2 * kGroup;
@@ -352,6 +356,8 @@ void setup_tc(moe_ctx* c) {
   // shared down: Ws2 [H][Is] x hs [rows][Is]
   ok &= make_tc_map(&g[kTcSharedDown].a, true, c->L.ws2, H, Is, 128);
   ok &= make_tc_map(&g[kTcSharedDown].b, true, c->w.hs, (uint64_t)f.max_rows, Is, 16);
+  ok &= make_tc_map(&g[kTcSharedDown].bt, true, c->w.hs, (uint64_t)f.max_rows, Is,
+                    (uint32_t)tc_gemm_tile_rows(kTcSharedDown));
   g[kTcSharedDown].n_k = (int)(Is / 64);
   g[kTcSharedDown].n_f = (int)(H / kGroup);
   g[kTcSharedDown].ldo = (int)H;
@@ -386,7 +392,10 @@ bool use_tc(const moe_ctx* c, int T) {
 // splits.  Returns false if the map cannot be encoded.
 bool router_args(const moe_ctx* c, const void* x, int T, TcGemm* rt, int* grid) {
   *rt = c->tc[kTcRouter];
-  if (!make_tc_map(&rt->b, true, x, (uint64_t)T, (uint64_t)c->cfg.hidden, 16)) return false;
+  if (!make_tc_map(&rt->b, true, x, (uint64_t)T, (uint64_t)c->cfg.hidden, 16) ||
+      !make_tc_map(&rt->bt, true, x, (uint64_t)T, (uint64_t)c->cfg.hidden,
+                   (uint32_t)tc_gemm_tile_rows(kTcRouter)))
+    return false;
   rt->T = T;
   rt->ksplit = c->opt_invariant ? std::min(kInvariantSplits, rt->n_k)
                                 : router_splits(c->sm_count, T, rt->n_f, rt->n_k, c->part_rows);
@@ -431,6 +440,7 @@ int run_forward(moe_ctx* c, const void* x, void* y, int T, cudaStream_t s,
     if (!router_args(c, x, T, &rt, &g_rt)) return MOE_ERR_CUDA;
     TcGemm sgu = c->tc[kTcSharedGateUp];
     sgu.b = rt.b;
+    sgu.bt = rt.bt;  // the router's and the shared gate/up's tiles have the same rows
     TcGemm sdn = c->tc[kTcSharedDown];
     sgu.T = sdn.T = T;
     const int tiles = (T + 127) / 128;

@@ -152,6 +152,8 @@ enum { kTcRoutedGateUp = 0, kTcRoutedDown = 1, kTcSharedGateUp = 2, kTcSharedDow
 struct TcGemm {
   CUtensorMap a;       // weights [rows][K], 128-byte boxes of 128 rows
   CUtensorMap b;       // tokens or slots [rows][K], 128-byte boxes of 16 rows
+  CUtensorMap bt;      // the same operand in boxes of a whole token tile (64 or
+                       // 128 rows): one copy per K block for a full tile
   int n_k;             // K blocks of 128 bytes
   int b_kwrap;         // K blocks after which the B operand's K coordinate wraps
   int ksplit;          // K splits per output tile (router; partial sums), else 1
@@ -176,6 +178,8 @@ struct TcGemm {
 };
 
 size_t tc_gemm_smem(int kind, int n_k);
+// Token rows per tile (N) of each GEMM kind: the box rows of TcGemm::bt.
+int tc_gemm_tile_rows(int kind);
 cudaError_t setup_tc_gemm(int kind, size_t smem);
 cudaError_t launch_tc_gemm(int kind, const TcGemm& g, int grid, size_t smem, cudaStream_t s,
                            bool pdl = false);
