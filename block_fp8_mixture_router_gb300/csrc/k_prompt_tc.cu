@@ -24,9 +24,14 @@
 // for it.  The tile's outputs are transposed through shared memory and
 // stored token-major with coalesced 128/256-byte rows.
 //
-// CTA roles (kTcThreads = 576 threads): warp 0 lane 0 issues TMA, warp 1 owns
-// TMEM and lane 0 issues the MMAs, warps 2-17 are the epilogue (warp w reads
-// TMEM lanes 32*(w%4).. and column quarter (w-2)/4 of the tile's tokens).
+// CTA roles (kTcThreads = 640 threads, 20 warps): warps 0 and 19 issue the
+// TMA copies (0: the weight tiles and the item's scales, 19: the token
+// tiles), warp 1 owns TMEM and issues the MMAs of the first A tile, warp 18
+// those of the second A tile of a pair, warps 2-17 are the epilogue (warp w
+// reads TMEM lanes 32*(w%4).. and column quarter (w-2)/4 of the tile's
+// tokens).  Issuing an async copy, an MMA, a commit or a barrier wait costs
+// one thread tens to a couple of hundred cycles, so each K block's issue
+// work is spread over two warps per side.
 // Every wait is bounded; a wait that gives up sets the status flag and all
 // roles leave their loops.
 #include <cuda.h>
@@ -42,11 +47,13 @@ namespace {
 // Epilogue warps, 4 per TMEM lane quarter: the per-K-block promotion is a
 // chain of dependent loads and FMAs, so four warps per SM sub-partition hide
 // its latency (two left the epilogue issue-bound at 40 % of the issue slots).
-// With the TMA and MMA warps that is 18 warps, so a thread may hold up to 96
-// registers; the block-FP8 epilogue keeps 2 x 16 promoted accumulators and
-// reads one tile's partials from TMEM at a time.
+// With two TMA and two MMA warps that is 20 warps, 5 per sub-partition, so a
+// thread may hold up to 96 registers; the block-FP8 epilogue keeps 2 x 16
+// promoted accumulators and reads one tile's partials from TMEM at a time.
 constexpr int kEpiWarps = 16;
-constexpr int kTcThreads = 64 + 32 * kEpiWarps;  // + the TMA and MMA warps
+constexpr int kTcThreads = 128 + 32 * kEpiWarps;  // + two TMA and two MMA warps
+constexpr int kWarpMma1 = 2 + kEpiWarps;          // MMAs of the pair's second tile
+constexpr int kWarpTmaB = 3 + kEpiWarps;          // token-tile copies
 constexpr int kTile = 128;        // output features per tile (M)
 constexpr int kKBytes = 128;      // bytes of K per stage (one 128B swizzle row)
 constexpr int kATileBytes = kTile * kKBytes;
@@ -155,8 +162,8 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
-// 18 warps: an SM sub-partition holds up to 5 of them, so a thread may use
-// at most 96 registers (5 x 32 x 96 <= 16384 per sub-partition)
+// 20 warps: an SM sub-partition holds 5 of them, so a thread may use at most
+// 96 registers (5 x 32 x 96 <= 16384 per sub-partition)
 template <int kKind>
 __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant__ TcGemm g) {
   using C = Cfg<kKind>;
@@ -190,12 +197,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    // full: both TMA warps arrive with their bytes; empty and tfull: one
+    // commit from each MMA warp
     for (int i = 0; i < S; ++i) {
-      tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], 1);
+      tc::mbar_init(&full[i], 2);
+      tc::mbar_init(&empty[i], kPair ? 2 : 1);
     }
     for (int i = 0; i < NB; ++i) {
-      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tfull[i], kPair ? 2 : 1);
       tc::mbar_init(&tempty[i], kEpiWarps);
     }
     for (int i = 0; i < 2; ++i) {
@@ -257,23 +266,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
   const int n_k = g.n_k;
   const int kx = kF8 ? kKBytes : kKBytes / 2;  // K elements per stage
 
-  if (warp == 0) {
-    // ---- TMA producer ----
-    if (lane == 0) {
-      uint32_t st = 0, ph = 0;
-      bool ok = true;
-      int n_issued = 0;  // stages issued so far (the last S are drained on abort)
-      for (int w = blockIdx.x, j = 0; w < n_items && ok; w += gridDim.x, ++j) {
-        const Item it = decode_item<kRouted, kN>(g, s_pre, s_off, s_cnt, w);
-        if constexpr (kF8) {
-          // this item's activation scales into scale slot j % 2
-          const int sl = j & 1;
-          if (!tc::wait_bounded(&sempty[sl], ((j >> 1) & 1) ^ 1u, s_abort, g.status)) {
-            ok = false;
-            break;
-          }
-          const ItemScales sc = item_scales(g, it);
-          uint8_t* slot = sbs + sl * sbs_slot;
+  // The TMA and MMA warps walk their loops as whole warps: every lane polls
+  // the barriers and computes the coordinates and descriptors, and lane 0
+  // issues the copies, MMAs and commits.  A wait counts as
+  // failed for the warp if it failed in any lane.
+  if (warp == 0 || warp == kWarpTmaB) {
+    // ---- TMA producers: warp 0 the weight tiles (and the item's scales),
+    // warp kWarpTmaB the token tiles; each arrives on full with its bytes ----
+    const bool wa = warp == 0;
+    uint32_t st = 0, ph = 0;
+    bool ok = true;
+    int n_issued = 0;  // stages issued so far (the last S are drained on abort)
+    for (int w = blockIdx.x, j = 0; w < n_items && ok; w += gridDim.x, ++j) {
+      const Item it = decode_item<kRouted, kN>(g, s_pre, s_off, s_cnt, w);
+      if (kF8 && wa) {
+        // this item's activation scales into scale slot j % 2
+        const int sl = j & 1;
+        const bool r = tc::wait_bounded(&sempty[sl], ((j >> 1) & 1) ^ 1u, s_abort, g.status);
+        if (__any_sync(0xffffffffu, !r)) {
+          ok = false;
+          break;
+        }
+        const ItemScales sc = item_scales(g, it);
+        uint8_t* slot = sbs + sl * sbs_slot;
+        if (lane == 0) {
           tc::mbar_arrive_expect_tx(&sfull[sl], sc.s[0].bytes + sc.s[1].bytes + sc.s[2].bytes);
           bulk_copy_g2s(slot, reinterpret_cast<const uint8_t*>(g.sb) + sc.s[0].off, sc.s[0].bytes,
                         &sfull[sl]);
@@ -282,81 +298,91 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
           bulk_copy_g2s(slot + span_a + span_w, reinterpret_cast<const uint8_t*>(g.sa) + sc.s[2].off,
                         sc.s[2].bytes, &sfull[sl]);
         }
-        const int arow = it.e * g.a_rows_e + it.f * g.f_rows;
-        // a tile of more than half the token rows takes one box of kN rows
-        // (rows past the tile belong to the next expert or lie beyond the
-        // operand, which reads zeros; the MMA does not use them), a smaller
-        // one its 16-row boxes: fewer copies for the one issuing thread
-        const bool whole = 2 * it.n > kN;
-        const int nb = whole ? 1 : (it.n + kBBox - 1) / kBBox;
-        const uint32_t bytes =
-            (kPair ? 2 : 1) * kATileBytes + (whole ? kN * kKBytes : nb * kBBoxBytes);
-        for (int kb = it.kb0; kb < it.kb1; ++kb) {
-          if (!tc::wait_bounded(&empty[st], ph ^ 1u, s_abort, g.status)) { ok = false; break; }
-          uint8_t* sp = stages + st * C::kStageBytes;
-          const int bx = (kb % g.b_kwrap) * kx;
+        __syncwarp();
+      }
+      const int arow = it.e * g.a_rows_e + it.f * g.f_rows;
+      // a tile of more than half the token rows takes one box of kN rows
+      // (rows past the tile belong to the next expert or lie beyond the
+      // operand, which reads zeros; the MMA does not use them), a smaller
+      // one its 16-row boxes: fewer copies for the issuing lane
+      const bool whole = 2 * it.n > kN;
+      const int nb = whole ? 1 : (it.n + kBBox - 1) / kBBox;
+      const uint32_t bytes =
+          wa ? (kPair ? 2 : 1) * kATileBytes : (whole ? kN * kKBytes : nb * kBBoxBytes);
+      for (int kb = it.kb0; kb < it.kb1; ++kb) {
+        const bool r = tc::wait_bounded(&empty[st], ph ^ 1u, s_abort, g.status);
+        if (__any_sync(0xffffffffu, !r)) { ok = false; break; }
+        uint8_t* sp = stages + st * C::kStageBytes;
+        const int bx = (kb % g.b_kwrap) * kx;
+        uint8_t* bp = sp + (kPair ? 2 : 1) * kATileBytes;
+        if (lane == 0) {
           tc::mbar_arrive_expect_tx(&full[st], bytes);
-          tc::tma_load_2d(sp, &g.a, kb * kx, arow, &full[st]);
-          if constexpr (kPair) tc::tma_load_2d(sp + kATileBytes, &g.a, kb * kx, arow + g.up_rows, &full[st]);
-          uint8_t* bp = sp + (kPair ? 2 : 1) * kATileBytes;
-          if (whole) {
+          if (wa) {
+            tc::tma_load_2d(sp, &g.a, kb * kx, arow, &full[st]);
+            if constexpr (kPair)
+              tc::tma_load_2d(sp + kATileBytes, &g.a, kb * kx, arow + g.up_rows, &full[st]);
+          } else if (whole) {
             tc::tma_load_2d(bp, &g.bt, bx, it.row0, &full[st]);
           } else {
             for (int i = 0; i < nb; ++i)
               tc::tma_load_2d(bp + i * kBBoxBytes, &g.b, bx, it.row0 + kBBox * i, &full[st]);
           }
-          ++n_issued;
-          if (++st == (uint32_t)S) { st = 0; ph ^= 1u; }
         }
+        __syncwarp();
+        ++n_issued;
+        if (++st == (uint32_t)S) { st = 0; ph ^= 1u; }
       }
-      if (!ok) {
-        // let copies already in flight land before the CTA leaves (bounded)
-        const unsigned long long t0 = tc::global_ns();
-        for (int i = 1; i <= S && i <= n_issued; ++i) {
-          const int k = n_issued - i;  // stage k % S was filled in phase (k / S) & 1
-          while (!tc::mbar_try_wait(&full[k % S], (uint32_t)((k / S) & 1)) &&
-                 tc::global_ns() - t0 < tc::kWaitLimitNs) {
-          }
+    }
+    if (!ok && lane == 0) {
+      // let copies already in flight land before the CTA leaves (bounded:
+      // a stage the other producer never armed gives up at the limit)
+      const unsigned long long t0 = tc::global_ns();
+      for (int i = 1; i <= S && i <= n_issued; ++i) {
+        const int k = n_issued - i;  // stage k % S was filled in phase (k / S) & 1
+        while (!tc::mbar_try_wait(&full[k % S], (uint32_t)((k / S) & 1)) &&
+               tc::global_ns() - t0 < tc::kWaitLimitNs) {
         }
       }
     }
-  } else if (warp == 1) {
-    // ---- MMA issuer ----
-    if (lane == 0) {
-      uint32_t st = 0, ph = 0, tb = 0, tph = 0;
-      bool ok = true;
-      for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-        const Item it = decode_item<kRouted, kN>(g, s_pre, s_off, s_cnt, w);
-        const int n16 = (it.n + 15) & ~15;
-        const uint32_t idesc = kF8 ? tc::idesc_f8(kTile, n16) : tc::idesc_bf16(kTile, n16);
-        for (int kb = it.kb0; kb < it.kb1; ++kb) {
-          if (kF8 || kb == it.kb0) {
-            if (!tc::wait_bounded(&tempty[tb], tph ^ 1u, s_abort, g.status)) { ok = false; break; }
-            tc::fence_after_sync();
-          }
-          if (!tc::wait_bounded(&full[st], ph, s_abort, g.status)) { ok = false; break; }
+  } else if (warp == 1 || (kPair && warp == kWarpMma1)) {
+    // ---- MMA issuers: warp 1 the first A tile, warp kWarpMma1 the second
+    // (pairs); each commits once to empty and to tfull ----
+    const int tile = warp == 1 ? 0 : 1;
+    uint32_t st = 0, ph = 0, tb = 0, tph = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const Item it = decode_item<kRouted, kN>(g, s_pre, s_off, s_cnt, w);
+      const int n16 = (it.n + 15) & ~15;
+      const uint32_t idesc = kF8 ? tc::idesc_f8(kTile, n16) : tc::idesc_bf16(kTile, n16);
+      for (int kb = it.kb0; kb < it.kb1; ++kb) {
+        if (kF8 || kb == it.kb0) {
+          const bool r = tc::wait_bounded(&tempty[tb], tph ^ 1u, s_abort, g.status);
+          if (__any_sync(0xffffffffu, !r)) { ok = false; break; }
           tc::fence_after_sync();
-          const uint32_t sa0 = tc::smem_u32(stages + st * C::kStageBytes);
-          const uint32_t sa1 = sa0 + kATileBytes;
-          const uint32_t sb = sa0 + (kPair ? 2 : 1) * kATileBytes;
-          const uint32_t d0 = tmem + tb * kAcc;
+        }
+        const bool r = tc::wait_bounded(&full[st], ph, s_abort, g.status);
+        if (__any_sync(0xffffffffu, !r)) { ok = false; break; }
+        tc::fence_after_sync();
+        // descriptors of the stage's operands; each 32-byte K step adds 2 to
+        // the start-address field (address >> 4)
+        const uint32_t sa0 = tc::smem_u32(stages + st * C::kStageBytes);
+        const uint64_t da = tc::sw128_desc(sa0 + tile * kATileBytes);
+        const uint64_t db = tc::sw128_desc(sa0 + (kPair ? 2 : 1) * kATileBytes);
+        const uint32_t d0 = tmem + tb * kAcc + tile * kN;
 #pragma unroll
-          for (int kk = 0; kk < kKBytes / 32; ++kk) {
-            const uint32_t acc = (kk > 0 || (!kF8 && kb > it.kb0)) ? 1u : 0u;
-            const uint64_t bdesc = tc::sw128_desc(sb + 32 * kk);
-            tc::mma<kF8>(d0, tc::sw128_desc(sa0 + 32 * kk), bdesc, idesc, acc);
-            if constexpr (kPair) tc::mma<kF8>(d0 + kN, tc::sw128_desc(sa1 + 32 * kk), bdesc, idesc, acc);
-          }
-          tc::commit(&empty[st]);
-          if (++st == (uint32_t)S) { st = 0; ph ^= 1u; }
-          if (kF8 || kb == it.kb1 - 1) {
-            tc::commit(&tfull[tb]);
-            if (++tb == (uint32_t)NB) { tb = 0; tph ^= 1u; }
-          }
+        for (int kk = 0; kk < kKBytes / 32; ++kk) {
+          const uint32_t acc = (kk > 0 || (!kF8 && kb > it.kb0)) ? 1u : 0u;
+          tc::mma_warp<kF8>(d0, da + 2 * kk, db + 2 * kk, idesc, acc);
+        }
+        tc::commit_warp(&empty[st]);
+        if (++st == (uint32_t)S) { st = 0; ph ^= 1u; }
+        if (kF8 || kb == it.kb1 - 1) {
+          tc::commit_warp(&tfull[tb]);
+          if (++tb == (uint32_t)NB) { tb = 0; tph ^= 1u; }
         }
       }
     }
-  } else {
+  } else if (warp >= 2 && warp < 2 + kEpiWarps) {
     // ---- epilogue ----
     const int ew = warp - 2;
     const int q = warp & 3;
@@ -402,7 +428,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
         const uint32_t ta0 = tmem + tl + tb * kAcc + c0;
         if constexpr (kF8) {
           // block-FP8: partial x (weight block scale x token scale), 16
-          // columns of both tiles under one TMEM wait at a time; the products
+          // columns of one tile under one TMEM wait at a time; the products
           // come from pbuf as broadcast vectors
           static_assert(kCols % 16 == 0, "x16 loads per tile");
 #pragma unroll
@@ -504,15 +530,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
             for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
               for (int u = 0; u < 4; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], o));
+            // the four columns' scales and codes on their fast paths first,
+            // the rare exact fallbacks after, so the four chains interleave
+            float sq[4];
+            uint32_t code[4];
+            bool rare[4], und[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sq[u] = group_scale_fast(m[u], rare[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (rare[u]) sq[u] = group_scale(m[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              code[u] = quant4_fast(v[u].x, v[u].y, v[u].z, v[u].w, sq[u], und[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (und[u]) code[u] = quant4_exact(v[u].x, v[u].y, v[u].z, v[u].w, sq[u]);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int col = c0s + kEpiWarps * u;
               if (col < it.n) {
                 const size_t r = (size_t)(it.row0 + col);
-                const float sq = group_scale(m[u]);
-                *reinterpret_cast<uint32_t*>(g.hq + r * g.ldo + fcol + 4 * lane) =
-                    quant4(v[u].x, v[u].y, v[u].z, v[u].w, sq);
-                if (lane == 0) g.sh[r * (g.ldo / kTile) + fcol / kTile] = sq;
+                *reinterpret_cast<uint32_t*>(g.hq + r * g.ldo + fcol + 4 * lane) = code[u];
+                if (lane == 0) g.sh[r * (g.ldo / kTile) + fcol / kTile] = sq[u];
               }
             }
           } else {

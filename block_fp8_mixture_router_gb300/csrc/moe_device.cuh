@@ -94,8 +94,13 @@ __device__ __forceinline__ void mma_bf16_k32(float (&d)[4], const uint4& a_lo, c
 }
 
 // ---- conversions ------------------------------------------------------------
+// v rounded to bf16 (nearest even) and back, with integer operations: the
+// same value as the conversion for every finite v and infinity, on the
+// full-rate integer pipe rather than the conversion unit.  NaN stays NaN.
 __device__ __forceinline__ float bf16_round(float v) {
-  return __bfloat162float(__float2bfloat16_rn(v));
+  const uint32_t u = __float_as_uint(v);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return v;
+  return __uint_as_float((u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u);
 }
 
 // e4m3 codes of four values, first value in the lowest byte: the hardware
@@ -126,22 +131,32 @@ static __device__ __noinline__ float div_ieee(float v, float s) { return __fdiv_
 // and v/s lies below it -- decides between q and its neighbour.  Dividends
 // below 2^-95 or near overflow, and quotients below 2^-63, whose remainder or
 // half-ulp product could leave the normal range, take the IEEE division.
-__device__ __forceinline__ float div_shared(float v, float s, float y) {
+__device__ __forceinline__ float div_shared_fast(float v, float s, float y, bool& rare) {
   const uint32_t ev = (__float_as_uint(v) >> 23) & 0xFFu;
-  if (y == 0.0f || ev > 252u || (ev < 32u && v != 0.0f)) return div_ieee(v, s);
-  if (ev < 32u) return v * y;  // a signed zero
+  rare = (y == 0.0f) | (ev > 252u) | ((ev < 32u) & (v != 0.0f));
   float q = v * y;
+  if (ev < 32u) return q;  // a signed zero
   q = fmaf(fmaf(-q, s, v), y, q);
   const float r = fmaf(-q, s, v);
   const uint32_t qb = __float_as_uint(q);
   const uint32_t e = (qb >> 23) & 0xFFu;
-  if (e < 64u || e > 253u) return div_ieee(v, s);
+  rare |= (e < 64u) | (e > 253u);
   const float half = s * __uint_as_float((e - 24u) << 23);
   const bool down = (r < 0.0f) != (q < 0.0f);
   const float h = (down && (qb & 0x7FFFFFu) == 0u) ? 0.5f * half : half;
   const float ar = fabsf(r);
   if (ar < h || (ar == h && !(qb & 1u))) return q;
   return __uint_as_float(down ? qb - 1u : qb + 1u);
+}
+
+// (div_shared_fast sets `rare` where the steps above cannot decide and the
+// IEEE division must; its result is then not to be used.  Callers that
+// divide several values at once take the fast path for all of them first and
+// the rare fallback after, so no out-of-line call splits their code.)
+__device__ __forceinline__ float div_shared(float v, float s, float y) {
+  bool rare;
+  const float q = div_shared_fast(v, s, y, rare);
+  return rare ? div_ieee(v, s) : q;
 }
 
 // Codes of v/s through the IEEE quotients, out of line (the rare groups
@@ -169,15 +184,24 @@ __device__ __forceinline__ bool e4m3_undecided(float q) {
 // Quantise four values of a group with scale s: the e4m3 codes of the IEEE
 // quotients v/s, taken from the products v * rcp(s) wherever those decide
 // them (all but a few groups in a million), else from the exact quotients.
-__device__ __forceinline__ uint32_t quant4(float v0, float v1, float v2, float v3, float s) {
+// The codes from the products alone; `undecided` is set where quant4 would
+// take the exact quotients instead (the codes returned are then not to be
+// used).
+__device__ __forceinline__ uint32_t quant4_fast(float v0, float v1, float v2, float v3, float s,
+                                                bool& undecided) {
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(s));
   const float q0 = v0 * y, q1 = v1 * y, q2 = v2 * y, q3 = v3 * y;
   const uint32_t es = (__float_as_uint(s) >> 23) & 0xFFu;
-  if ((es - 2u > 250u) | e4m3_undecided(q0) | e4m3_undecided(q1) | e4m3_undecided(q2) |
-      e4m3_undecided(q3))
-    return quant4_exact(v0, v1, v2, v3, s);
+  undecided = (es - 2u > 250u) | e4m3_undecided(q0) | e4m3_undecided(q1) | e4m3_undecided(q2) |
+              e4m3_undecided(q3);
   return e4m3x4(q0, q1, q2, q3);
+}
+
+__device__ __forceinline__ uint32_t quant4(float v0, float v1, float v2, float v3, float s) {
+  bool undecided;
+  const uint32_t c = quant4_fast(v0, v1, v2, v3, s, undecided);
+  return undecided ? quant4_exact(v0, v1, v2, v3, s) : c;
 }
 
 // silu(z) = z / (1 + e^-z) with the fast exponential and divide; the
@@ -207,6 +231,14 @@ __device__ __forceinline__ float warp_sum(float v) {
 // 1 for an all-zero group.
 __device__ __forceinline__ float group_scale(float amax) {
   return amax > 0.0f ? div_shared(amax, 448.0f, 0x1.24924ap-9f) : 1.0f;  // RN(1/448)
+}
+
+// group_scale without the out-of-line division: `rare` is set where
+// group_scale must be called instead.
+__device__ __forceinline__ float group_scale_fast(float amax, bool& rare) {
+  const float q = div_shared_fast(amax, 448.0f, 0x1.24924ap-9f, rare);
+  rare &= amax > 0.0f;
+  return amax > 0.0f ? q : 1.0f;
 }
 
 }  // namespace moe
