@@ -22,16 +22,20 @@
 // A gate tile and its up tile share the token operand and land in the same
 // TMEM lanes, so the thread that owns feature j holds both halves of SwiGLU
 // for it.  The tile's outputs are transposed through shared memory and
-// stored token-major with coalesced 128/256-byte rows.
+// stored token-major with coalesced rows.
 //
-// CTA roles (kTcThreads = 640 threads, 20 warps): warps 0 and 19 issue the
+// CTA roles (kTcThreads = 768 threads, 24 warps): warps 0 and 19 issue the
 // TMA copies (0: the weight tiles and the item's scales, 19: the token
 // tiles), warp 1 owns TMEM and issues the MMAs of the first A tile, warp 18
 // those of the second A tile of a pair, warps 2-17 are the epilogue (warp w
 // reads TMEM lanes 32*(w%4).. and column quarter (w-2)/4 of the tile's
 // tokens).  Issuing an async copy, an MMA, a commit or a barrier wait costs
 // one thread tens to a couple of hundred cycles, so each K block's issue
-// work is spread over two warps per side.
+// work is spread over two warps per side.  For the block-FP8 kinds the
+// epilogue hands each finished item to warps 20-23 through shared memory
+// (both tiles as bf16) and goes on to the next item's K blocks; those warps
+// apply SwiGLU, quantise and store, so the stores no longer hold up the
+// promotion, and through it the tensor cores.
 // Every wait is bounded; a wait that gives up sets the status flag and all
 // roles leave their loops.
 #include <cuda.h>
@@ -47,13 +51,16 @@ namespace {
 // Epilogue warps, 4 per TMEM lane quarter: the per-K-block promotion is a
 // chain of dependent loads and FMAs, so four warps per SM sub-partition hide
 // its latency (two left the epilogue issue-bound at 40 % of the issue slots).
-// With two TMA and two MMA warps that is 20 warps, 5 per sub-partition, so a
-// thread may hold up to 96 registers; the block-FP8 epilogue keeps 2 x 16
-// promoted accumulators and reads one tile's partials from TMEM at a time.
+// With two TMA, two MMA and four store warps that is 24 warps, 6 per
+// sub-partition, so a thread may hold up to 80 registers; the block-FP8
+// epilogue keeps 2 x 16 promoted accumulators and reads 8 columns of one
+// tile from TMEM at a time.
 constexpr int kEpiWarps = 16;
-constexpr int kTcThreads = 128 + 32 * kEpiWarps;  // + two TMA and two MMA warps
+constexpr int kStoreWarps = 4;  // block-FP8 kinds: quantise and store finished items
+constexpr int kTcThreads = 128 + 32 * (kEpiWarps + kStoreWarps);  // + two TMA, two MMA warps
 constexpr int kWarpMma1 = 2 + kEpiWarps;          // MMAs of the pair's second tile
 constexpr int kWarpTmaB = 3 + kEpiWarps;          // token-tile copies
+constexpr int kWarpStore0 = 4 + kEpiWarps;        // first store warp
 constexpr int kTile = 128;        // output features per tile (M)
 constexpr int kKBytes = 128;      // bytes of K per stage (one 128B swizzle row)
 constexpr int kATileBytes = kTile * kKBytes;
@@ -162,8 +169,169 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
-// 20 warps: an SM sub-partition holds 5 of them, so a thread may use at most
-// 96 registers (5 x 32 x 96 <= 16384 per sub-partition)
+// Stores output tile columns c = w0, w0 + kW, ... of an item from tbuf ([token
+// column][128 features], fp32), kW warps taking part, four columns per warp
+// at a time so their reductions and divisions overlap: the routed gate/up
+// quantises each column's 128 SwiGLU values as one group into hq and sh
+// (per-row contexts store them as fp32 rows instead), the router stores fp32
+// logits, the other kinds bf16 rows.
+template <int kKind, int kW>
+__device__ __forceinline__ void store_cols(const TcGemm& g, const Item& it, const float* tbuf,
+                                           int fcol, int w0, int lane) {
+  for (int c0s = w0; c0s < it.n; c0s += 4 * kW) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int col = c0s + kW * u;
+      v[u] = col < it.n ? *reinterpret_cast<const float4*>(tbuf + col * kTile + 4 * lane)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if constexpr (kKind == kTcRoutedGateUp) {
+      if (g.hf) {
+        // one scale per row: the fp32 SwiGLU rows, quantised per row
+        // once every feature tile of the row is done (k_quant_h_rows)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int col = c0s + kW * u;
+          if (col < it.n)
+            *reinterpret_cast<float4*>(g.hf + (size_t)(it.row0 + col) * g.ldo + fcol +
+                                       4 * lane) = v[u];
+        }
+        continue;
+      }
+      float m[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        m[u] = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], o));
+      // the four columns' scales and codes on their fast paths first,
+      // the rare exact fallbacks after, so the four chains interleave
+      float sq[4];
+      uint32_t code[4];
+      bool rare[4], und[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) sq[u] = group_scale_fast(m[u], rare[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (rare[u]) sq[u] = group_scale(m[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        code[u] = quant4_fast(v[u].x, v[u].y, v[u].z, v[u].w, sq[u], und[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (und[u]) code[u] = quant4_exact(v[u].x, v[u].y, v[u].z, v[u].w, sq[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int col = c0s + kW * u;
+        if (col < it.n) {
+          const size_t r = (size_t)(it.row0 + col);
+          *reinterpret_cast<uint32_t*>(g.hq + r * g.ldo + fcol + 4 * lane) = code[u];
+          if (lane == 0) g.sh[r * (g.ldo / kTile) + fcol / kTile] = sq[u];
+        }
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int col = c0s + kW * u;
+        if (col >= it.n) continue;
+        const size_t r = (size_t)(it.row0 + col);
+        if constexpr (kKind == kTcRouter) {
+          const int e = fcol + 4 * lane;  // logits [row][E], fp32
+          float* o = g.outf + ((size_t)it.ks * g.T + r) * g.ldo + e;
+          if (e + 3 < g.ldo) {
+            *reinterpret_cast<float4*>(o) = v[u];
+          } else {
+            if (e < g.ldo) o[0] = v[u].x;
+            if (e + 1 < g.ldo) o[1] = v[u].y;
+            if (e + 2 < g.ldo) o[2] = v[u].z;
+          }
+        } else {
+          __nv_bfloat162 p0 = __floats2bfloat162_rn(v[u].x, v[u].y);
+          __nv_bfloat162 p1 = __floats2bfloat162_rn(v[u].z, v[u].w);
+          uint2 o;
+          o.x = *reinterpret_cast<uint32_t*>(&p0);
+          o.y = *reinterpret_cast<uint32_t*>(&p1);
+          *reinterpret_cast<uint2*>(g.out + r * g.ldo + fcol + 4 * lane) = o;
+        }
+      }
+    }
+  }
+}
+
+// Two bf16 values packed in a word (first in the low half) as floats.
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// The routed gate/up's SwiGLU and store by the store warps, from the gate
+// and up tiles in t16 ([tile][token column][128 features], bf16, tile 1 at
+// column kN).  kW warps take four token columns each per pass, eight lanes
+// per column and 16 of its 128 SwiGLU values per lane (4-value chunks k,
+// k+8, k+16, k+24 of lane k of the eight, so that each load and store
+// instruction covers whole rows).  A column's group amax is then three
+// shuffles away, and each lane divides by its column's scale once for its
+// 16 values.
+template <int kW, int kN>
+__device__ __forceinline__ void store_gateup_cols(const TcGemm& g, const Item& it,
+                                                  const __nv_bfloat16* t16, int fcol, int w0,
+                                                  int lane) {
+  const int k = lane & 7;
+  for (int cb = 4 * w0; cb < it.n; cb += 4 * kW) {
+    const int col = cb + (lane >> 3);
+    const bool ok = col < it.n;
+    float4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok) {
+        const uint2 zg = *reinterpret_cast<const uint2*>(t16 + col * kTile + 4 * (k + 8 * i));
+        const uint2 zu = *reinterpret_cast<const uint2*>(t16 + (kN + col) * kTile + 4 * (k + 8 * i));
+        const float2 g01 = bf16x2_to_float2(zg.x), g23 = bf16x2_to_float2(zg.y);
+        const float2 u01 = bf16x2_to_float2(zu.x), u23 = bf16x2_to_float2(zu.y);
+        v[i] = make_float4(silu_f32(g01.x) * u01.x, silu_f32(g01.y) * u01.y,
+                           silu_f32(g23.x) * u23.x, silu_f32(g23.y) * u23.y);
+      }
+    }
+    const size_t r = (size_t)(it.row0 + (ok ? col : 0));
+    if (g.hf) {
+      // one scale per row: the fp32 SwiGLU rows, quantised per row once
+      // every feature tile of the row is done (k_quant_h_rows)
+      if (ok)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<float4*>(g.hf + r * g.ldo + fcol + 4 * (k + 8 * i)) = v[i];
+      continue;
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    bool rare;
+    float sq = group_scale_fast(m, rare);
+    if (rare) sq = group_scale(m);
+    uint32_t code[4];
+    bool und[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) code[i] = quant4_fast(v[i].x, v[i].y, v[i].z, v[i].w, sq, und[i]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (und[i]) code[i] = quant4_exact(v[i].x, v[i].y, v[i].z, v[i].w, sq);
+    if (ok) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<uint32_t*>(g.hq + r * g.ldo + fcol + 4 * (k + 8 * i)) = code[i];
+      if (k == 0) g.sh[r * (g.ldo / kTile) + fcol / kTile] = sq;
+    }
+  }
+}
+
+// 24 warps: an SM sub-partition holds 6 of them, so a thread may use at most
+// 80 registers (6 x 32 x 80 <= 16384 per sub-partition)
 template <int kKind>
 __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant__ TcGemm g) {
   using C = Cfg<kKind>;
@@ -189,7 +357,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
   uint64_t* tempty = bars + 2 * S + NB;
   uint64_t* sfull = bars + 2 * S + 2 * NB;
   uint64_t* sempty = sfull + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sempty + 2);
+  // block-FP8: tbuf holds a finished item (dfull) / has been stored (dfree)
+  uint64_t* dfull = sempty + 2;
+  uint64_t* dfree = dfull + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(dfree + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_pre = reinterpret_cast<int*>(s_tmem + 2);  // [E+1]
   int* s_off = s_pre + kMaxExperts + 1;              // [E]
@@ -211,6 +382,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
       tc::mbar_init(&sfull[i], 1);
       tc::mbar_init(&sempty[i], kEpiWarps);
     }
+    tc::mbar_init(dfull, kEpiWarps);
+    tc::mbar_init(dfree, kStoreWarps);
     *s_abort = 0;
     tc::fence_barrier_init();
     tc::tma_prefetch_map(&g.a);
@@ -404,12 +577,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
         tc::wait_bounded(&sfull[sl], (j >> 1) & 1, s_abort, g.status);
         const ItemScales sc = item_scales(g, it);
         const uint8_t* slot = sbs + sl * sbs_slot;
+        epi_sync();  // every warp has left the previous item's K loop, pbuf's last reader
         sc_tok = reinterpret_cast<const float*>(slot + sc.s[0].lead);
         s_wg = reinterpret_cast<const float*>(slot + span_a + sc.s[1].lead);
         s_wu = reinterpret_cast<const float*>(slot + span_a + span_w + sc.s[2].lead);
         // (weight block scale x token scale) for every (tile, K block, token);
-        // padding tokens get 0.  The previous item's K loop, the last reader of
-        // pbuf, ended before that item's store phase and its barriers.
+        // padding tokens get 0
         for (int i = 32 * ew + lane; i < n_k * kN; i += 32 * kEpiWarps) {
           const int kb = i / kN, t = i - kb * kN;
           const float st = t < it.n ? sc_tok[t * n_k + kb] : 0.0f;
@@ -427,27 +600,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
         tc::fence_after_sync();
         const uint32_t ta0 = tmem + tl + tb * kAcc + c0;
         if constexpr (kF8) {
-          // block-FP8: partial x (weight block scale x token scale), 16
+          // block-FP8: partial x (weight block scale x token scale), 8
           // columns of one tile under one TMEM wait at a time; the products
           // come from pbuf as broadcast vectors
-          static_assert(kCols % 16 == 0, "x16 loads per tile");
+          static_assert(kCols % 8 == 0, "x8 loads per tile");
 #pragma unroll
-          for (int c4 = 0; c4 < kCols / 16; ++c4) {
-            if (c0 + 16 * c4 < n16) {
+          for (int c8 = 0; c8 < kCols / 8; ++c8) {
+            if (c0 + 8 * c8 < n16) {
 #pragma unroll
               for (int tile = 0; tile < 2; ++tile) {
-                uint32_t va[16];
-                tc::tmem_ld16(ta0 + tile * kN + 16 * c4, va);
+                uint32_t va[8];
+                tc::tmem_ld8(ta0 + tile * kN + 8 * c8, va);
                 const float4* ps = reinterpret_cast<const float4*>(
-                    pbuf + (tile * n_k + kb) * kN + c0 + 16 * c4);
+                    pbuf + (tile * n_k + kb) * kN + c0 + 8 * c8);
                 float* acc = tile == 0 ? acc0 : acc1;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
+                for (int q4 = 0; q4 < 2; ++q4) {
                   const float4 s4 = ps[q4];
                   const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
                   for (int i = 0; i < 4; ++i) {
-                    const int c = 16 * c4 + 4 * q4 + i;
+                    const int c = 8 * c8 + 4 * q4 + i;
                     acc[c] = fmaf(__uint_as_float(va[4 * q4 + i]), ss[i], acc[c]);
                   }
                 }
@@ -481,108 +654,46 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
       if constexpr (kF8) {
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sempty[j & 1]);  // scale slot free
-      }
-      // output tiles of this item: one for SwiGLU and the bf16 kinds, two for
-      // the routed down pair; each goes through tbuf
-      constexpr int kOut = (kF8 && !C::kSwiGLU) ? 2 : 1;
-#pragma unroll
-      for (int ot = 0; ot < kOut; ++ot) {
-        if constexpr (kF8) {
-          epi_sync();  // every warp is done reading tbuf
+        // hand the item to the store warps through tbuf, once they have
+        // stored the previous one: both tiles as bf16, the precision SwiGLU
+        // reads gate and up in and the down outputs are stored in
+        if (j > 0) tc::wait_bounded(dfree, (uint32_t)((j - 1) & 1), s_abort, g.status);
+        {
+          __nv_bfloat16* t16 = reinterpret_cast<__nv_bfloat16*>(tbuf);
 #pragma unroll
           for (int i = 0; i < kCols; ++i) {
-            float v;
-            if constexpr (C::kSwiGLU) v = silu_f32(bf16_round(acc0[i])) * bf16_round(acc1[i]);
-            else v = ot == 0 ? acc0[i] : acc1[i];
-            tbuf[(c0 + i) * kTile + row] = v;
+            t16[(c0 + i) * kTile + row] = __float2bfloat16_rn(acc0[i]);
+            t16[(kN + c0 + i) * kTile + row] = __float2bfloat16_rn(acc1[i]);
           }
         }
-        epi_sync();
-        // ---- store: token columns ew, ew+8, ... (128 features each), four
-        // columns at a time so their reductions and divisions overlap ----
-        const int fcol = it.f * g.f_rows + ot * kTile;  // first output feature
-        for (int c0s = ew; c0s < it.n; c0s += 4 * kEpiWarps) {
-          float4 v[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int col = c0s + kEpiWarps * u;
-            v[u] = col < it.n ? *reinterpret_cast<const float4*>(tbuf + col * kTile + 4 * lane)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-          if constexpr (kKind == kTcRoutedGateUp) {
-            if (g.hf) {
-              // one scale per row: the fp32 SwiGLU rows, quantised per row
-              // once every feature tile of the row is done (k_quant_h_rows)
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int col = c0s + kEpiWarps * u;
-                if (col < it.n)
-                  *reinterpret_cast<float4*>(g.hf + (size_t)(it.row0 + col) * g.ldo + fcol +
-                                             4 * lane) = v[u];
-              }
-              continue;
-            }
-            float m[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              m[u] = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-              for (int u = 0; u < 4; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], o));
-            // the four columns' scales and codes on their fast paths first,
-            // the rare exact fallbacks after, so the four chains interleave
-            float sq[4];
-            uint32_t code[4];
-            bool rare[4], und[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) sq[u] = group_scale_fast(m[u], rare[u]);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (rare[u]) sq[u] = group_scale(m[u]);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              code[u] = quant4_fast(v[u].x, v[u].y, v[u].z, v[u].w, sq[u], und[u]);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (und[u]) code[u] = quant4_exact(v[u].x, v[u].y, v[u].z, v[u].w, sq[u]);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int col = c0s + kEpiWarps * u;
-              if (col < it.n) {
-                const size_t r = (size_t)(it.row0 + col);
-                *reinterpret_cast<uint32_t*>(g.hq + r * g.ldo + fcol + 4 * lane) = code[u];
-                if (lane == 0) g.sh[r * (g.ldo / kTile) + fcol / kTile] = sq[u];
-              }
-            }
-          } else {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int col = c0s + kEpiWarps * u;
-              if (col >= it.n) continue;
-              const size_t r = (size_t)(it.row0 + col);
-              if constexpr (kKind == kTcRouter) {
-                const int e = fcol + 4 * lane;  // logits [row][E], fp32
-                float* o = g.outf + ((size_t)it.ks * g.T + r) * g.ldo + e;
-                if (e + 3 < g.ldo) {
-                  *reinterpret_cast<float4*>(o) = v[u];
-                } else {
-                  if (e < g.ldo) o[0] = v[u].x;
-                  if (e + 1 < g.ldo) o[1] = v[u].y;
-                  if (e + 2 < g.ldo) o[2] = v[u].z;
-                }
-              } else {
-                __nv_bfloat162 p0 = __floats2bfloat162_rn(v[u].x, v[u].y);
-                __nv_bfloat162 p1 = __floats2bfloat162_rn(v[u].z, v[u].w);
-                uint2 o;
-                o.x = *reinterpret_cast<uint32_t*>(&p0);
-                o.y = *reinterpret_cast<uint32_t*>(&p1);
-                *reinterpret_cast<uint2*>(g.out + r * g.ldo + fcol + 4 * lane) = o;
-              }
-            }
-          }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(dfull);
+        continue;
+      }
+      // bf16 kinds: the output tile, through tbuf
+      epi_sync();
+      store_cols<kKind, kEpiWarps>(g, it, tbuf, it.f * g.f_rows, ew, lane);
+    }
+  } else if (kF8 && warp >= kWarpStore0) {
+    // ---- store warps (block-FP8): each item from tbuf to global memory ----
+    const int sw = warp - kWarpStore0;
+    for (int w = blockIdx.x, j = 0; w < n_items; w += gridDim.x, ++j) {
+      const Item it = decode_item<kRouted, kN>(g, s_pre, s_off, s_cnt, w);
+      tc::wait_bounded(dfull, (uint32_t)(j & 1), s_abort, g.status);
+      const __nv_bfloat16* t16 = reinterpret_cast<const __nv_bfloat16*>(tbuf);
+      if constexpr (C::kSwiGLU) {
+        store_gateup_cols<kStoreWarps, kN>(g, it, t16, it.f * g.f_rows, sw, lane);
+      } else {
+        // the routed down pair: two output tiles of bf16 rows
+        for (int ot = 0; ot < 2; ++ot) {
+          const int fcol = it.f * g.f_rows + ot * kTile;
+          for (int col = sw; col < it.n; col += kStoreWarps)
+            *reinterpret_cast<uint2*>(g.out + (size_t)(it.row0 + col) * g.ldo + fcol + 4 * lane) =
+                *reinterpret_cast<const uint2*>(t16 + (ot * kN + col) * kTile + 4 * lane);
         }
       }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(dfree);
     }
   }
   __syncthreads();
@@ -601,7 +712,7 @@ size_t smem_bytes(int n_k) {
                              : 0;
   const size_t prod = C::kF8 ? (size_t)2 * n_k * C::kN * 4 : 0;
   return 1024 + (size_t)C::kStages * C::kStageBytes + (size_t)C::kN * kTile * 4 + 2 * slot +
-         prod + (2 * C::kStages + 2 * C::kNumBuf + 4) * 8 + 16 + (3 * kMaxExperts + 1) * 4;
+         prod + (2 * C::kStages + 2 * C::kNumBuf + 6) * 8 + 16 + (3 * kMaxExperts + 1) * 4;
 }
 
 const void* kernel_of(int kind) {

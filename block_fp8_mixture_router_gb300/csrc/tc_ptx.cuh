@@ -198,6 +198,17 @@ __device__ __forceinline__ void commit_warp(uint64_t* bar) {
       "=r"(v[o + 10]), "=r"(v[o + 11]), "=r"(v[o + 12]), "=r"(v[o + 13]), "=r"(v[o + 14]),    \
       "=r"(v[o + 15])
 
+// 8 consecutive fp32 columns of this warp's 32 TMEM lanes, waited for.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7])
+      : "r"(taddr)
+      : "memory");
+}
+
 // 16 consecutive fp32 columns of this warp's 32 TMEM lanes (lane i of the
 // warp reads TMEM lane 32*(warp%4) + i), waited for before returning.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
