@@ -369,13 +369,36 @@ def test_repeat_bitwise(full_case):
             assert torch.equal(y.view(torch.int16), ys[0].view(torch.int16))
 
 
-def test_forward_host_matches_device(full_case):
-    x = full_case.x(3, tag="host")
-    y_dev = full_case.moe.forward(x)
-    xh = x.cpu().pin_memory()
-    y_host = full_case.moe.forward_host(xh)
-    torch.cuda.synchronize()
-    assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
+@pytest.mark.parametrize("rows", [1, 3, 64])
+def test_forward_host_matches_device(full_case, rows):
+    """moe_forward_host gives moe_forward's bits: with pinned buffers (the
+    same pair with new contents, another pair, after an option change) and
+    with pageable ones."""
+    net = full_case.moe
+
+    def check(xh, yh, x):
+        net.forward_host(xh, yh)
+        y_dev = net.forward(x)
+        torch.cuda.synchronize()
+        assert torch.equal(yh.view(torch.int16), y_dev.cpu().view(torch.int16))
+
+    xh = full_case.x(rows, tag=f"host{rows}").cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    for tag in ("a", "b"):  # the same buffers with new contents
+        x = full_case.x(rows, tag=f"host{tag}{rows}")
+        xh.copy_(x.cpu())
+        check(xh, yh, x)
+    xh2, yh2 = xh.clone().pin_memory(), torch.empty_like(xh).pin_memory()
+    check(xh2, yh2, x)
+    net.set_option(m.MOE_OPT_PDL, 0)
+    try:
+        check(xh, yh, x)
+    finally:
+        net.set_option(m.MOE_OPT_PDL, 1)
+    check(xh, yh, x)
+    xp, yp = x.cpu(), torch.empty((rows, x.shape[1]), dtype=torch.bfloat16)
+    assert not xp.is_pinned() and not yp.is_pinned()
+    check(xp, yp, x)
 
 
 # ---- boundary behaviour ------------------------------------------------------
