@@ -951,7 +951,7 @@ STAGE_LAUNCHES = {}
 
 def launches_hint(T: int) -> int:
     """Kernel launches of one forward of T rows (graph size bound only)."""
-    return 1 if T <= 5 else (3 if T <= 16 else 12)
+    return 1 if T <= 4 else 12
 
 
 # prompt legs reported beside the one-row headline: (workload, steps, instances)

@@ -265,11 +265,21 @@ struct StageRec {
   } while (0)
 
 // The decode kernels serve rows <= kDecodeRows for hidden sizes up to 4096.
+// 2..kRowsAuto rows on the role-split multi-row kernel unless another kernel
+// is asked for.  Above that the grouped tcgen05 kernels are faster on GB300
+// than both it and the three chained decode kernels: per layer, 52.9 against
+// 59.8 us at 5 rows, 53.7 against 54.7 us (chained) at 6, 57.0 against
+// 68.5 us at 11 and 59.4 against 77.3 us at 16; at 4 rows they tie.
+constexpr int kRowsAuto = 4;
+
 bool use_decode(const moe_ctx* c, int T) {
   if (c->opt_path == 2 || c->opt_path == 4 || c->opt_invariant) return false;
   if (T > kDecodeRows || c->cfg.hidden > 4096) return false;
   // one scale per row: only the role-split decode kernels quantise whole rows
   if (per_row_scales(c->cfg)) return use_row(c, T) || use_rows(c, T);
+  // automatic choice: the chained kernels only where the tcgen05 ones are
+  // not available
+  if ((c->opt_path == 0 || c->opt_path == 1) && T > kRowsAuto && c->tc_ok) return false;
   return true;
 }
 
@@ -278,12 +288,6 @@ bool use_decode(const moe_ctx* c, int T) {
 bool use_row(const moe_ctx* c, int T) {
   return T == 1 && c->row_smem > 0 && (c->opt_path == 0 || c->opt_path == 1);
 }
-
-// 2..kRowsAuto rows on the role-split multi-row kernel unless another decode
-// kernel is asked for.  Above that the three chained kernels are faster on
-// GB300: they spread the routed work over every SM instead of the routed
-// role's share (measured at 6, 8, 11 and 16 rows).
-constexpr int kRowsAuto = 5;
 
 bool use_rows(const moe_ctx* c, int T) {
   if (T < 2 || T > kDecodeRows || c->rows_smem <= 0) return false;

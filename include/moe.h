@@ -282,11 +282,11 @@ int moe_expert_activations(moe_ctx* ctx, int rows, uint8_t* hq, float* sh, void*
  * quantization). */
 int moe_forward_codes(moe_ctx* ctx, int rows, uint8_t* codes, float* scales, void* stream);
 
-/* Options.  MOE_OPT_PATH: 0 = automatic (rows <= 16 on the decode kernels:
- * the role-split one-row kernel for 1 row, the role-split multi-row kernel
- * for 2..5 rows, three chained decode kernels for 6..16 rows; more rows on
- * the grouped prompt kernels on the tcgen05 tensor cores), 1 = the same as
- * 0, 2 = always the grouped prompt kernels, 3 = rows <= 16 on the three
+/* Options.  MOE_OPT_PATH: 0 = automatic (the role-split one-row kernel for
+ * 1 row, the role-split multi-row kernel for 2..4 rows, the grouped prompt
+ * kernels on the tcgen05 tensor cores for more; the three chained decode
+ * kernels take 5..16 rows where the tcgen05 kernels are not available), 1 =
+ * the same as 0, 2 = always the grouped prompt kernels, 3 = rows <= 16 on the three
  * chained decode kernels, 4 = always the grouped prompt kernels with
  * warp-level MMAs instead of tcgen05 (the path every forward takes when a
  * context's shape leaves no room for the tcgen05 kernels: hidden or inter
