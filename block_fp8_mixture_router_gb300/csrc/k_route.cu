@@ -136,6 +136,7 @@ cudaError_t launch_topk_splits(const KArgs& a, const float* part, int ks, cudaSt
 //   finish: slot = (rows of all experts before e) + (rows of e in earlier
 //           blocks) + (rank in the block).  Block 0 also writes the per-expert
 //           counts, offsets and the chunk list of the warp-MMA kernels.
+// A single block (up to kSchedRows rows) takes both steps in one kernel.
 // Nothing depends on timing: every sum has a fixed order.
 
 __global__ void __launch_bounds__(256) k_sched_count(KArgs a, int* __restrict__ rank,
@@ -167,27 +168,25 @@ __global__ void __launch_bounds__(256) k_sched_count(KArgs a, int* __restrict__ 
   }
 }
 
-__global__ void __launch_bounds__(256) k_sched_finish(KArgs a, const int* __restrict__ rank,
-                                                      const int* __restrict__ blk_cnt, int nb) {
+// The finishing steps for block b: slots of the block's pairs and, for
+// block 0, the per-expert counts, offsets and chunk list.  counts(e, &pre,
+// &tot) gives expert e's rows in earlier blocks and in all blocks; rank(p)
+// the rank of pair p among its expert's rows in its block.
+template <class Counts, class Rank>
+__device__ __forceinline__ void sched_finish_block(const KArgs& a, int b, Counts counts,
+                                                   Rank rank) {
   __shared__ int s_pre[kMaxExperts];   // rows of e in earlier blocks
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_tot[kMaxExperts];
   __shared__ int s_ch[kMaxExperts + 1];
   __shared__ int s_wsum[2][8];
-  const int T = a.d.T, k = a.d.k, E = a.d.E, b = blockIdx.x, tid = threadIdx.x;
+  const int T = a.d.T, k = a.d.k, E = a.d.E, tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   int tot = 0, chs = 0;
-  pdl_wait();
-  pdl_trigger();
   if (tid < E) {
-    int pre = 0, rest = 0;
-    // unrolled so the blocks' counts are loaded several at a time
-#pragma unroll 8
-    for (int bb = 0; bb < b; ++bb) pre += __ldg(blk_cnt + (size_t)bb * E + tid);
-#pragma unroll 8
-    for (int bb = b; bb < nb; ++bb) rest += __ldg(blk_cnt + (size_t)bb * E + tid);
+    int pre = 0;
+    counts(tid, &pre, &tot);
     s_pre[tid] = pre;
-    tot = pre + rest;
     s_tot[tid] = tot;
     chs = (tot + kChunk - 1) / kChunk;
   }
@@ -228,8 +227,8 @@ __global__ void __launch_bounds__(256) k_sched_finish(KArgs a, const int* __rest
   __syncthreads();
   const int p0 = b * kSchedRows * k, np = min(kSchedRows, T - b * kSchedRows) * k;
   for (int i = tid; i < np; i += 256) {
-    const int p = p0 + i, e = __ldg(a.w.idx + p);
-    const int slot = s_off[e] + s_pre[e] + rank[p];
+    const int p = p0 + i, e = a.w.idx[p];
+    const int slot = s_off[e] + s_pre[e] + rank(p);
     a.w.pair_of_slot[slot] = p;
     a.w.slot_of_pair[p] = slot;
   }
@@ -252,10 +251,63 @@ __global__ void __launch_bounds__(256) k_sched_finish(KArgs a, const int* __rest
   }
 }
 
+__global__ void __launch_bounds__(256) k_sched_finish(KArgs a, const int* __restrict__ rank,
+                                                      const int* __restrict__ blk_cnt, int nb) {
+  const int b = blockIdx.x, E = a.d.E;
+  pdl_wait();
+  pdl_trigger();
+  sched_finish_block(
+      a, b,
+      [&](int e, int* pre, int* tot) {
+        int p = 0, rest = 0;
+        // unrolled so the blocks' counts are loaded several at a time
+#pragma unroll 8
+        for (int bb = 0; bb < b; ++bb) p += __ldg(blk_cnt + (size_t)bb * E + e);
+#pragma unroll 8
+        for (int bb = b; bb < nb; ++bb) rest += __ldg(blk_cnt + (size_t)bb * E + e);
+        *pre = p;
+        *tot = p + rest;
+      },
+      [&](int p) { return rank[p]; });
+}
+
+// Up to kSchedRows rows (one block): counting and finishing in one CTA, the
+// block's bitmap kept in shared memory, one launch instead of two.
+__global__ void __launch_bounds__(256) k_sched_one(KArgs a) {
+  __shared__ uint32_t bm[kMaxExperts][kSchedRows / 32];
+  const int T = a.d.T, k = a.d.k, E = a.d.E, tid = threadIdx.x;
+  for (int i = tid; i < E * (kSchedRows / 32); i += 256) (&bm[0][0])[i] = 0u;
+  pdl_wait();
+  pdl_trigger();
+  __syncthreads();
+  const int np = T * k;
+  for (int i = tid; i < np; i += 256) {
+    const int tl = i / k, e = a.w.idx[i];
+    atomicOr(&bm[e][tl >> 5], 1u << (tl & 31));
+  }
+  __syncthreads();
+  sched_finish_block(
+      a, 0,
+      [&](int e, int* pre, int* tot) {
+        int c = 0;
+#pragma unroll
+        for (int w = 0; w < kSchedRows / 32; ++w) c += __popc(bm[e][w]);
+        *pre = 0;
+        *tot = c;
+      },
+      [&](int p) {
+        const int tl = p / k, e = a.w.idx[p];
+        int r = __popc(bm[e][tl >> 5] & ((1u << (tl & 31)) - 1u));
+        for (int w = 0; w < (tl >> 5); ++w) r += __popc(bm[e][w]);
+        return r;
+      });
+}
+
 cudaError_t setup_schedule() { return cudaSuccess; }
 
 cudaError_t launch_schedule(const KArgs& a, cudaStream_t s, bool pdl) {
   const int nb = (a.d.T + kSchedRows - 1) / kSchedRows;
+  if (nb == 1) return launch_pdl(k_sched_one, dim3(1), dim3(256), 0, s, pdl, a);
   int* rank = a.w.sched_rank;
   int* blk = a.w.sched_blk;
   cudaError_t e = launch_pdl(k_sched_count, dim3(nb), dim3(256), 0, s, pdl, a, rank, blk);

@@ -80,8 +80,8 @@ struct DevWork {
   int* done;            // [12] barrier counters (self-resetting) and the decode launch tag
   unsigned long long* tlog;  // [kDecodeRows][E] decode logits as {launch tag, value} words
   unsigned long long* xw;  // decode exchange words: [16k][I] h, [16k][H] d, [16][Is] hs, [16][H] ds
-  int* sched_rank;      // [T*k] rank of each pair among its expert's rows in its 256-row block
-  int* sched_blk;       // [ceil(T/256)][E] rows per expert in each 256-row block
+  int* sched_rank;      // [T*k] rank of each pair among its expert's rows in its 128-row block
+  int* sched_blk;       // [ceil(T/128)][E] rows per expert in each 128-row block
 };
 
 // The residual add + RMS norm in front of the layer, when a forward takes
