@@ -59,8 +59,10 @@ __global__ void __launch_bounds__(kAnThreads, 8 / NC)
   const uint4* rr = reinterpret_cast<const uint4*>(residual + row);
   const uint4* xr = reinterpret_cast<const uint4*>(x + row);
 
-  // every chunk's loads first, then residual + x rounded to bf16 (the new
-  // residual stream), kept packed
+  // every chunk's loads first (once the previous kernel, which may have
+  // written the inputs, has completed), then residual + x rounded to bf16
+  // (the new residual stream), kept packed
+  pdl_wait();
   uint4 ra[NC], xa[NC];
 #pragma unroll
   for (int j = 0; j < NC; ++j) {
@@ -70,6 +72,7 @@ __global__ void __launch_bounds__(kAnThreads, 8 / NC)
       xa[j] = __ldcs(xr + c);
     }
   }
+  pdl_trigger();  // the next kernel's prologue may overlap the rest
   uint4 hp[NC];
   float ss = 0.0f;
 #pragma unroll
@@ -140,18 +143,13 @@ __global__ void __launch_bounds__(kAnThreads, 8 / NC)
 
 cudaError_t launch_add_rmsnorm_quant(const bf16* residual, const bf16* x, const bf16* gamma,
                                      float eps, int rows, int H, bf16* h_out, bf16* xn_out,
-                                     uint8_t* codes, float* scales, cudaStream_t s) {
+                                     uint8_t* codes, float* scales, cudaStream_t s, bool pdl) {
   const int nch = H / 8;
-  if (nch <= kAnThreads)
-    k_add_rmsnorm_quant<1><<<rows, kAnThreads, 0, s>>>(residual, x, gamma, eps, H, h_out,
-                                                       xn_out, codes, scales);
-  else if (nch <= 2 * kAnThreads)
-    k_add_rmsnorm_quant<2><<<rows, kAnThreads, 0, s>>>(residual, x, gamma, eps, H, h_out,
-                                                       xn_out, codes, scales);
-  else
-    k_add_rmsnorm_quant<4><<<rows, kAnThreads, 0, s>>>(residual, x, gamma, eps, H, h_out,
-                                                       xn_out, codes, scales);
-  return cudaGetLastError();
+  auto* kernel = nch <= kAnThreads       ? k_add_rmsnorm_quant<1>
+                 : nch <= 2 * kAnThreads ? k_add_rmsnorm_quant<2>
+                                         : k_add_rmsnorm_quant<4>;
+  return launch_pdl(kernel, dim3(rows), dim3(kAnThreads), 0, s, pdl, residual, x, gamma, eps, H,
+                    h_out, xn_out, codes, scales);
 }
 
 }  // namespace moe

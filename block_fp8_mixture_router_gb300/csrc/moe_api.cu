@@ -840,7 +840,7 @@ int moe_add_rmsnorm_quantize(moe_ctx* c, const void* residual, const void* x, co
   if (launch_add_rmsnorm_quant(static_cast<const bf16*>(residual), static_cast<const bf16*>(x),
                                static_cast<const bf16*>(gamma), eps, rows, H,
                                static_cast<bf16*>(h_out), static_cast<bf16*>(xn_out), codes,
-                               scales, s) != cudaSuccess)
+                               scales, s, c->opt_pdl != 0) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -888,7 +888,8 @@ int moe_forward_addnorm(moe_ctx* c, const void* residual, const void* x, const v
   bf16* xn = xn_out ? static_cast<bf16*>(xn_out) : c->stage_x;
   if (launch_add_rmsnorm_quant(static_cast<const bf16*>(residual), static_cast<const bf16*>(x),
                                static_cast<const bf16*>(gamma), eps, rows, H,
-                               static_cast<bf16*>(h_out), xn, c->w.xq, c->w.sx, s) != cudaSuccess)
+                               static_cast<bf16*>(h_out), xn, c->w.xq, c->w.sx, s,
+                               c->opt_pdl != 0) != cudaSuccess)
     return MOE_ERR_CUDA;
   return run_forward(c, xn, y, rows, s, nullptr, true);
 }
