@@ -303,8 +303,10 @@ def test_path_option_range(t11_case):
     assert m.moe_set_option(t11_case.moe.ctx, m.MOE_OPT_PATH, m.PATH_AUTO) == m.MOE_OK
 
 
-@pytest.mark.parametrize("rows", [2, 4, 5, 6, 16, 17, 64, 255])
+@pytest.mark.parametrize("rows", [2, 3, 4, 5, 6, 15, 16, 17, 64, 128, 129, 255, 1023])
 def test_ragged_rows(full_case, rows):
+    """Both sides of every automatic path boundary (1 | 2..4 | 5..), of the
+    one-block schedule (up to 128 rows) and of the token tiles."""
     x = full_case.x(rows, tag=f"r{rows}")
     sample = sorted(set([0, rows - 1] + list(range(0, rows, max(1, rows // 6)))))
     run_and_check(full_case, x, sample_rows=sample)
