@@ -43,7 +43,7 @@ EXPORTED = ("moe_create", "moe_load_weights", "moe_forward", "moe_forward_host",
             "moe_last_device_status", "moe_destroy", "moe_status_string",
             "moe_profile_forward", "moe_route_static", "moe_add_rmsnorm_quantize",
             "moe_forward_codes", "moe_forward_addnorm", "moe_chain_create",
-            "moe_chain_forward", "moe_chain_destroy")
+            "moe_chain_forward", "moe_chain_destroy", "moe_debug_poison_workspace")
 
 MOE_ROUTE_STATIC_MAX_LOGITS = 262144
 
@@ -96,6 +96,7 @@ def load_library(path: str = LIB_PATH):
     L.moe_chain_destroy.argtypes = [vp]
     L.moe_chain_destroy.restype = None
     L.moe_set_option.argtypes = [vp, i, i]
+    L.moe_debug_poison_workspace.argtypes = [vp, i, vp]
     L.moe_profile_forward.argtypes = [vp, vp, vp, i, vp, vp, i, ctypes.POINTER(ctypes.c_int), vp]
     L.moe_required_bytes.argtypes = [ctypes.POINTER(moe_config), ctypes.POINTER(ctypes.c_size_t)]
     L.moe_last_device_status.argtypes = [vp]
@@ -149,6 +150,12 @@ def moe_forward(ctx, x, y, rows: int, stream=None) -> int:
 
 def moe_forward_host(ctx, x, y, rows: int, stream=None) -> int:
     return load_library().moe_forward_host(ctx, _ptr(x), _ptr(y), rows, _stream(stream))
+
+
+def moe_debug_poison_workspace(ctx, byte: int, stream=None) -> int:
+    """Fills the context's data workspace with `byte` (a test of the
+    kernels' independence from earlier calls' leftovers)."""
+    return load_library().moe_debug_poison_workspace(ctx, byte, _stream(stream))
 
 
 def moe_route(ctx, x, rows: int, idx, w, stream=None) -> int:
@@ -327,6 +334,9 @@ class MoELayer:
             y = torch.empty_like(x)
         _check(moe_forward_host(self.ctx, x, y, x.shape[0], stream), "moe_forward_host")
         return y
+
+    def poison_workspace(self, byte: int = 0xFF, stream=None):
+        _check(moe_debug_poison_workspace(self.ctx, byte, stream), "moe_debug_poison_workspace")
 
     def route(self, x: torch.Tensor, stream=None):
         T = x.shape[0]

@@ -33,6 +33,9 @@ struct moe_ctx {
   size_t rows_smem = 0;    // 2..16-row decode kernel: shared memory per CTA, 0 = unavailable
   cudaStream_t last_stream = nullptr;
   std::vector<void*> allocs;
+  // the value buffers of the workspace: every byte a forward reads from them
+  // it wrote earlier in the same call (moe_debug_poison_workspace fills them)
+  std::vector<std::pair<void*, size_t>> data_regions;
   DevLayer L{};
   DevWork w{};
   bf16* stage_x = nullptr;
@@ -561,6 +564,10 @@ int moe_create(const moe_config* cfg, int device, moe_ctx** out) {
     }
     c->allocs.push_back(ptrs[i]);
   }
+  // (values only: logits, weights, codes, scales, activations, outputs.  The
+  // index arrays are left out: a wrong value there is a wrong address.)
+  for (int i : {8, 10, 11, 12, 13, 22, 23, 24, 26, 27, 28, 30, 31, 33, 34, 36})
+    c->data_regions.emplace_back(ptrs[i], plan.sizes[i]);
   c->L.w13 = (const uint8_t*)ptrs[0];
   c->L.s13 = (const float*)ptrs[1];
   c->L.w2 = (const uint8_t*)ptrs[2];
@@ -1121,6 +1128,21 @@ void moe_chain_destroy(moe_chain* ch) {
     cudaFree(ch->table);
   }
   delete ch;
+}
+
+int moe_debug_poison_workspace(moe_ctx* c, int byte, void* stream) {
+  if (!c || byte < 0 || byte > 255) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(c->device);
+  if (!guard.ok) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  c->last_stream = s;
+  for (const auto& r : c->data_regions)
+    if (cudaMemsetAsync(r.first, byte, r.second, s) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+  c->fwd_rows = 0;  // the workspace no longer holds a forward's codes
+  return MOE_OK;
 }
 
 void moe_destroy(moe_ctx* c) {

@@ -194,6 +194,17 @@ int moe_route(moe_ctx* ctx, const void* x, int rows, int32_t* idx, float* w, voi
 int moe_route_static(const void* x, const float* router, int rows, int hidden, int n_experts,
                      int top_k, int32_t* idx, float* w, void* stream);
 
+/* Fills the value buffers of the context's workspace with `byte` (0..255):
+ * every buffer of values that a forward reads only after writing them in the
+ * same call (logits, routing weights, activation and SwiGLU codes and their
+ * scales, expert outputs, staging rows).  Index arrays (routing, schedule),
+ * weights, counters, launch tags and the status word are left alone.  A forward after it gives the same bits as before it: a check that
+ * no kernel depends on what an earlier call left behind (0xFF makes every
+ * bf16, fp32 and e4m3 value there a NaN).  Asynchronous on `stream`.
+ * A test entry point; the pages that define the layer have no counterpart
+ * to it. */
+int moe_debug_poison_workspace(moe_ctx* ctx, int byte, void* stream);
+
 /* Activation quantisation only: codes e4m3 [rows][H] and scales fp32
  * [rows][H/128], both device pointers.  Asynchronous.  This launches the
  * row quantisation kernel of the warp-MMA prompt path; every forward kernel

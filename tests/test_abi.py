@@ -124,12 +124,12 @@ def _declaration_comments():
 def test_every_declaration_cites_its_defining_passage():
     """Each entry point's comment names the passage of the pages that defines
     the operation; the allocation-free router says the pages have no
-    counterpart instead."""
+    counterpart instead, as does the workspace-poisoning test entry."""
     comments = _declaration_comments()
     assert set(comments) == set(declared_functions())
     for name, text in comments.items():
         flat = " ".join(text.split())
-        if name == "moe_route_static":
+        if name in ("moe_route_static", "moe_debug_poison_workspace"):
             assert "no counterpart" in flat, name
             assert "Defined by:" not in flat, name
             continue
