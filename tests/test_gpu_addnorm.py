@@ -118,9 +118,10 @@ def test_addnorm_tiny(tiny_ctx, rows):
     check_addnorm(tiny_ctx, r, x, g, 1e-5, out)
 
 
-@pytest.mark.parametrize("hidden", [4096, 8192])
+@pytest.mark.parametrize("hidden", [2560, 3072, 4096, 6144, 8192])
 def test_addnorm_wide_rows(dev, hidden):
-    """Rows wider than 2048 take two or four chunks per thread (a context with
+    """Rows wider than 2048 take two or four chunks per thread; 2560, 3072
+    and 6144 leave the last chunk slot of some threads idle (a context with
     no weights: the add-norm needs none, so only the oracle is compared)."""
     shape = W.MoEShape(hidden=hidden, n_experts=16, top_k=4, inter=128, shared_inter=128)
     ctx = _ctx(shape, dev, load=False)
