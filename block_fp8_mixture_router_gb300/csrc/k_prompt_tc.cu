@@ -1,5 +1,6 @@
-// Prompt path (rows > 16): the expert GEMMs on the fifth-generation tensor
-// cores (tcgen05.mma with TMEM accumulators, operands staged by TMA).
+// Grouped path (five rows or more on the automatic path): the expert GEMMs on
+// the fifth-generation tensor cores (tcgen05.mma with TMEM accumulators,
+// operands staged by TMA).
 //
 // Expert arithmetic: PR #939 "Fish Audio Drama 3 text to speech on one CUDA
 // GPU", section "Precision" (block-FP8 weights with one fp32 scale per
@@ -728,49 +729,82 @@ const void* kernel_of(int kind) {
 // ---- activation quantisation straight into (expert, row) slot order --------
 // One CTA per row: quantise x[t] in 1 x 128 groups (as quant_row_and_gate),
 // write the codes and scales to each of the row's k slots, and gamma[t].
-__global__ void __launch_bounds__(256) k_quant_scatter(KArgs a, uint8_t* xg, float* sxg) {
+// One CTA per row t, 256 threads, each 8 consecutive elements per pass (a
+// 1 x 128 group is a half-warp): the row's codes and group scales are
+// written to its k slots.  The row's first pass is loaded before the slot
+// numbers are looked up, so the two reads overlap.
+constexpr int kQsThreads = 256;
+constexpr int kQsPass = 8 * kQsThreads;  // elements of a row per pass
+
+__device__ __forceinline__ float amax8(const uint4 r) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    m = fmaxf(m, fmaxf(fabsf(__low2float(p)), fabsf(__high2float(p))));
+  }
+  return m;
+}
+
+__global__ void __launch_bounds__(kQsThreads, 5) k_quant_scatter(KArgs a, uint8_t* xg, float* sxg) {
   __shared__ int slots[kMaxTopK];
-  __shared__ float red[8];
+  __shared__ float red[kQsThreads / 32];
   const int t = blockIdx.x, H = a.d.H, k = a.d.k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ngroups = H / kGroup;
+  const bf16* xr = a.x + (size_t)t * H;
+  const bool pre_q = a.an.pre_q != 0;  // the add-norm already wrote the row's codes
+  // the shared gate's weights (immutable) before the wait
+  const int base0 = 8 * threadIdx.x;
+  uint4 graw = make_uint4(0u, 0u, 0u, 0u);
+  if (base0 < H) graw = __ldg(reinterpret_cast<const uint4*>(a.L.gate + base0));
   pdl_wait();
   pdl_trigger();
+  uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+  if (base0 < H) raw = *reinterpret_cast<const uint4*>(xr + base0);
   if (threadIdx.x < k) slots[threadIdx.x] = a.w.slot_of_pair[t * k + threadIdx.x];
   __syncthreads();
-  const bf16* xr = a.x + (size_t)t * H;
-  const int ngroups = H / kGroup;
-  const bool pre_q = a.an.pre_q != 0;  // the add-norm already wrote the row's codes
   const float rs = (a.d.per_row && !pre_q) ? row_scale(xr, H, red) : 0.0f;
-  // the shared gate's dot product from the same registers as the codes
-  float acc = 0.0f;
-  for (int gi = warp; gi < ngroups; gi += 8) {
-    const int base = gi * kGroup + 4 * lane;
-    const uint2 raw = *reinterpret_cast<const uint2*>(xr + base);
-    const uint2 graw = *reinterpret_cast<const uint2*>(a.L.gate + base);
-    const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-    const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-    const __nv_bfloat162 g0 = *reinterpret_cast<const __nv_bfloat162*>(&graw.x);
-    const __nv_bfloat162 g1 = *reinterpret_cast<const __nv_bfloat162*>(&graw.y);
-    const float v0 = __low2float(p0), v1 = __high2float(p0), v2 = __low2float(p1),
-                v3 = __high2float(p1);
-    acc = fmaf(v0, __low2float(g0), acc);
-    acc = fmaf(v1, __high2float(g0), acc);
-    acc = fmaf(v2, __low2float(g1), acc);
-    acc = fmaf(v3, __high2float(g1), acc);
-    uint32_t packed;
+  float acc = 0.0f;  // the shared gate's dot product from the same registers
+  for (int base = base0; base < H; base += kQsPass) {
+    if (base != base0) {
+      raw = *reinterpret_cast<const uint4*>(xr + base);
+      graw = __ldg(reinterpret_cast<const uint4*>(a.L.gate + base));
+    }
+    const uint32_t xw[4] = {raw.x, raw.y, raw.z, raw.w};
+    const uint32_t gw[4] = {graw.x, graw.y, graw.z, graw.w};
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&xw[i]);
+      const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(&gw[i]);
+      v[2 * i] = __low2float(p);
+      v[2 * i + 1] = __high2float(p);
+      acc = fmaf(v[2 * i], __low2float(g), acc);
+      acc = fmaf(v[2 * i + 1], __high2float(g), acc);
+    }
+    const int gi = base / kGroup;
+    uint2 packed;
     float s;
     if (pre_q) {
-      packed = *reinterpret_cast<const uint32_t*>(a.w.xq + (size_t)t * H + base);
+      packed = *reinterpret_cast<const uint2*>(a.w.xq + (size_t)t * H + base);
       s = a.w.sx[(size_t)t * ngroups + gi];
     } else {
-      float m = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
-      m = warp_max(m);
+      // a pass covers whole groups (H % 128 == 0), so whole half-warps take
+      // part in it
+      const unsigned half = 0xFFFFu << (lane & 16);
+      float m = amax8(raw);
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
       s = a.d.per_row ? rs : group_scale(m);
-      packed = quant4(v0, v1, v2, v3, s);
+      packed.x = quant4(v[0], v[1], v[2], v[3], s);
+      packed.y = quant4(v[4], v[5], v[6], v[7], s);
     }
     for (int j = 0; j < k; ++j) {
-      *reinterpret_cast<uint32_t*>(xg + (size_t)slots[j] * H + base) = packed;
-      if (lane == 0) sxg[(size_t)slots[j] * ngroups + gi] = s;
+      const size_t sl = (size_t)slots[j];
+      *reinterpret_cast<uint2*>(xg + sl * H + base) = packed;
+      if ((lane & 15) == 0) sxg[sl * ngroups + gi] = s;
     }
   }
   acc = warp_sum(acc);
@@ -778,7 +812,7 @@ __global__ void __launch_bounds__(256) k_quant_scatter(KArgs a, uint8_t* xg, flo
   __syncthreads();
   if (threadIdx.x == 0) {
     float v = 0.0f;
-    for (int w = 0; w < 8; ++w) v += red[w];
+    for (int w = 0; w < kQsThreads / 32; ++w) v += red[w];
     a.w.gamma[t] = sigmoid_f32(v);
   }
 }
@@ -891,7 +925,7 @@ cudaError_t launch_quant_h_rows(const float* hf, uint8_t* hq, float* sh, int n_r
 
 cudaError_t launch_quant_scatter(const KArgs& a, uint8_t* xg, float* sxg, cudaStream_t s,
                                  bool pdl) {
-  return launch_pdl(k_quant_scatter, dim3(a.d.T), dim3(256), 0, s, pdl, a, xg, sxg);
+  return launch_pdl(k_quant_scatter, dim3(a.d.T), dim3(kQsThreads), 0, s, pdl, a, xg, sxg);
 }
 
 // Tensor map of a row-major 2-D array [rows][cols] (element size `esize`),

@@ -259,14 +259,22 @@ __global__ void __launch_bounds__(256) k_sched_finish(KArgs a, const int* __rest
   sched_finish_block(
       a, b,
       [&](int e, int* pre, int* tot) {
-        int p = 0, rest = 0;
-        // unrolled so the blocks' counts are loaded several at a time
-#pragma unroll 8
-        for (int bb = 0; bb < b; ++bb) p += __ldg(blk_cnt + (size_t)bb * E + e);
-#pragma unroll 8
-        for (int bb = b; bb < nb; ++bb) rest += __ldg(blk_cnt + (size_t)bb * E + e);
+        // the blocks' counts 32 at a time: all loads of a batch are in
+        // flight before its sums (integer sums: any order gives the same)
+        int p = 0, tot_e = 0;
+        for (int b0 = 0; b0 < nb; b0 += 32) {
+          int v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            v[j] = b0 + j < nb ? __ldg(blk_cnt + (size_t)(b0 + j) * E + e) : 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            p += b0 + j < b ? v[j] : 0;
+            tot_e += v[j];
+          }
+        }
         *pre = p;
-        *tot = p + rest;
+        *tot = tot_e;
       },
       [&](int p) { return rank[p]; });
 }
