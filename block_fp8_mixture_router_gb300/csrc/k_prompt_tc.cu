@@ -726,152 +726,7 @@ const void* kernel_of(int kind) {
   }
 }
 
-// ---- activation quantisation straight into (expert, row) slot order --------
-// One CTA per row: quantise x[t] in 1 x 128 groups (as quant_row_and_gate),
-// write the codes and scales to each of the row's k slots, and gamma[t].
-// One CTA per row t, 256 threads, each 8 consecutive elements per pass (a
-// 1 x 128 group is a half-warp): the row's codes and group scales are
-// written to its k slots.  The row's first pass is loaded before the slot
-// numbers are looked up, so the two reads overlap.
-constexpr int kQsThreads = 256;
-constexpr int kQsPass = 8 * kQsThreads;  // elements of a row per pass
-
-__device__ __forceinline__ float amax8(const uint4 r) {
-  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-  float m = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-    m = fmaxf(m, fmaxf(fabsf(__low2float(p)), fabsf(__high2float(p))));
-  }
-  return m;
-}
-
-__global__ void __launch_bounds__(kQsThreads, 5) k_quant_scatter(KArgs a, uint8_t* xg, float* sxg) {
-  __shared__ int slots[kMaxTopK];
-  __shared__ float red[kQsThreads / 32];
-  const int t = blockIdx.x, H = a.d.H, k = a.d.k;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int ngroups = H / kGroup;
-  const bf16* xr = a.x + (size_t)t * H;
-  const bool pre_q = a.an.pre_q != 0;  // the add-norm already wrote the row's codes
-  // the shared gate's weights (immutable) before the wait
-  const int base0 = 8 * threadIdx.x;
-  uint4 graw = make_uint4(0u, 0u, 0u, 0u);
-  if (base0 < H) graw = __ldg(reinterpret_cast<const uint4*>(a.L.gate + base0));
-  pdl_wait();
-  pdl_trigger();
-  uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-  if (base0 < H) raw = *reinterpret_cast<const uint4*>(xr + base0);
-  if (threadIdx.x < k) slots[threadIdx.x] = a.w.slot_of_pair[t * k + threadIdx.x];
-  __syncthreads();
-  const float rs = (a.d.per_row && !pre_q) ? row_scale(xr, H, red) : 0.0f;
-  float acc = 0.0f;  // the shared gate's dot product from the same registers
-  for (int base = base0; base < H; base += kQsPass) {
-    if (base != base0) {
-      raw = *reinterpret_cast<const uint4*>(xr + base);
-      graw = __ldg(reinterpret_cast<const uint4*>(a.L.gate + base));
-    }
-    const uint32_t xw[4] = {raw.x, raw.y, raw.z, raw.w};
-    const uint32_t gw[4] = {graw.x, graw.y, graw.z, graw.w};
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&xw[i]);
-      const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(&gw[i]);
-      v[2 * i] = __low2float(p);
-      v[2 * i + 1] = __high2float(p);
-      acc = fmaf(v[2 * i], __low2float(g), acc);
-      acc = fmaf(v[2 * i + 1], __high2float(g), acc);
-    }
-    const int gi = base / kGroup;
-    uint2 packed;
-    float s;
-    if (pre_q) {
-      packed = *reinterpret_cast<const uint2*>(a.w.xq + (size_t)t * H + base);
-      s = a.w.sx[(size_t)t * ngroups + gi];
-    } else {
-      // a pass covers whole groups (H % 128 == 0), so whole half-warps take
-      // part in it
-      const unsigned half = 0xFFFFu << (lane & 16);
-      float m = amax8(raw);
-#pragma unroll
-      for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
-      s = a.d.per_row ? rs : group_scale(m);
-      packed.x = quant4(v[0], v[1], v[2], v[3], s);
-      packed.y = quant4(v[4], v[5], v[6], v[7], s);
-    }
-    for (int j = 0; j < k; ++j) {
-      const size_t sl = (size_t)slots[j];
-      *reinterpret_cast<uint2*>(xg + sl * H + base) = packed;
-      if ((lane & 15) == 0) sxg[sl * ngroups + gi] = s;
-    }
-  }
-  acc = warp_sum(acc);
-  if (lane == 0) red[warp] = acc;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float v = 0.0f;
-    for (int w = 0; w < kQsThreads / 32; ++w) v += red[w];
-    a.w.gamma[t] = sigmoid_f32(v);
-  }
-}
-
-// ---- SwiGLU rows with one scale per row ---------------------------------------
-// One warp per slot: the row's amax over its I fp32 values, one scale, and the
-// e4m3 codes of every value (rows of hf [slots][I] -> hq [slots][I], and the
-// row's scale in each of its I/128 entries of sh).
-__global__ void __launch_bounds__(256) k_quant_h_rows(const float* __restrict__ hf,
-                                                      uint8_t* __restrict__ hq,
-                                                      float* __restrict__ sh, int n_rows, int I) {
-  const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  pdl_wait();
-  pdl_trigger();
-  if (r >= n_rows) return;
-  const float* row = hf + (size_t)r * I;
-  float m = 0.0f;
-  for (int c = 4 * lane; c < I; c += 128) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(row + c));
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-  }
-  const float s = group_scale(warp_max(m));
-  for (int c = 4 * lane; c < I; c += 128) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(row + c));
-    *reinterpret_cast<uint32_t*>(hq + (size_t)r * I + c) = quant4(v.x, v.y, v.z, v.w, s);
-  }
-  for (int g = lane; g < I / kGroup; g += 32) sh[(size_t)r * (I / kGroup) + g] = s;
-}
-
-// Router weights as three bf16 parts, w = hi + mid + lo exactly (each part
-// rounds the remainder of the previous ones; a float's 24 significant bits
-// fit in three 8-bit ones).  With bf16 x every product x * part is exact in
-// fp32, so the tensor-core GEMM over [hi | mid | lo] gives fp32 logits.
-// out [Epad][3H]; rows E..Epad-1 are zero.
-__global__ void k_split_router(const float* __restrict__ wr, bf16* __restrict__ out, int E,
-                               int Epad, int H) {
-  const size_t n = (size_t)Epad * H;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const int e = (int)(i / H), c = (int)(i % H);
-    const float w = e < E ? wr[(size_t)e * H + c] : 0.0f;
-    const bf16 hi = __float2bfloat16_rn(w);
-    const float r1 = w - __bfloat162float(hi);
-    const bf16 mid = __float2bfloat16_rn(r1);
-    const bf16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
-    bf16* row = out + (size_t)e * 3 * H;
-    row[c] = hi;
-    row[H + c] = mid;
-    row[2 * H + c] = lo;
-  }
-}
-
 }  // namespace
-
-cudaError_t launch_split_router(const float* wr, bf16* out, int E, int Epad, int H,
-                                cudaStream_t s) {
-  k_split_router<<<1024, 256, 0, s>>>(wr, out, E, Epad, H);
-  return cudaGetLastError();
-}
 
 int tc_gemm_tile_rows(int kind) {
   switch (kind) {
@@ -914,18 +769,6 @@ cudaError_t launch_tc_gemm(int kind, const TcGemm& g, int grid, size_t smem, cud
   cfg.numAttrs = pdl ? 1 : 0;
   const cudaError_t e = cudaLaunchKernelExC(&cfg, kernel_of(kind), args);
   return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-cudaError_t launch_quant_h_rows(const float* hf, uint8_t* hq, float* sh, int n_rows, int I,
-                                cudaStream_t s, bool pdl) {
-  if (n_rows < 1) return cudaSuccess;
-  return launch_pdl(k_quant_h_rows, dim3((n_rows + 7) / 8), dim3(256), 0, s, pdl, hf, hq, sh,
-                    n_rows, I);
-}
-
-cudaError_t launch_quant_scatter(const KArgs& a, uint8_t* xg, float* sxg, cudaStream_t s,
-                                 bool pdl) {
-  return launch_pdl(k_quant_scatter, dim3(a.d.T), dim3(kQsThreads), 0, s, pdl, a, xg, sxg);
 }
 
 // Tensor map of a row-major 2-D array [rows][cols] (element size `esize`),
