@@ -14,13 +14,16 @@ namespace moe {
 namespace {
 
 // ---- activation quantisation straight into (expert, row) slot order --------
-// One CTA per row t, 256 threads, each 8 consecutive elements per pass (a
-// 1 x 128 group is a half-warp): x[t] quantised in 1 x 128 groups (as
-// quant_row_and_gate), its codes and group scales written to each of the
-// row's k slots, and gamma[t] from the same registers.  The row's first pass
-// is loaded before the slot numbers are looked up, so the two reads overlap.
+// Two rows per CTA of 256 threads, 128 threads per row, each 16 consecutive
+// elements per pass (a 1 x 128 group is 8 threads): x[t] quantised in 1 x 128
+// groups (as quant_row_and_gate), its codes (16 bytes per thread) and group
+// scales written to each of the row's k slots, and gamma[t] from the same
+// registers.  Every thread reads the slot numbers itself, so no barrier
+// stands between the row's loads and its stores.
 constexpr int kQsThreads = 256;
-constexpr int kQsPass = 8 * kQsThreads;  // elements of a row per pass
+constexpr int kQsRowThreads = 128;           // threads per row
+constexpr int kQsRows = kQsThreads / kQsRowThreads;
+constexpr int kQsPass = 16 * kQsRowThreads;  // elements of a row per pass
 
 __device__ __forceinline__ float amax8(const uint4 r) {
   const uint32_t w[4] = {r.x, r.y, r.z, r.w};
@@ -33,72 +36,102 @@ __device__ __forceinline__ float amax8(const uint4 r) {
   return m;
 }
 
-__global__ void __launch_bounds__(kQsThreads, 5) k_quant_scatter(KArgs a, uint8_t* xg, float* sxg) {
-  __shared__ int slots[kMaxTopK];
+__global__ void __launch_bounds__(kQsThreads, 4) k_quant_scatter(KArgs a, uint8_t* xg, float* sxg) {
   __shared__ float red[kQsThreads / 32];
-  const int t = blockIdx.x, H = a.d.H, k = a.d.k;
+  const int T = a.d.T, H = a.d.H, k = a.d.k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int half = threadIdx.x / kQsRowThreads;  // which of the CTA's rows
+  const int t = blockIdx.x * kQsRows + half;
+  const bool active = t < T;
   const int ngroups = H / kGroup;
   const bf16* xr = a.x + (size_t)t * H;
   const bool pre_q = a.an.pre_q != 0;  // the add-norm already wrote the row's codes
   // the shared gate's weights (immutable) before the wait
-  const int base0 = 8 * threadIdx.x;
-  uint4 graw = make_uint4(0u, 0u, 0u, 0u);
-  if (base0 < H) graw = __ldg(reinterpret_cast<const uint4*>(a.L.gate + base0));
+  const int base0 = 16 * (threadIdx.x % kQsRowThreads);
+  uint4 g0 = make_uint4(0u, 0u, 0u, 0u), g1 = g0;
+  if (base0 < H) {
+    g0 = __ldg(reinterpret_cast<const uint4*>(a.L.gate + base0));
+    g1 = __ldg(reinterpret_cast<const uint4*>(a.L.gate + base0 + 8));
+  }
   pdl_wait();
   pdl_trigger();
-  uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-  if (base0 < H) raw = *reinterpret_cast<const uint4*>(xr + base0);
-  if (threadIdx.x < k) slots[threadIdx.x] = a.w.slot_of_pair[t * k + threadIdx.x];
-  __syncthreads();
-  const float rs = (a.d.per_row && !pre_q) ? row_scale(xr, H, red) : 0.0f;
+  uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
+  if (active && base0 < H) {
+    x0 = *reinterpret_cast<const uint4*>(xr + base0);
+    x1 = *reinterpret_cast<const uint4*>(xr + base0 + 8);
+  }
+  // one scale per row: the row's amax over its threads' warps
+  float rs = 0.0f;
+  if (a.d.per_row && !pre_q) {
+    float m = 0.0f;
+    if (active)
+      for (int base = base0; base < H; base += kQsPass)
+        m = fmaxf(m, fmaxf(amax8(*reinterpret_cast<const uint4*>(xr + base)),
+                           amax8(*reinterpret_cast<const uint4*>(xr + base + 8))));
+    m = warp_max(m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    constexpr int kRowWarps = kQsRowThreads / 32;
+    for (int w = 0; w < kRowWarps; ++w) rs = fmaxf(rs, red[half * kRowWarps + w]);
+    rs = group_scale(rs);
+    __syncthreads();  // red is free again
+  }
+  const int* slot_row = a.w.slot_of_pair + (size_t)t * k;
   float acc = 0.0f;  // the shared gate's dot product from the same registers
-  for (int base = base0; base < H; base += kQsPass) {
-    if (base != base0) {
-      raw = *reinterpret_cast<const uint4*>(xr + base);
-      graw = __ldg(reinterpret_cast<const uint4*>(a.L.gate + base));
-    }
-    const uint32_t xw[4] = {raw.x, raw.y, raw.z, raw.w};
-    const uint32_t gw[4] = {graw.x, graw.y, graw.z, graw.w};
-    float v[8];
+  if (active) {
+    for (int base = base0; base < H; base += kQsPass) {
+      if (base != base0) {
+        x0 = *reinterpret_cast<const uint4*>(xr + base);
+        x1 = *reinterpret_cast<const uint4*>(xr + base + 8);
+        g0 = __ldg(reinterpret_cast<const uint4*>(a.L.gate + base));
+        g1 = __ldg(reinterpret_cast<const uint4*>(a.L.gate + base + 8));
+      }
+      const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      float v[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&xw[i]);
-      const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(&gw[i]);
-      v[2 * i] = __low2float(p);
-      v[2 * i + 1] = __high2float(p);
-      acc = fmaf(v[2 * i], __low2float(g), acc);
-      acc = fmaf(v[2 * i + 1], __high2float(g), acc);
-    }
-    const int gi = base / kGroup;
-    uint2 packed;
-    float s;
-    if (pre_q) {
-      packed = *reinterpret_cast<const uint2*>(a.w.xq + (size_t)t * H + base);
-      s = a.w.sx[(size_t)t * ngroups + gi];
-    } else {
-      // a pass covers whole groups (H % 128 == 0), so whole half-warps take
-      // part in it
-      const unsigned half = 0xFFFFu << (lane & 16);
-      float m = amax8(raw);
+      for (int i = 0; i < 8; ++i) {
+        const __nv_bfloat162 p = *reinterpret_cast<const __nv_bfloat162*>(&xw[i]);
+        const __nv_bfloat162 g = *reinterpret_cast<const __nv_bfloat162*>(&gw[i]);
+        v[2 * i] = __low2float(p);
+        v[2 * i + 1] = __high2float(p);
+        acc = fmaf(v[2 * i], __low2float(g), acc);
+        acc = fmaf(v[2 * i + 1], __high2float(g), acc);
+      }
+      const int gi = base / kGroup;
+      uint4 packed;
+      float sc;
+      if (pre_q) {
+        packed = *reinterpret_cast<const uint4*>(a.w.xq + (size_t)t * H + base);
+        sc = a.w.sx[(size_t)t * ngroups + gi];
+      } else {
+        // a pass covers whole groups (H % 128 == 0), so the 8 threads of a
+        // group take part in it together
+        const unsigned grp = 0xFFu << (lane & 24);
+        float m = fmaxf(amax8(x0), amax8(x1));
 #pragma unroll
-      for (int o = 1; o < 16; o <<= 1) m = fmaxf(m, __shfl_xor_sync(half, m, o));
-      s = a.d.per_row ? rs : group_scale(m);
-      packed.x = quant4(v[0], v[1], v[2], v[3], s);
-      packed.y = quant4(v[4], v[5], v[6], v[7], s);
-    }
-    for (int j = 0; j < k; ++j) {
-      const size_t sl = (size_t)slots[j];
-      *reinterpret_cast<uint2*>(xg + sl * H + base) = packed;
-      if ((lane & 15) == 0) sxg[sl * ngroups + gi] = s;
+        for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(grp, m, o));
+        sc = a.d.per_row ? rs : group_scale(m);
+        packed.x = quant4(v[0], v[1], v[2], v[3], sc);
+        packed.y = quant4(v[4], v[5], v[6], v[7], sc);
+        packed.z = quant4(v[8], v[9], v[10], v[11], sc);
+        packed.w = quant4(v[12], v[13], v[14], v[15], sc);
+      }
+#pragma unroll 4
+      for (int j = 0; j < k; ++j) {
+        const size_t sl = (size_t)slot_row[j];
+        *reinterpret_cast<uint4*>(xg + sl * H + base) = packed;
+        if ((lane & 7) == 0) sxg[sl * ngroups + gi] = sc;
+      }
     }
   }
   acc = warp_sum(acc);
   if (lane == 0) red[warp] = acc;
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x % kQsRowThreads == 0 && active) {
+    constexpr int kRowWarps = kQsRowThreads / 32;
     float v = 0.0f;
-    for (int w = 0; w < kQsThreads / 32; ++w) v += red[w];
+    for (int w = 0; w < kRowWarps; ++w) v += red[half * kRowWarps + w];
     a.w.gamma[t] = sigmoid_f32(v);
   }
 }
@@ -168,7 +201,8 @@ cudaError_t launch_quant_h_rows(const float* hf, uint8_t* hq, float* sh, int n_r
 
 cudaError_t launch_quant_scatter(const KArgs& a, uint8_t* xg, float* sxg, cudaStream_t s,
                                  bool pdl) {
-  return launch_pdl(k_quant_scatter, dim3(a.d.T), dim3(kQsThreads), 0, s, pdl, a, xg, sxg);
+  return launch_pdl(k_quant_scatter, dim3((a.d.T + kQsRows - 1) / kQsRows), dim3(kQsThreads), 0,
+                    s, pdl, a, xg, sxg);
 }
 
 }  // namespace moe
