@@ -106,10 +106,21 @@ template <bool kRouted, int kN>
 __device__ __forceinline__ Item decode_item(const TcGemm& g, const int* s_pre, const int* s_off,
                                             const int* s_cnt, int w) {
   Item it;
-  const int wf = w / g.ksplit;
-  it.ks = w - wf * g.ksplit;
-  it.kb0 = (int)((long long)it.ks * g.n_k / g.ksplit);
-  it.kb1 = (int)((long long)(it.ks + 1) * g.n_k / g.ksplit);
+  // every role decodes every item, so this stays cheap: only the router
+  // splits K (the routed kinds never do), and its split bounds fit 32-bit
+  // products (K splits <= 16, K blocks well below 2^26)
+  int wf = w;
+  it.ks = 0;
+  it.kb0 = 0;
+  it.kb1 = g.n_k;
+  if constexpr (!kRouted) {
+    if (g.ksplit > 1) {
+      wf = w / g.ksplit;
+      it.ks = w - wf * g.ksplit;
+      it.kb0 = it.ks * g.n_k / g.ksplit;
+      it.kb1 = (it.ks + 1) * g.n_k / g.ksplit;
+    }
+  }
   const int tile = wf / g.n_f;
   it.f = wf - tile * g.n_f;
   if constexpr (kRouted) {
