@@ -351,6 +351,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
   constexpr int S = C::kStages, kN = C::kN, kCols = C::kCols, NB = C::kNumBuf;
   constexpr int kAcc = C::kAccCols;
   extern __shared__ uint8_t smem_raw[];
+  // block-FP8: the item whose scales scale slot s holds, decoded by the
+  // weight-tile TMA warp and published with the slot's barrier, so that the
+  // epilogue warps need not decode it again
+  __shared__ Item s_item[2];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* stages = base;
@@ -396,6 +400,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
     }
     tc::mbar_init(dfull, kEpiWarps);
     tc::mbar_init(dfree, kStoreWarps);
+    // an empty item in both slots: after a failed wait the epilogue may read
+    // a slot that no item was published to, and must then find no K blocks
+    for (int i = 0; i < 2; ++i) s_item[i] = Item{0, 0, 0, 0, 0, 0, 0};
     *s_abort = 0;
     tc::fence_barrier_init();
     tc::tma_prefetch_map(&g.a);
@@ -475,6 +482,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
         const ItemScales sc = item_scales(g, it);
         uint8_t* slot = sbs + sl * sbs_slot;
         if (lane == 0) {
+          s_item[sl] = it;  // published by the arrival below (release)
           tc::mbar_arrive_expect_tx(&sfull[sl], sc.s[0].bytes + sc.s[1].bytes + sc.s[2].bytes);
           bulk_copy_g2s(slot, reinterpret_cast<const uint8_t*>(g.sb) + sc.s[0].off, sc.s[0].bytes,
                         &sfull[sl]);
@@ -578,7 +586,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
     // After a failed wait the warps still walk every item (all later waits
     // give up at once), so each of them reaches every named barrier.
     for (int w = blockIdx.x, j = 0; w < n_items; w += gridDim.x, ++j) {
-      const Item it = decode_item<kRouted, kN>(g, s_pre, s_off, s_cnt, w);
+      // block-FP8: the item comes with its scale slot; the bf16 kinds decode it
+      Item it;
+      if constexpr (kF8) {
+        tc::wait_bounded(&sfull[j & 1], (j >> 1) & 1, s_abort, g.status);
+        it = s_item[j & 1];
+      } else {
+        it = decode_item<kRouted, kN>(g, s_pre, s_off, s_cnt, w);
+      }
       const int n16 = (it.n + 15) & ~15;
       // this item's scales in the slot: [token][n_k], and n_k per A tile
       const float* sc_tok = nullptr;
@@ -586,7 +601,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
       const float* s_wu = nullptr;
       if constexpr (kF8) {
         const int sl = j & 1;
-        tc::wait_bounded(&sfull[sl], (j >> 1) & 1, s_abort, g.status);
         const ItemScales sc = item_scales(g, it);
         const uint8_t* slot = sbs + sl * sbs_slot;
         epi_sync();  // every warp has left the previous item's K loop, pbuf's last reader
