@@ -608,12 +608,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_tc_gemm(const __grid_constant
         s_wg = reinterpret_cast<const float*>(slot + span_a + sc.s[1].lead);
         s_wu = reinterpret_cast<const float*>(slot + span_a + span_w + sc.s[2].lead);
         // (weight block scale x token scale) for every (tile, K block, token);
-        // padding tokens get 0
-        for (int i = 32 * ew + lane; i < n_k * kN; i += 32 * kEpiWarps) {
-          const int kb = i / kN, t = i - kb * kN;
-          const float st = t < it.n ? sc_tok[t * n_k + kb] : 0.0f;
-          pbuf[i] = s_wg[kb] * st;
-          pbuf[n_k * kN + i] = s_wu[kb] * st;
+        // padding tokens get 0.  With n_k % 4 == 0 the token scales are read
+        // as float4 rows (16-byte aligned then), four K blocks per thread,
+        // consecutive lanes on consecutive vectors: no bank conflicts on
+        // the reads, which a token-major walk (stride n_k) would have.
+        if ((n_k & 3) == 0) {
+          const int nq = n_k >> 2;
+          for (int v = 32 * ew + lane; v < kN * nq; v += 32 * kEpiWarps) {
+            const int t = v / nq, kq = v - t * nq;
+            const float4 s4 = t < it.n ? reinterpret_cast<const float4*>(sc_tok + t * n_k)[kq]
+                                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            const float st[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int kb = 4 * kq + r;
+              pbuf[kb * kN + t] = s_wg[kb] * st[r];
+              pbuf[(n_k + kb) * kN + t] = s_wu[kb] * st[r];
+            }
+          }
+        } else {
+          for (int i = 32 * ew + lane; i < n_k * kN; i += 32 * kEpiWarps) {
+            const int kb = i / kN, t = i - kb * kN;
+            const float st = t < it.n ? sc_tok[t * n_k + kb] : 0.0f;
+            pbuf[i] = s_wg[kb] * st;
+            pbuf[n_k * kN + i] = s_wu[kb] * st;
+          }
         }
         epi_sync();
       }
