@@ -26,8 +26,8 @@
 // stored token-major with coalesced rows.
 //
 // CTA roles (kTcThreads = 768 threads, 24 warps): warps 0 and 19 issue the
-// TMA copies (0: the weight tiles and the item's scales, 19: the token
-// tiles), warp 1 owns TMEM and issues the MMAs of the first A tile, warp 18
+// TMA copies (0: the weight tiles and the item's scales, with the decoded
+// item itself for the epilogue; 19: the token tiles), warp 1 owns TMEM and issues the MMAs of the first A tile, warp 18
 // those of the second A tile of a pair, warps 2-17 are the epilogue (warp w
 // reads TMEM lanes 32*(w%4).. and column quarter (w-2)/4 of the tile's
 // tokens).  Issuing an async copy, an MMA, a commit or a barrier wait costs
